@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 E4M3 packed-varlen attention hot path on GB300.
+
+One step = the whole hot path over one batch: fa_lp_quantize (amax pass, pack passes) followed by
+fa_lp_forward_varlen (the tcgen05 attention kernel), on synthetic BF16 inputs already resident in
+HBM. Default workload: one segment S=30272, H=56, D=128 (MiniMax-H3 shape), Q/K/V as strided views
+of one fused [T, 3, H, 128] buffer, N(0,1) BF16.
+
+Metric: TFLOPS = 4 * sum_s L_s^2 * H * D / step time (SGLang PR #40175's FLOP convention for
+non-causal attention, Speed Tests). Inputs (1.3 GB) and codes (0.65 GB) exceed the 129 MB L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+N > 1 (torchrun, one process per GPU): independent replicas of the full workload on every rank
+(the path has no exchange step), max-over-ranks time, weak scaling.
+--impl reference: the CPU oracle timed on the host cores over a bounded sample of the same
+workload (there is no installable reference implementation of this path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "E4M3 varlen attn TFLOPS at S=30272,H=56,D=128; % of FP8 tensor peak"
+UNIT = "TFLOPS"
+D = 128
+# dense FP8 / dense BF16 tensor rate of the part (nominal 4.5 / 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
+KERNELS_PER_STEP = 4  # amax, pack Q/K, pack V^T, attention
+
+# DRAM traffic of the attention kernel per launch, from an ncu capture, keyed by the SHA-256 of
+# attn_fp8.cu at capture time (null when the kernel changed since the counters were taken).
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="fp8_s30272_h56")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def workload(name):
+    from precision_attention_diffusion_gb300 import inputs
+    w = inputs.WORKLOADS[name]
+    return list(w["cu"]), int(w["heads"])
+
+
+def attn_flops(cu, H):
+    return 4.0 * sum((b - a) ** 2 for a, b in zip(cu[:-1], cu[1:])) * H * D
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(fp8=FP8_OVER_BF16 * float(p["bf16_tflops"]),
+                    fp8_sustained=FP8_OVER_BF16 * float(p["bf16_tflops_sustained"]),
+                    hbm=float(p["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(fp8=FP8_OVER_BF16 * 1900.0, fp8_sustained=FP8_OVER_BF16 * 1700.0, hbm=6800.0,
+                    source="fallback")
+
+
+def file_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200", "-f", self.path]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        load = [x for x in sm if x > 0.5 * smax] or sm
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the workload (the cpu_baseline object and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def oracle_sample(cu, H, seconds, seed=0):
+    """Time the oracle (as it stands, all host threads) on head 0 of the workload: FP8 quantize
+    of that head's full Q/K/V, then FP8-emulating attention of R query rows of the longest
+    segment. Extrapolates to the whole workload: per head, quantize once + L rows."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from precision_attention_diffusion_gb300 import inputs
+    lens = [b - a for a, b in zip(cu[:-1], cu[1:])]
+    s_long = int(np.argmax(lens))
+    a, b = cu[s_long], cu[s_long + 1]
+    L = b - a
+    T = cu[-1]
+    q, k, v = inputs.qkv_separate(T, 1, seed=seed)
+    bits = lambda x: x.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    qz = [oracle.fp8_quantize(bits(x)) for x in (q, k, v)]
+    t_quant = time.perf_counter() - t0
+    ncores = os.cpu_count() or 1
+    g = np.random.default_rng(seed)
+
+    def attn_rows(n):
+        rows = [(int(t), 0) for t in g.integers(a, b, n)]
+        t1 = time.perf_counter()
+        oracle.attn_fp8(qz[0][0], qz[1][0], qz[2][0], qz[0][1], qz[1][1], qz[2][1], cu, rows,
+                        1.0 / math.sqrt(D))
+        return time.perf_counter() - t1
+
+    n0 = 2 * ncores
+    t_cal = attn_rows(n0)
+    per_row = t_cal / n0
+    budget = max(seconds - t_quant - t_cal, 0.0)
+    n1 = int(budget / max(per_row, 1e-9))
+    n1 = max(0, min(n1, 200000))
+    t_more = attn_rows(n1) if n1 > 0 else 0.0
+    R = n0 + n1
+    t_attn = t_cal + t_more
+    # full-workload estimate: each head quantizes once and runs every query row of every segment
+    per_row = t_attn / R
+    # per-row cost grows with its segment's length: scale by L_s / L_longest
+    est_s = H * (t_quant + per_row * sum(x * x for x in lens) / L)
+    value = attn_flops(cu, H) / est_s / 1e12
+    return dict(value=value, unit=UNIT, cores=ncores, kind="oracle",
+                sample=(f"head 0 of {H}: FP8 quantize of its full Q/K/V ({T} tokens, "
+                        f"{t_quant:.2f} s) + FP8-emulating attention of {R} random query rows of "
+                        f"the {L}-token segment ({t_attn:.2f} s); extrapolated to all {H} heads "
+                        f"and rows"),
+                seconds=t_quant + t_attn, est_full_workload_s=est_s)
+
+
+# ------------------------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cu, H = workload(args.workload)
+    per_step = max(args.cpu_seconds / 3.0, 3.0)
+    for _ in range(args.warmup):
+        oracle_sample(cu, H, per_step / 2)
+    vals, secs = [], []
+    for i in range(args.steps):
+        r = oracle_sample(cu, H, per_step, seed=i)
+        vals.append(r["value"])
+        secs.append(r["est_full_workload_s"])
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8-emulating oracle)",
+        "data": "synthetic", "config": config_of(args.workload, cu, H),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(name, cu, H):
+    T = cu[-1]
+    return {"workload": name, "tokens": T, "heads": H, "head_dim": D,
+            "segments": [b - a for a, b in zip(cu[:-1], cu[1:])],
+            "qkv_layout": "strided views of one fused [T,3,H,128] BF16 buffer",
+            "softmax_scale": 1 / math.sqrt(D), "causal": False,
+            "l2": "inputs (1.3 GB) and codes larger than L2: no flush"}
+
+
+def run_ours(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    from precision_attention_diffusion_gb300 import build as fbuild
+    fbuild.build()
+    from precision_attention_diffusion_gb300 import fa_lp
+
+    cu, H = workload(args.workload)
+    T = cu[-1]
+    flops = attn_flops(cu, H)
+    g = torch.Generator(device="cuda").manual_seed(1234 + rank)
+    buf = torch.randn((T, 3, H, D), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, k, v = buf[:, 0], buf[:, 1], buf[:, 2]
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
+    cu_dev = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    plan = fa_lp.Plan(cu, H, mode=fa_lp.MODE_FP8)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.quantize(q, k, v, stream)
+        plan.forward(out, cu_dev, stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if plan.last_error():
+        raise RuntimeError("device wait expired during warm-up")
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    evq = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    ev[0].record(stream)
+    for i in range(K):
+        evq[i][0].record(stream)
+        plan.quantize(q, k, v, stream)
+        evq[i][1].record(stream)
+        evf[i][0].record(stream)
+        plan.forward(out, cu_dev, stream)
+        evf[i][1].record(stream)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    total_ms = ev[0].elapsed_time(ev[1])
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in evf)
+    q_ms = statistics.mean(a.elapsed_time(b) for a, b in evq)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if plan.last_error():
+        raise RuntimeError("device wait expired in the timed region")
+    ms_per_step = total_ms / K
+    value = ws * flops / (ms_per_step / 1e3) / 1e12
+
+    # end to end through the public call with host buffers: H2D of the step's inputs from pinned
+    # memory, quantize + attention, D2H of the output
+    e2e = None
+    if not args.no_e2e:
+        hbuf = buf.cpu().pin_memory()
+        hout = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
+        dbuf = torch.empty_like(buf)
+        dq, dk, dv = dbuf[:, 0], dbuf[:, 1], dbuf[:, 2]
+
+        def e2e_step():
+            dbuf.copy_(hbuf, non_blocking=True)
+            plan.attention(dq, dk, dv, cu_dev, out=out, stream=stream)
+            hout.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / K
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": ws * flops / (e_ms / 1e3) / 1e12, "unit": UNIT,
+               "ms_per_step": e_ms, "h2d_bytes_per_step": hbuf.numel() * hbuf.element_size(),
+               "d2h_bytes_per_step": hout.numel() * hout.element_size()}
+
+    pk = peaks()
+    achieved = flops / (fwd_ms / 1e3) / 1e12
+    sha = file_sha(os.path.join(ROOT, "precision_attention_diffusion_gb300", "csrc", "attn_fp8.cu"))
+    traffic = NCU_TRAFFIC.get((args.workload, sha))
+    roof = {"bound": "tensor", "achieved": achieved, "peak": pk["fp8"], "unit": "TFLOP/s",
+            "frac": achieved / pk["fp8"], "traffic": traffic,
+            "kernel": "attn_fp8_kernel", "launch_ms": fwd_ms,
+            "peak_note": (f"dense FP8 = {FP8_OVER_BF16:g} x {pk['source']} BF16 cuBLAS burst; "
+                          f"frac of sustained = {achieved / pk['fp8_sustained']:.3f}"),
+            "algorithmic_flops_per_launch": flops}
+    # quantize passes: HBM-bound; algorithmic bytes = 2 reads of Q/K/V + 1 write of the codes
+    q_bytes = 2 * 3 * T * H * D * 2 + 3 * T * H * D
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 in/out)",
+        "data": "synthetic", "config": config_of(args.workload, cu, H),
+        "forward_ms": fwd_ms, "forward_tflops": achieved, "quantize_ms": q_ms,
+        "quantize_gbs": q_bytes / (q_ms / 1e3) / 1e9,
+        "frac_of_fp8_peak": achieved / pk["fp8"],
+        "roofline": roof, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * K,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,218 @@
+/*
+ * fa_lp.h -- C ABI of the GB300 (sm_103a) low-precision packed-varlen attention forward.
+ *
+ * The operation (FlashInfer docs, flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4,
+ * description; SGLang PR #40175 "add fp8_fa_sm120 FP8 backend for SM120 GPUs", Modifications):
+ * for every segment [a, b) of cu_seqlens and every head h,
+ *
+ *     out[a:b, h] = softmax(q[a:b, h] @ k[a:b, h]^T * softmax_scale) @ v[a:b, h]
+ *
+ * non-causal, head_dim 128, BF16 in and out, computed on quantized operands:
+ *   FA_LP_MODE_FP8   : E4M3 Q/K/V with one amax scale per (tensor, head), FP32 accumulation,
+ *                      online softmax, probabilities re-quantized to E4M3 before the PV product.
+ *   FA_LP_MODE_NVFP4 : SageAttention3-style NVFP4: E2M1 codes with one UE4M3 scale per 16
+ *                      elements, K centred by its segment's per-channel mean, Q by its 128-row
+ *                      block mean (the qm K^T term added back), V transposed with per-16-key
+ *                      scales, two-level P scaling (row maximum brought to 448*6).
+ *
+ * Conventions (all entry points):
+ *   - Every function returns an int status (FA_LP_OK or an FA_LP_ERR_* code); nothing throws
+ *     across the ABI. fa_lp_status_string() names a status.
+ *   - "device pointer" arguments are CUDA device addresses on the plan's device; "host pointer"
+ *     arguments are ordinary host memory. The caller keeps ownership of everything it passes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
+ *     enqueued on it and the call returns without synchronizing; no host-device synchronization
+ *     happens inside fa_lp_quantize / fa_lp_forward_varlen / fa_lp_attention.
+ *   - Strides are in ELEMENTS (BF16 = 2 bytes). The channel (head_dim) axis must be contiguous.
+ *   - The quantized operands live in one grow-only workspace per device, shared by every plan and
+ *     both modes. Calls that use the same device must therefore be ordered (one stream, or
+ *     externally synchronized streams): fa_lp_quantize for one plan followed by fa_lp_quantize for
+ *     another plan overwrites the first plan's codes.
+ *   - There is no fallback: shapes or devices the kernels do not handle return
+ *     FA_LP_ERR_UNSUPPORTED (head_dim != 128 is not expressible; a device other than sm_103 is).
+ */
+#ifndef FA_LP_H_
+#define FA_LP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_LP_API __attribute__((visibility("default")))
+#else
+#define FA_LP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------------------- */
+#define FA_LP_OK 0
+#define FA_LP_ERR_INVALID_ARG 1     /* bad pointer, size, stride, cu_seqlens or mode            */
+#define FA_LP_ERR_UNSUPPORTED 2     /* valid request the kernels do not serve (device arch, ...) */
+#define FA_LP_ERR_CUDA 3            /* a CUDA runtime / driver call failed                       */
+#define FA_LP_ERR_OOM 4             /* workspace or plan metadata allocation failed              */
+#define FA_LP_ERR_DEVICE_TIMEOUT 5  /* a bounded device-side wait expired (see fa_lp_get_last_error) */
+#define FA_LP_ERR_STATE 6           /* call out of order (e.g. forward before quantize)          */
+
+/* ---- modes ----------------------------------------------------------------------------------- */
+#define FA_LP_MODE_FP8 0
+#define FA_LP_MODE_NVFP4 1
+
+#define FA_LP_HEAD_DIM 128
+
+typedef struct fa_lp_plan fa_lp_plan;
+
+/* Human-readable name of a status code. Never NULL; the string is static. */
+FA_LP_API const char* fa_lp_status_string(int status);
+
+/*
+ * fa_lp_plan_create -- validate a packed-varlen segmentation and build (or fetch from the cache)
+ * the plan for it.
+ * Passage: FlashInfer docs, minimax_h3_sm120_varlen_attention_nvfp4, Parameters (cu_seqlens:
+ * cu_seqlens[0] = 0, non-decreasing entries, cu_seqlens[-1] = tokens; cu_seqlens_host avoids a
+ * synchronizing device-to-host copy and the segment plan is cached per (cu_seqlens, heads,
+ * device); softmax_scale defaults to 1/sqrt(128)).
+ *   tokens          : T, total packed tokens (>= 0).
+ *   heads           : H (1..1024).
+ *   cu_seqlens_host : host pointer, num_segments + 1 int32 entries. Copied; not retained.
+ *   num_segments    : >= 1. Empty segments (cu[s] == cu[s+1]) are allowed and produce no work.
+ *   softmax_scale   : > 0 and finite; <= 0 or NaN selects 1/sqrt(128).
+ *   mode            : FA_LP_MODE_FP8 or FA_LP_MODE_NVFP4.
+ *   device          : CUDA device ordinal the plan will run on (not touched here).
+ *   out             : receives the plan. A plan with an identical key is shared (reference
+ *                     counted); every successful create needs one fa_lp_plan_destroy.
+ * Host-only: makes no CUDA call, so it also works on a machine without a GPU.
+ * Errors: FA_LP_ERR_INVALID_ARG for a malformed cu_seqlens, NULL pointers, bad heads or mode.
+ */
+FA_LP_API int fa_lp_plan_create(int64_t tokens, int heads, const int32_t* cu_seqlens_host,
+                      int num_segments, float softmax_scale, int mode, int device,
+                      fa_lp_plan** out);
+
+/* Release one reference. The last release frees the plan's host state and its small device
+ * metadata buffer (cudaFree, after synchronizing the device). The shared workspace is kept;
+ * see fa_lp_release_workspace. NULL is accepted. */
+FA_LP_API int fa_lp_plan_destroy(fa_lp_plan* plan);
+
+/* Plan facts, for callers and tests.
+ *   padded_tokens : rows of the padded token axis (every segment starts on a 128-row boundary).
+ *   work_items    : attention work items (segment, head, pair of 128-row query tiles).
+ *   workspace     : bytes of the per-device workspace this plan needs. */
+FA_LP_API int fa_lp_plan_info(const fa_lp_plan* plan, int64_t* padded_tokens, int64_t* work_items,
+                    size_t* workspace_bytes);
+
+/* Bytes of workspace the plan needs (cf. the FlashInfer op's workspace_bytes_nvfp4). */
+FA_LP_API int fa_lp_workspace_bytes(const fa_lp_plan* plan, size_t* bytes);
+
+/*
+ * fa_lp_quantize -- quantize BF16 Q, K, V straight from (possibly strided) device views into the
+ * device workspace.
+ * Passage: SGLang PR #40175, Modifications (fused_prep.py: quantize strided BF16 Q/K/V views per
+ * head straight into the kernel buffers, amax then pack, no FP32 intermediates, no layout copy);
+ * review reply (the pack pass writes every padding position). NVFP4: FlashInfer docs (K centred
+ * by the segment's per-channel mean, Q by its 128-row block mean, E2M1 + UE4M3 per 16, V
+ * transposed with per-16-key scales).
+ *   q, k, v       : device pointers to BF16 [tokens, heads, 128] views; element strides
+ *                   (*_stride_tok, *_stride_head) may be any positive values (e.g. slices of a
+ *                   fused [T, 3, H, 128] buffer); channel stride 1; 16-byte aligned rows.
+ *   stream        : cudaStream_t (as void*).
+ * FP8 mode: per (tensor, head) amax over all tokens, descale = amax/448, codes
+ * E4M3_rn_sat(x * (448/amax)). NVFP4 mode: K means, Q block means, E2M1/UE4M3 packing.
+ * Grows the device workspace if needed (stream-ordered cudaMallocAsync/cudaFreeAsync).
+ * Retains no reference to q, k, v after the kernels read them.
+ * Errors: INVALID_ARG (NULL, misaligned, non-positive strides), UNSUPPORTED (device not sm_103),
+ * OOM, CUDA.
+ */
+FA_LP_API int fa_lp_quantize(fa_lp_plan* plan, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                   const void* k, int64_t k_stride_tok, int64_t k_stride_head, const void* v,
+                   int64_t v_stride_tok, int64_t v_stride_head, void* stream);
+
+/*
+ * fa_lp_forward_varlen -- attention over the quantized operands of the last fa_lp_quantize of
+ * this plan (same device, same stream order).
+ * Passage: SGLang PR #40175, Modifications (kernel.py: E4M3 QK and PV with FP32 accumulation,
+ * online softmax, probabilities packed to E4M3) and FlashInfer docs (description; out: optional
+ * pre-allocated output of q's shape and dtype; the output is rounded to BF16 once).
+ *   cu_seqlens_dev : device pointer to the same num_segments+1 int32 values the plan was built
+ *                    from (accepted for the documented call shape; the kernels index with the
+ *                    plan's copy, so its contents are not read).
+ *   out            : device pointer, BF16 [tokens, heads, 128] with element strides
+ *                    (out_stride_tok, out_stride_head), caller-owned. Only rows inside segments
+ *                    are written; other rows are left untouched.
+ *   stream         : cudaStream_t (as void*).
+ * Errors: STATE (no quantize on this plan yet), INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+FA_LP_API int fa_lp_forward_varlen(fa_lp_plan* plan, const int32_t* cu_seqlens_dev, void* out,
+                         int64_t out_stride_tok, int64_t out_stride_head, void* stream);
+
+/* fa_lp_attention -- fa_lp_quantize followed by fa_lp_forward_varlen on the same stream: the
+ * one-call form out = attention(q, k, v, cu_seqlens) of the FlashInfer op's signature. */
+FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_tok,
+                    int64_t q_stride_head, const void* k, int64_t k_stride_tok,
+                    int64_t k_stride_head, const void* v, int64_t v_stride_tok,
+                    int64_t v_stride_head, const int32_t* cu_seqlens_dev, void* out,
+                    int64_t out_stride_tok, int64_t out_stride_head, void* stream);
+
+/*
+ * Inspection of the quantized operands (for bit-exact tests). `which` selects one array of the
+ * workspace; the descriptor gives its device address and layout. Valid until the next call that
+ * may grow the workspace.
+ */
+#define FA_LP_Q_CODES 0     /* FP8: u8 [H][Tpad][128]  NVFP4: u8 [H][Tpad][64] (2 codes/byte)   */
+#define FA_LP_K_CODES 1     /* same layout as Q                                                  */
+#define FA_LP_V_CODES 2     /* FP8: u8 [H][128][Tpad] (V^T)  NVFP4: u8 [H][128][Tpad/2]          */
+#define FA_LP_DESCALE 3     /* FP8: f32 [3][H] = amax/448 of q, k, v                             */
+#define FA_LP_Q_SCALES 4    /* NVFP4: u8 [H][Tpad][8] UE4M3, one per 16 channels                 */
+#define FA_LP_K_SCALES 5    /* NVFP4: u8 [H][Tpad][8]                                            */
+#define FA_LP_V_SCALES 6    /* NVFP4: u8 [H][128][Tpad/16], one per 16 keys                      */
+#define FA_LP_Q_MEANS 7     /* NVFP4: f32 [H][Tpad/128][128], block means                        */
+#define FA_LP_K_MEANS 8     /* NVFP4: f32 [num_segments][H][128], segment means                  */
+
+typedef struct fa_lp_array_desc {
+  const void* data;  /* device address                                                     */
+  int64_t dims[3];   /* outermost first                                                    */
+  int64_t strides[3];/* bytes                                                              */
+  int elem_bytes;    /* 1 or 4                                                             */
+} fa_lp_array_desc;
+
+/* Padded token axis: segment s occupies rows [row_offset[s], row_offset[s] + L_s) of Tpad, where
+ * row_offset[s] = sum over s' < s of roundup(L_s', 128); rows in between hold zero codes.
+ * row_offsets must have room for num_segments + 1 entries (host pointer). */
+FA_LP_API int fa_lp_plan_row_offsets(const fa_lp_plan* plan, int64_t* row_offsets);
+
+FA_LP_API int fa_lp_get_quantized(const fa_lp_plan* plan, int which, fa_lp_array_desc* desc);
+
+/* Copy one quantized array (see fa_lp_get_quantized) into a caller-owned device buffer of at
+ * least dims[0]*dims[1]*dims[2]*elem_bytes bytes, stream-ordered on `stream`.
+ * Errors: INVALID_ARG (NULL, buffer too small, bad `which`), STATE (nothing quantized yet). */
+FA_LP_API int fa_lp_copy_quantized(const fa_lp_plan* plan, int which, void* dst, size_t dst_bytes,
+                         void* stream);
+
+/*
+ * fa_lp_get_last_error -- device-side status of the plan's kernels: 0 when every bounded
+ * device wait completed, otherwise a code with the waiting role in its low byte. Reading it
+ * synchronizes the device and clears it. Returns FA_LP_ERR_DEVICE_TIMEOUT when non-zero.
+ */
+FA_LP_API int fa_lp_get_last_error(fa_lp_plan* plan, int* device_status);
+
+/* Upper bound on the spin iterations of every device-side barrier wait of this plan's
+ * kernels (default 2^26 probes, seconds or more). A wait that reaches it records an error, the kernel
+ * drains its in-flight copies, frees its tensor memory and returns. Small values are for tests of
+ * that path. spins >= 1. */
+FA_LP_API int fa_lp_plan_set_wait_limit(fa_lp_plan* plan, int64_t spins);
+
+/* Free the workspace of `device` (stream-ordered on `stream`). Plans stay valid; the next
+ * quantize allocates again. */
+FA_LP_API int fa_lp_release_workspace(int device, void* stream);
+
+/* Encode `n` fp32 device values with the device's converters (format 0: E4M3 rn satfinite,
+ * one byte per value; format 1: E2M1 rn satfinite, one 4-bit code per byte). For tests that pin
+ * the hardware conversions against the format definitions. */
+FA_LP_API int fa_lp_encode(int format, const float* x, int64_t n, uint8_t* codes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_LP_H_ */

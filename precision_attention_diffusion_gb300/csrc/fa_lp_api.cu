@@ -1,0 +1,517 @@
+// fa_lp_api.cu -- the C ABI entry points of libfa_lp.so: plan building and caching, argument
+// validation, the per-device grow-only workspace, and dispatch to the CUDA launchers.
+//
+// Passages: FlashInfer docs, flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4,
+// Parameters (cu_seqlens contract, host copy, plan cache keyed by (cu_seqlens, heads, device),
+// default softmax scale) and description (grow-only per-device workspace shared by the FP8 and
+// NVFP4 ops); SGLang PR #40175, review replies (no input references retained, output owned by the
+// caller, allocation stream-ordered on the calling stream).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "fa_lp_internal.h"
+
+using falp::BlockInfo;
+using falp::SegInfo;
+using falp::WorkItem;
+
+namespace {
+
+std::mutex g_mu;
+
+// ---- plan cache, keyed by (cu_seqlens, tokens, heads, scale bits, mode, device) ---------------
+using PlanKey = std::tuple<std::vector<int32_t>, int64_t, int, uint32_t, int, int>;
+std::map<PlanKey, fa_lp_plan*> g_plans;
+
+PlanKey key_of(const fa_lp_plan& p) {
+  uint32_t sb;
+  std::memcpy(&sb, &p.scale, 4);
+  return PlanKey(p.cu, p.tokens, p.heads, sb, p.mode, p.device);
+}
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("FA_LP_LOG");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- per-device workspace ----------------------------------------------------------------------
+struct DevWs {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<int, DevWs> g_ws;
+
+// ---- device capability check ---------------------------------------------------------------------
+int check_device(int device) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(device);
+  if (it != cache.end()) return it->second;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  const int st = (major == 10 && minor == 3) ? FA_LP_OK : FA_LP_ERR_UNSUPPORTED;
+  cache[device] = st;
+  return st;
+}
+
+int check_current_device(const fa_lp_plan* p) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return FA_LP_ERR_CUDA;
+  if (cur != p->device) return FA_LP_ERR_INVALID_ARG;
+  return check_device(p->device);
+}
+
+// Upload the plan's segment / block / work tables once (stream-ordered).
+int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
+  if (p->dmeta) return FA_LP_OK;
+  const size_t n_seg = p->segs.size() * sizeof(SegInfo);
+  const size_t n_blk = p->blocks.size() * sizeof(BlockInfo);
+  const size_t n_wrk = p->work.size() * sizeof(WorkItem);
+  const size_t o_seg = 0;
+  const size_t o_blk = align_up(o_seg + n_seg, 256);
+  const size_t o_wrk = align_up(o_blk + n_blk, 256);
+  const size_t o_err = align_up(o_wrk + n_wrk, 256);
+  const size_t total = o_err + 256;
+  void* d = nullptr;
+  if (cudaMalloc(&d, total) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_LP_ERR_OOM;
+  }
+  std::vector<uint8_t> host(total, 0);
+  if (n_seg) std::memcpy(host.data() + o_seg, p->segs.data(), n_seg);
+  if (n_blk) std::memcpy(host.data() + o_blk, p->blocks.data(), n_blk);
+  if (n_wrk) std::memcpy(host.data() + o_wrk, p->work.data(), n_wrk);
+  if (cudaMemcpyAsync(d, host.data(), total, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaFree(d);
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  p->dmeta = d;
+  uint8_t* b = static_cast<uint8_t*>(d);
+  p->d_segs = reinterpret_cast<SegInfo*>(b + o_seg);
+  p->d_blocks = reinterpret_cast<BlockInfo*>(b + o_blk);
+  p->d_work = reinterpret_cast<WorkItem*>(b + o_wrk);
+  p->d_err = reinterpret_cast<int*>(b + o_err);
+  if (log_enabled())
+    std::fprintf(stderr, "[fa_lp] plan %p: device tables %zu bytes on device %d\n", (void*)p,
+                 total, p->device);
+  return FA_LP_OK;
+}
+
+bool bad_view(const void* ptr, int64_t st, int64_t sh) {
+  if (!ptr) return true;
+  if (st <= 0 || sh <= 0) return true;
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return true;
+  if (st % 8 != 0 || sh % 8 != 0) return true;  // 16-byte aligned rows of 128 BF16
+  return false;
+}
+
+void build_plan(fa_lp_plan* p) {
+  const int ns = p->nseg;
+  p->row_off.assign(ns + 1, 0);
+  p->segs.resize(ns);
+  int64_t row = 0;
+  for (int s = 0; s < ns; ++s) {
+    const int64_t L = int64_t(p->cu[s + 1]) - p->cu[s];
+    const int64_t nb = (L + falp::kTile - 1) / falp::kTile;
+    p->row_off[s] = row;
+    p->segs[s] = SegInfo{p->cu[s], int32_t(L), int32_t(row), int32_t(nb)};
+    for (int64_t b = 0; b < nb; ++b) {
+      const int64_t nv = std::min<int64_t>(falp::kTile, L - b * falp::kTile);
+      p->blocks.push_back(BlockInfo{int32_t(p->cu[s] + b * falp::kTile), int32_t(nv), s, int32_t(b)});
+    }
+    row += nb * falp::kTile;
+  }
+  p->row_off[ns] = row;
+  p->tpad = row;
+
+  // Work list: longest segment first (LPT), then head, then pairs of query tiles, so that the
+  // CTAs running at the same time share one head's K/V in L2.
+  std::vector<int> order(ns);
+  for (int s = 0; s < ns; ++s) order[s] = s;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return p->segs[a].len > p->segs[b].len; });
+  for (int s : order) {
+    const int nb = p->segs[s].nblk;
+    if (nb == 0) continue;
+    for (int h = 0; h < p->heads; ++h)
+      for (int t = 0; t < nb; t += 2) p->work.push_back(WorkItem{s, h, t, std::min(2, nb - t)});
+  }
+
+  // Workspace layout.
+  const size_t H = size_t(p->heads), Tp = size_t(p->tpad);
+  falp::WsLayout& w = p->ws;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 1), 1024);
+    return o;
+  };
+  if (p->mode == FA_LP_MODE_FP8) {
+    w.q_codes = take(H * Tp * 128);
+    w.k_codes = take(H * Tp * 128);
+    w.v_codes = take(H * 128 * Tp);
+    w.amax = take(3 * H * 4);
+    w.descale = take(3 * H * 4);
+  } else {
+    w.q_codes = take(H * Tp * 64);
+    w.k_codes = take(H * Tp * 64);
+    w.v_codes = take(H * 128 * Tp / 2);
+    w.q_sf = take(H * Tp * 8);
+    w.k_sf = take(H * Tp * 8);
+    w.v_sf = take(H * 128 * (Tp / 16));
+    w.q_mean = take(H * (Tp / 128) * 128 * 4);
+    w.k_mean = take(size_t(p->nseg) * H * 128 * 4);
+  }
+  w.total = off;
+}
+
+}  // namespace
+
+namespace falp {
+
+int next_launch_generation() {
+  static std::atomic<int> g{0};
+  int v = g.fetch_add(1) + 1;
+  if (v <= 0) {  // wrapped: restart at 1
+    g.store(1);
+    v = 1;
+  }
+  return v;
+}
+
+int workspace_acquire(int device, size_t bytes, cudaStream_t stream, void** base) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevWs& w = g_ws[device];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      if (cudaFreeAsync(w.ptr, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_LP_ERR_CUDA;
+      }
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, bytes, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_LP_ERR_OOM;
+    }
+    w.ptr = p;
+    w.bytes = bytes;
+    if (log_enabled())
+      std::fprintf(stderr, "[fa_lp] workspace on device %d grown to %zu bytes\n", device, bytes);
+  }
+  *base = w.ptr;
+  return FA_LP_OK;
+}
+
+int encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                      uint32_t box1, CUtensorMapSwizzle swz) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  if (!fn) return FA_LP_ERR_CUDA;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_LP_OK : FA_LP_ERR_CUDA;
+}
+
+}  // namespace falp
+
+extern "C" {
+
+const char* fa_lp_status_string(int status) {
+  switch (status) {
+    case FA_LP_OK: return "ok";
+    case FA_LP_ERR_INVALID_ARG: return "invalid argument";
+    case FA_LP_ERR_UNSUPPORTED: return "unsupported (this library serves sm_103 GPUs only)";
+    case FA_LP_ERR_CUDA: return "CUDA error";
+    case FA_LP_ERR_OOM: return "out of device memory";
+    case FA_LP_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+    case FA_LP_ERR_STATE: return "call out of order (quantize before forward)";
+    default: return "unknown status";
+  }
+}
+
+int fa_lp_plan_create(int64_t tokens, int heads, const int32_t* cu, int num_segments,
+                      float softmax_scale, int mode, int device, fa_lp_plan** out) {
+  if (!out || !cu) return FA_LP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (tokens < 0 || tokens > (int64_t(1) << 30)) return FA_LP_ERR_INVALID_ARG;
+  if (heads < 1 || heads > 1024 || num_segments < 1 || device < 0) return FA_LP_ERR_INVALID_ARG;
+  if (mode != FA_LP_MODE_FP8 && mode != FA_LP_MODE_NVFP4) return FA_LP_ERR_INVALID_ARG;
+  if (cu[0] != 0 || int64_t(cu[num_segments]) != tokens) return FA_LP_ERR_INVALID_ARG;
+  for (int s = 0; s < num_segments; ++s)
+    if (cu[s + 1] < cu[s]) return FA_LP_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    softmax_scale = 1.0f / std::sqrt(float(FA_LP_HEAD_DIM));
+
+  auto* p = new fa_lp_plan();
+  p->tokens = tokens;
+  p->heads = heads;
+  p->nseg = num_segments;
+  p->scale = softmax_scale;
+  p->mode = mode;
+  p->device = device;
+  p->cu.assign(cu, cu + num_segments + 1);
+
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_plans.find(key_of(*p));
+  if (it != g_plans.end()) {
+    delete p;
+    it->second->refcount++;
+    *out = it->second;
+    return FA_LP_OK;
+  }
+  build_plan(p);
+  g_plans[key_of(*p)] = p;
+  if (log_enabled())
+    std::fprintf(stderr, "[fa_lp] plan %p: T=%lld H=%d segs=%d Tpad=%lld items=%zu ws=%zu\n",
+                 (void*)p, (long long)tokens, heads, num_segments, (long long)p->tpad,
+                 p->work.size(), p->ws.total);
+  *out = p;
+  return FA_LP_OK;
+}
+
+int fa_lp_plan_destroy(fa_lp_plan* p) {
+  if (!p) return FA_LP_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (--p->refcount > 0) return FA_LP_OK;
+  g_plans.erase(key_of(*p));
+  int st = FA_LP_OK;
+  if (p->dmeta) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dmeta) != cudaSuccess) {
+      cudaGetLastError();
+      st = FA_LP_ERR_CUDA;
+    }
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+  }
+  delete p;
+  return st;
+}
+
+int fa_lp_plan_info(const fa_lp_plan* p, int64_t* padded_tokens, int64_t* work_items,
+                    size_t* workspace_bytes) {
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  if (padded_tokens) *padded_tokens = p->tpad;
+  if (work_items) *work_items = int64_t(p->work.size());
+  if (workspace_bytes) *workspace_bytes = p->ws.total;
+  return FA_LP_OK;
+}
+
+int fa_lp_workspace_bytes(const fa_lp_plan* p, size_t* bytes) {
+  if (!p || !bytes) return FA_LP_ERR_INVALID_ARG;
+  *bytes = p->ws.total;
+  return FA_LP_OK;
+}
+
+int fa_lp_plan_row_offsets(const fa_lp_plan* p, int64_t* row_offsets) {
+  if (!p || !row_offsets) return FA_LP_ERR_INVALID_ARG;
+  std::copy(p->row_off.begin(), p->row_off.end(), row_offsets);
+  return FA_LP_OK;
+}
+
+int fa_lp_plan_set_wait_limit(fa_lp_plan* p, int64_t spins) {
+  if (!p || spins < 1) return FA_LP_ERR_INVALID_ARG;
+  p->spin_limit = spins;
+  return FA_LP_OK;
+}
+
+int fa_lp_quantize(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
+                   int64_t kst, int64_t ksh, const void* v, int64_t vst, int64_t vsh,
+                   void* stream_) {
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  if (p->tokens > 0 && (bad_view(q, qst, qsh) || bad_view(k, kst, ksh) || bad_view(v, vst, vsh)))
+    return FA_LP_ERR_INVALID_ARG;
+  int st = check_current_device(p);
+  if (st != FA_LP_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if ((st = ensure_device_meta(p, stream)) != FA_LP_OK) return st;
+  void* base = nullptr;
+  if ((st = falp::workspace_acquire(p->device, p->ws.total, stream, &base)) != FA_LP_OK) return st;
+  if (p->tokens > 0) {
+    st = (p->mode == FA_LP_MODE_FP8)
+             ? falp::launch_fp8_quantize(*p, static_cast<uint8_t*>(base), q, qst, qsh, k, kst, ksh,
+                                         v, vst, vsh, stream)
+             : falp::launch_nvfp4_quantize(*p, static_cast<uint8_t*>(base), q, qst, qsh, k, kst,
+                                           ksh, v, vst, vsh, stream);
+    if (st != FA_LP_OK) return st;
+  }
+  p->quantized = true;
+  return FA_LP_OK;
+}
+
+int fa_lp_forward_varlen(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out, int64_t ost,
+                         int64_t osh, void* stream_) {
+  (void)cu_seqlens_dev;
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  if (!p->quantized) return FA_LP_ERR_STATE;
+  if (p->tokens > 0 && bad_view(out, ost, osh)) return FA_LP_ERR_INVALID_ARG;
+  int st = check_current_device(p);
+  if (st != FA_LP_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const DevWs& w = g_ws[p->device];
+    if (!w.ptr || w.bytes < p->ws.total) return FA_LP_ERR_STATE;
+    base = w.ptr;
+  }
+  if (p->work.empty()) return FA_LP_OK;
+  return (p->mode == FA_LP_MODE_FP8)
+             ? falp::launch_fp8_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, stream)
+             : falp::launch_nvfp4_attention(*p, static_cast<uint8_t*>(base), out, ost, osh,
+                                            stream);
+}
+
+int fa_lp_attention(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
+                    int64_t kst, int64_t ksh, const void* v, int64_t vst, int64_t vsh,
+                    const int32_t* cu_seqlens_dev, void* out, int64_t ost, int64_t osh,
+                    void* stream) {
+  const int st = fa_lp_quantize(p, q, qst, qsh, k, kst, ksh, v, vst, vsh, stream);
+  if (st != FA_LP_OK) return st;
+  return fa_lp_forward_varlen(p, cu_seqlens_dev, out, ost, osh, stream);
+}
+
+int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
+  if (!p || !d) return FA_LP_ERR_INVALID_ARG;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_ws.find(p->device);
+    if (it == g_ws.end() || !it->second.ptr || it->second.bytes < p->ws.total)
+      return FA_LP_ERR_STATE;
+    base = it->second.ptr;
+  }
+  const uint8_t* b = static_cast<const uint8_t*>(base);
+  const int64_t H = p->heads, Tp = p->tpad;
+  std::memset(d, 0, sizeof(*d));
+  auto set = [&](size_t off, int64_t d0, int64_t d1, int64_t d2, int eb) {
+    d->data = b + off;
+    d->dims[0] = d0; d->dims[1] = d1; d->dims[2] = d2;
+    d->strides[2] = eb;
+    d->strides[1] = d2 * eb;
+    d->strides[0] = d1 * d2 * eb;
+    d->elem_bytes = eb;
+    return FA_LP_OK;
+  };
+  if (p->mode == FA_LP_MODE_FP8) {
+    switch (which) {
+      case FA_LP_Q_CODES: return set(p->ws.q_codes, H, Tp, 128, 1);
+      case FA_LP_K_CODES: return set(p->ws.k_codes, H, Tp, 128, 1);
+      case FA_LP_V_CODES: return set(p->ws.v_codes, H, 128, Tp, 1);
+      case FA_LP_DESCALE: return set(p->ws.descale, 1, 3, H, 4);
+      default: return FA_LP_ERR_INVALID_ARG;
+    }
+  }
+  switch (which) {
+    case FA_LP_Q_CODES: return set(p->ws.q_codes, H, Tp, 64, 1);
+    case FA_LP_K_CODES: return set(p->ws.k_codes, H, Tp, 64, 1);
+    case FA_LP_V_CODES: return set(p->ws.v_codes, H, 128, Tp / 2, 1);
+    case FA_LP_Q_SCALES: return set(p->ws.q_sf, H, Tp, 8, 1);
+    case FA_LP_K_SCALES: return set(p->ws.k_sf, H, Tp, 8, 1);
+    case FA_LP_V_SCALES: return set(p->ws.v_sf, H, 128, Tp / 16, 1);
+    case FA_LP_Q_MEANS: return set(p->ws.q_mean, H, Tp / 128, 128, 4);
+    case FA_LP_K_MEANS: return set(p->ws.k_mean, p->nseg, H, 128, 4);
+    default: return FA_LP_ERR_INVALID_ARG;
+  }
+}
+
+int fa_lp_copy_quantized(const fa_lp_plan* p, int which, void* dst, size_t dst_bytes,
+                         void* stream) {
+  if (!p || !dst) return FA_LP_ERR_INVALID_ARG;
+  fa_lp_array_desc d;
+  const int st = fa_lp_get_quantized(p, which, &d);
+  if (st != FA_LP_OK) return st;
+  const size_t bytes = size_t(d.dims[0]) * size_t(d.dims[1]) * size_t(d.dims[2]) * d.elem_bytes;
+  if (dst_bytes < bytes) return FA_LP_ERR_INVALID_ARG;
+  return falp::cuda_status(cudaMemcpyAsync(dst, d.data, bytes, cudaMemcpyDeviceToDevice,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int fa_lp_get_last_error(fa_lp_plan* p, int* device_status) {
+  if (!p || !device_status) return FA_LP_ERR_INVALID_ARG;
+  *device_status = 0;
+  if (!p->dmeta) return FA_LP_OK;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  if (cur != p->device) cudaSetDevice(p->device);
+  int v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&v, p->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
+  if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  *device_status = v;
+  return v ? FA_LP_ERR_DEVICE_TIMEOUT : FA_LP_OK;
+}
+
+int fa_lp_release_workspace(int device, void* stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_ws.find(device);
+  if (it == g_ws.end() || !it->second.ptr) return FA_LP_OK;
+  const cudaError_t e = cudaFreeAsync(it->second.ptr, static_cast<cudaStream_t>(stream));
+  it->second = DevWs{};
+  for (auto& kv : g_plans)
+    if (kv.second->device == device) kv.second->quantized = false;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  return FA_LP_OK;
+}
+
+int fa_lp_encode(int format, const float* x, int64_t n, uint8_t* codes, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !codes)) || (format != 0 && format != 1))
+    return FA_LP_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_LP_ERR_CUDA;
+  const int st = check_device(dev);
+  if (st != FA_LP_OK) return st;
+  if (n == 0) return FA_LP_OK;
+  return falp::launch_encode(format, x, n, codes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// fa_lp_internal.h -- declarations shared by the translation units of libfa_lp.so (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/fa_lp.h"
+
+namespace falp {
+
+constexpr int kD = FA_LP_HEAD_DIM;  // 128
+constexpr int kTile = 128;          // rows of a query tile / keys of a key tile / padding quantum
+
+// One segment of the packed batch, as the kernels see it.
+struct SegInfo {
+  int32_t tok0;     // first token of the segment in the packed input (cu_seqlens[s])
+  int32_t len;      // L_s
+  int32_t row0;     // first row of the segment on the padded token axis
+  int32_t nblk;     // ceil(L_s / 128)
+};
+
+// 128-row block of the padded token axis (quantize passes).
+struct BlockInfo {
+  int32_t tok0;     // token of the block's first row, or -1 (never: every block has a segment)
+  int32_t nvalid;   // rows of the block that hold tokens (the rest are zero padding)
+  int32_t seg;      // segment index
+  int32_t blk;      // block index inside its segment
+};
+
+// Attention work item: a pair of 128-row query tiles of one (segment, head).
+struct WorkItem {
+  int32_t seg;
+  int32_t head;
+  int32_t qt0;      // index of the first query tile inside the segment
+  int32_t nq;       // 1 or 2 query tiles
+};
+
+// Workspace layout of one plan (byte offsets from the workspace base, 1024-aligned).
+struct WsLayout {
+  size_t q_codes = 0, k_codes = 0, v_codes = 0;  // FP8: [H][Tp][128], [H][Tp][128], [H][128][Tp]
+  size_t q_sf = 0, k_sf = 0, v_sf = 0;           // NVFP4 scale bytes
+  size_t q_mean = 0, k_mean = 0;                 // NVFP4 means (f32)
+  size_t amax = 0, descale = 0;                  // FP8: u32 [3][H], f32 [3][H]
+  size_t total = 0;
+};
+
+}  // namespace falp
+
+struct fa_lp_plan {
+  // key
+  int64_t tokens = 0;
+  int heads = 0;
+  int nseg = 0;
+  float scale = 0.f;
+  int mode = 0;
+  int device = 0;
+  std::vector<int32_t> cu;
+  // derived
+  int64_t tpad = 0;
+  std::vector<int64_t> row_off;  // nseg + 1
+  std::vector<falp::SegInfo> segs;
+  std::vector<falp::BlockInfo> blocks;
+  std::vector<falp::WorkItem> work;
+  falp::WsLayout ws;
+  int64_t spin_limit = int64_t(1) << 26;
+  // device metadata (created on first use on the plan's device)
+  void* dmeta = nullptr;
+  falp::SegInfo* d_segs = nullptr;
+  falp::BlockInfo* d_blocks = nullptr;
+  falp::WorkItem* d_work = nullptr;
+  int* d_err = nullptr;  // [0]: sticky device status, [1]: abort word (launch generation)
+  bool quantized = false;
+  int refcount = 1;
+};
+
+namespace falp {
+
+// Per-device shared workspace (grow-only). Returns FA_LP_OK and the base pointer.
+int workspace_acquire(int device, size_t bytes, cudaStream_t stream, void** base);
+
+// Tensor-map encoder from the driver (resolved once through the runtime's entry-point query).
+int encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                      uint32_t box1, CUtensorMapSwizzle swz);
+
+// Launchers (defined next to their kernels). All enqueue on `stream` and return a status.
+int launch_fp8_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t qst,
+                        int64_t qsh, const void* k, int64_t kst, int64_t ksh, const void* v,
+                        int64_t vst, int64_t vsh, cudaStream_t stream);
+int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
+                         cudaStream_t stream);
+int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t qst,
+                          int64_t qsh, const void* k, int64_t kst, int64_t ksh, const void* v,
+                          int64_t vst, int64_t vsh, cudaStream_t stream);
+int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
+                           cudaStream_t stream);
+int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
+
+// Distinct positive id per kernel launch (device-side abort words compare against it).
+int next_launch_generation();
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_LP_OK : FA_LP_ERR_CUDA; }
+
+}  // namespace falp

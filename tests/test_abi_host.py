@@ -1,0 +1,118 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a and loads, it exports every
+function include/fa_lp.h declares, and the host-only plan logic (cu_seqlens validation, padded
+token axis, work list, workspace size) behaves as documented. No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_lp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from precision_attention_diffusion_gb300 import build, fa_lp
+    build.build()
+    return fa_lp.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^FA_LP_API\s+(?:int|const char\*)\s+(fa_lp_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_documented_calls():
+    names = declared_functions()
+    for must in ("fa_lp_plan_create", "fa_lp_quantize", "fa_lp_forward_varlen",
+                 "fa_lp_attention", "fa_lp_plan_destroy", "fa_lp_workspace_bytes",
+                 "fa_lp_get_last_error", "fa_lp_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from precision_attention_diffusion_gb300 import fa_lp
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(fa_lp.EXPORTS)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.fa_lp_status_string(s)
+    assert b"unknown" in lib.fa_lp_status_string(99)
+
+
+def _create(lib, cu, heads=4, mode=0, scale=0.0, tokens=None):
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    h = ctypes.c_void_p()
+    t = cu[-1] if tokens is None else tokens
+    st = lib.fa_lp_plan_create(t, heads, arr, len(cu) - 1, scale, mode, 0, ctypes.byref(h))
+    return st, h
+
+
+@pytest.mark.parametrize("cu,tokens", [([1, 5], None), ([0, 5, 3], None), ([0, 5], 6),
+                                       ([0, -1, 5], None)])
+def test_plan_rejects_malformed_cu_seqlens(lib, cu, tokens):
+    st, h = _create(lib, cu, tokens=tokens)
+    assert st == 1 and not h.value
+
+
+def test_plan_rejects_bad_heads_and_mode(lib):
+    assert _create(lib, [0, 5], heads=0)[0] == 1
+    assert _create(lib, [0, 5], mode=7)[0] == 1
+
+
+def test_plan_padded_axis_and_work_list(lib):
+    from precision_attention_diffusion_gb300 import fa_lp
+    cu = [0, 0, 17, 4113, 4113, 31800, 32768]
+    st, h = _create(lib, cu, heads=56)
+    assert st == 0
+    try:
+        tp, wi, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+        assert lib.fa_lp_plan_info(h, ctypes.byref(tp), ctypes.byref(wi), ctypes.byref(ws)) == 0
+        lens = [b - a for a, b in zip(cu[:-1], cu[1:])]
+        blocks = [(L + 127) // 128 for L in lens]
+        assert tp.value == 128 * sum(blocks)
+        assert wi.value == 56 * sum((b + 1) // 2 for b in blocks)
+        # FP8 workspace: Q, K codes [H][Tp][128], V^T [H][128][Tp], plus two [3][H] arrays
+        assert ws.value >= 3 * 56 * 128 * tp.value
+        offs = (ctypes.c_int64 * len(cu))()
+        assert lib.fa_lp_plan_row_offsets(h, offs) == 0
+        want, acc = [], 0
+        for b in blocks:
+            want.append(acc)
+            acc += 128 * b
+        want.append(acc)
+        assert list(offs) == want
+        assert all(o % 128 == 0 for o in offs)
+    finally:
+        assert lib.fa_lp_plan_destroy(h) == 0
+
+
+def test_plan_cache_shares_identical_keys(lib):
+    st1, h1 = _create(lib, [0, 100, 300], heads=2)
+    st2, h2 = _create(lib, [0, 100, 300], heads=2)
+    st3, h3 = _create(lib, [0, 100, 300], heads=3)
+    try:
+        assert st1 == st2 == st3 == 0
+        assert h1.value == h2.value and h1.value != h3.value
+    finally:
+        for h in (h1, h2, h3):
+            assert lib.fa_lp_plan_destroy(h) == 0
+
+
+def test_calls_validate_before_touching_the_device(lib):
+    st, h = _create(lib, [0, 64], heads=1)
+    try:
+        # NULL views are rejected before any CUDA call
+        assert lib.fa_lp_quantize(h, None, 128, 128, None, 128, 128, None, 128, 128, None) == 1
+        # forward before quantize is out of order
+        assert lib.fa_lp_forward_varlen(h, None, ctypes.c_void_p(16), 128, 128, None) == 6
+        assert lib.fa_lp_plan_set_wait_limit(h, 0) == 1
+        assert lib.fa_lp_plan_set_wait_limit(h, 5) == 0
+        assert lib.fa_lp_encode(3, None, 0, None, None) == 1
+    finally:
+        lib.fa_lp_plan_destroy(h)

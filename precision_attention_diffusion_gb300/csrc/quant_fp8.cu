@@ -122,11 +122,17 @@ __global__ void __launch_bounds__(256) fp8_pack_vt_kernel(const uint16_t* __rest
                                                           const BlockInfo* __restrict__ blocks,
                                                           int H, int64_t Tp,
                                                           const uint32_t* __restrict__ amax,
-                                                          uint8_t* __restrict__ vt) {
+                                                          uint8_t* __restrict__ vt,
+                                                          float* __restrict__ descale) {
   __shared__ __align__(16) uint8_t tile[kTile][kD + 4];
   const int b = blockIdx.x, h = blockIdx.y;
   const BlockInfo bi = blocks[b];
-  const float inv = inv_of(amax[2 * H + h]);
+  const uint32_t ab = amax[2 * H + h];
+  const float inv = inv_of(ab);
+  if (b == 0 && threadIdx.x == 0) {
+    const float a = __uint_as_float(ab);
+    descale[2 * H + h] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+  }
   const int sub = threadIdx.x & 15;
   for (int r = threadIdx.x >> 4; r < kTile; r += 16) {
     uint2 c = make_uint2(0u, 0u);
@@ -187,7 +193,8 @@ int launch_fp8_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t
                                              reinterpret_cast<float*>(ws + p.ws.descale));
   dim3 g3(nblk, unsigned(H));
   fp8_pack_vt_kernel<<<g3, 256, 0, stream>>>(vb, vst, vsh, p.d_blocks, H, p.tpad, amax,
-                                             ws + p.ws.v_codes);
+                                             ws + p.ws.v_codes,
+                                             reinterpret_cast<float*>(ws + p.ws.descale));
   return cuda_status(cudaGetLastError());
 }
 

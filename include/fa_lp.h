@@ -141,6 +141,12 @@ FA_LP_API int fa_lp_quantize(fa_lp_plan* plan, const void* q, int64_t q_stride_t
  *                    (out_stride_tok, out_stride_head), caller-owned. Only rows inside segments
  *                    are written; other rows are left untouched.
  *   stream         : cudaStream_t (as void*).
+ * FP8 arithmetic: S = (E4M3 Q codes . E4M3 K codes) accumulated in FP32 on the tensor cores;
+ * online softmax over 128-key tiles counted from each segment start, in log2 units with
+ * c = dq*dk*softmax_scale*log2(e); the reference maximum m is the first tile's row maximum and
+ * moves to a later tile's maximum M only when (M - m)*c > 8 (then O and l are rescaled by
+ * 2^((m - M)*c)); P = E4M3_rn(2^(S*c - m*c)) <= 256; l sums the quantized P; O accumulates
+ * P * V codes in FP32; out = BF16_rn(O * dv / l).
  * Errors: STATE (no quantize on this plan yet), INVALID_ARG, UNSUPPORTED, CUDA.
  */
 FA_LP_API int fa_lp_forward_varlen(fa_lp_plan* plan, const int32_t* cu_seqlens_dev, void* out,

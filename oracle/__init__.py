@@ -62,8 +62,8 @@ def lib() -> ctypes.CDLL:
             L.orc_fp8_quantize.argtypes = [P, i64, i32, i64, i64, P, P, i32]
             L.orc_attn_exact.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32, P, i32,
                                          f64, P, i64, P, i32]
-            L.orc_attn_fp8.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, i32, i32, P, i64,
-                                       P, P, i32]
+            L.orc_attn_fp8.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, i32, i32, f64, P,
+                                       i64, P, P, i32]
             L.orc_nvfp4_kmean.argtypes = [P, i64, i64, i64, i32, P, i32, P, i32]
             L.orc_nvfp4_qblock_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_qblock_offsets.restype = i64
             L.orc_nvfp4_vgroup_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_vgroup_offsets.restype = i64
@@ -153,8 +153,11 @@ def attn_exact(q, k, v, cu, rows, scale, nthreads=0):
     return out
 
 
-def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, nthreads=0):
-    """C2: FP8-emulating attention from codes/descales -> (out fp64 [n,128], out bf16 bits)."""
+def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, tau=0.0,
+             nthreads=0):
+    """C2: FP8-emulating attention from codes/descales -> (out fp64 [n,128], out bf16 bits).
+    n_kv: key-tile width; tau: threshold (log2 units) for moving the reference maximum, 0 = the
+    exact running maximum; p_shift: power-of-two shift applied to P before E4M3 rounding."""
     cq, ck, cv = (np.ascontiguousarray(a, np.uint8) for a in (cq, ck, cv))
     dq, dk, dv = (np.ascontiguousarray(a, np.float32) for a in (dq, dk, dv))
     cu = np.ascontiguousarray(cu, np.int32)
@@ -162,7 +165,8 @@ def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, nthre
     o64 = np.empty((rows.shape[0], D), np.float64)
     o16 = np.empty((rows.shape[0], D), np.uint16)
     lib().orc_attn_fp8(_p(cq), _p(ck), _p(cv), _p(dq), _p(dk), _p(dv), cq.shape[0], cq.shape[1],
-                       _p(cu), len(cu) - 1, float(scale), int(n_kv), int(p_shift), _p(rows),
+                       _p(cu), len(cu) - 1, float(scale), int(n_kv), int(p_shift), float(tau),
+                       _p(rows),
                        rows.shape[0], _p(o64), _p(o16), _threads(nthreads))
     return o64, o16
 

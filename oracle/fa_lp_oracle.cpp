@@ -20,8 +20,11 @@
 //  r3  E4M3: round to nearest, ties to even, saturate to +-448, sign of zero kept, subnormals kept.
 //  r4  FP8 P is the unscaled exp(S - m) in [0,1], rounded through fp32 then to E4M3 (shift p = 0;
 //      p is a parameter so that a kernel using a power-of-two shift can be replayed).
-//  r5  online softmax over key tiles of n_kv keys counted from the segment start, with the exact
-//      running maximum after every tile (no lazy threshold).
+//  r5  online softmax over key tiles of n_kv keys counted from the segment start. The reference
+//      maximum m starts at the first tile's maximum and moves to a later tile's maximum only when
+//      that exceeds m by more than tau (in log2 units, i.e. by a factor 2^tau in probability);
+//      tau = 0 is the exact running maximum. Both are parameters so that the kernel's own rule
+//      is replayed.
 //  r6  the softmax denominator l sums the quantized probabilities.
 //  r7  NVFP4 Q blocks and V key groups start at each segment's first token; partial last block's
 //      mean is over present rows; padded V keys are zero.
@@ -295,11 +298,12 @@ void orc_attn_exact(const uint16_t* q, int64_t qst, int64_t qsh,
 void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
                   const float* dq, const float* dk, const float* dv,
                   int64_t T, int H, const int32_t* cu, int nseg, double scale, int n_kv,
-                  int p_shift, const int64_t* rows, int64_t nrows, double* out64,
+                  int p_shift, double tau, const int64_t* rows, int64_t nrows, double* out64,
                   uint16_t* out16, int nthreads) {
   (void)T;
   const double inf = std::numeric_limits<double>::infinity();
   const double pscale = std::ldexp(1.0, p_shift);
+  const double tau_nat = tau * std::log(2.0);  // threshold in the natural-log units of S
   parallel_for(nrows, nthreads, [&](int64_t r) {
     const int64_t t = rows[2 * r];
     const int h = static_cast<int>(rows[2 * r + 1]);
@@ -320,7 +324,7 @@ void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
         sc[j - j0] = acc * sfac;
         mt = std::max(mt, sc[j - j0]);
       }
-      const double m_new = std::max(m, mt);
+      const double m_new = (m == -inf || mt > m + tau_nat) ? mt : m;
       const double alpha = (m == -inf) ? 0.0 : std::exp(m - m_new);
       l *= alpha;
       for (int c = 0; c < kD; ++c) o[c] *= alpha;

@@ -15,10 +15,11 @@
 //     in the order S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} ..., so that one tile's softmax
 //     overlaps the other tile's tensor work;
 //   * warps 0-3 / 4-7 run the online softmax of Q0 / Q1, one thread per query row (row == TMEM
-//     lane), with the exact running maximum after every 128-key tile (reading r5):
-//       m' = max(m, max_j S_j);  alpha = 2^((m - m') c);  P_j = E4M3(2^(S_j c - m' c))
-//       l = l alpha + sum_j P_j (the quantized P, reading r6);  O = O alpha (skipped when every
-//       row of the warp has alpha == 1, which is exact) before P V_j accumulates,
+//     lane). The reference maximum m is the first tile's maximum and moves to a later tile's
+//     maximum M only when (M - m) c > 8 (reading r5 with tau = 8; the pages leave the rule open):
+//       alpha = 2^((m - m') c);  P_j = E4M3(2^(S_j c - m' c)) <= 256
+//       l = l alpha + sum_j P_j (the quantized P, reading r6);  O = O alpha before P V_j
+//       accumulates (only when some row of the warp moved its reference; alpha == 1 otherwise),
 //     where S is the raw E4M3 dot product and c = dq dk softmax_scale log2(e);
 //   * epilogue: out = BF16_rn(O dv / l) for rows inside the segment only.
 // Every barrier wait is bounded; on expiry the kernel records an error, drains its in-flight
@@ -39,6 +40,9 @@ constexpr int kMmaWarp = 9;
 constexpr uint32_t kTileBytes = 128 * 128;
 constexpr uint32_t kIdesc = idesc_f8f6f4(128, 128, 0, 0);  // E4M3 x E4M3 -> F32, M=N=128
 constexpr long long kDrainSpins = 1ll << 20;
+// Threshold (log2 units) by which a key tile's maximum must exceed the reference maximum before
+// the reference moves (and O, l are rescaled). P = 2^(S c - m c) <= 2^kTau stays inside E4M3.
+constexpr float kTau = 8.0f;
 
 struct Smem {
   uint8_t q[2][kTileBytes];
@@ -187,6 +191,20 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const Wor
   drain_phase(smem_u32(&S.bar_drain), 0);
 }
 
+// Row maximum of 128 values: eight independent 3-input-max chains, then a 3-level combine
+// (depth 10 instead of a 127-deep serial chain).
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    acc[k] = s[k];
+#pragma unroll
+    for (int i = 1; i < 16; i += 2)
+      acc[k] = max3f(acc[k], s[k + 8 * i], s[k + 8 * (i + 1 < 16 ? i + 1 : i)]);
+  }
+  return max3f(max3f(acc[0], acc[1], acc[2]), max3f(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+}
+
 __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
                                                      const WorkItem& wi, const SegInfo& sg,
                                                      uint32_t tmem, int t, int wq, int lane) {
@@ -198,7 +216,7 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
   const uint32_t s_addr = tmem + uint32_t(128 * t) + lane_off;
   const uint32_t o_addr = tmem + 256u + uint32_t(128 * t) + lane_off;
   const int last_valid = sg.len - (n_kv - 1) * kTile;  // keys of the last tile, 1..128
-  float m = -INFINITY, l = 0.f;
+  float m = -INFINITY, l = 0.f;                          // reference maximum (raw units), sum
   bool ok = true;
   for (int j = 0; j < n_kv; ++j) {
     ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_s[t]), j & 1, S, a, kRoleSoftmax));
@@ -216,37 +234,38 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
       for (int i = 0; i < 128; ++i)
         if (i >= last_valid) s[i] = -INFINITY;
     }
-    float mx = s[0];
-#pragma unroll
-    for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
-    const float m_new = fmaxf(m, mx);
-    const float alpha = (m_new == m) ? 1.f : ex2_approx((m - m_new) * c);
-    const float mc = m_new * c;
+    // Reference maximum: moves only when the tile's maximum exceeds it by more than kTau (log2
+    // units), so P stays below 2^kTau = 256 < 448 and O needs rescaling only on such moves.
+    const float mx = row_max128(s);
+    const bool move = (m == -INFINITY) || ((mx - m) * c > kTau);
+    const float m_new = move ? mx : m;
+    const float alpha = move ? ex2_approx((m - m_new) * c) : 1.f;  // m = -inf gives 0
+    const float nmc = -m_new * c;
     uint32_t pk[32];
     float rs = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float p[8];
+    for (int g = 0; g < 4; ++g) {  // 32 keys per group
+      uint32_t hs[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) p[e] = ex2_approx(fmaf(s[8 * i + e], c, -mc));
-      const uint16_t c01 = cvt_e4m3x2(p[0], p[1]), c23 = cvt_e4m3x2(p[2], p[3]);
-      const uint16_t c45 = cvt_e4m3x2(p[4], p[5]), c67 = cvt_e4m3x2(p[6], p[7]);
-      pk[2 * i] = uint32_t(c01) | (uint32_t(c23) << 16);
-      pk[2 * i + 1] = uint32_t(c45) | (uint32_t(c67) << 16);
-      // sum of the 8 quantized values: pairs and quads of E4M3 values in [0, 1] add exactly in
-      // f16 (multiples of 2^-9 below 4 need <= 11 significant bits); the rest in fp32
-      const uint32_t h01 = cvt_e4m3x2_to_f16x2(c01), h23 = cvt_e4m3x2_to_f16x2(c23);
-      const uint32_t h45 = cvt_e4m3x2_to_f16x2(c45), h67 = cvt_e4m3x2_to_f16x2(c67);
-      const __half2 q4 = __hadd2(__hadd2(*reinterpret_cast<const __half2*>(&h01),
-                                         *reinterpret_cast<const __half2*>(&h23)),
-                                 __hadd2(*reinterpret_cast<const __half2*>(&h45),
-                                         *reinterpret_cast<const __half2*>(&h67)));
-      const float2 f = __half22float2(q4);
+      for (int i = 0; i < 8; ++i) {  // 4 keys
+        const int k0 = 32 * g + 4 * i;
+        float x0, x1, x2, x3;
+        fma2(x0, x1, s[k0], s[k0 + 1], c, nmc);
+        fma2(x2, x3, s[k0 + 2], s[k0 + 3], c, nmc);
+        const uint16_t c01 = cvt_e4m3x2(ex2_approx(x0), ex2_approx(x1));
+        const uint16_t c23 = cvt_e4m3x2(ex2_approx(x2), ex2_approx(x3));
+        pk[8 * g + i] = uint32_t(c01) | (uint32_t(c23) << 16);
+        // the quantized values, back in f16 (exact), summed pairwise
+        hs[i] = hadd2_u32(cvt_e4m3x2_to_f16x2(c01), cvt_e4m3x2_to_f16x2(c23));
+      }
+      const uint32_t h4 = hadd2_u32(hadd2_u32(hadd2_u32(hs[0], hs[1]), hadd2_u32(hs[2], hs[3])),
+                                    hadd2_u32(hadd2_u32(hs[4], hs[5]), hadd2_u32(hs[6], hs[7])));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h4));
       rs += f.x + f.y;
     }
     l = l * alpha + rs;
     tmem_st32(s_addr, pk);
-    if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+    if (j > 0 && __any_sync(0xffffffffu, move)) {
       ok = __all_sync(0xffffffffu,
                       wait_phase(smem_u32(&S.bar_o[t]), (j - 1) & 1, S, a, kRoleSoftmax));
       if (!ok) break;

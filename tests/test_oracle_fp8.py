@@ -260,3 +260,36 @@ def test_fp8_varlen_rows_match_single_segment_runs():
         cq, ck, cv, dq, dk, dv = qz
         alone, _ = oracle.attn_fp8(cq[a:b], ck[a:b], cv[a:b], dq, dk, dv, [0, b - a], [(t - a, h)], SCALE)
         assert np.array_equal(packed[r], alone[0])
+
+
+def test_fp8_lazy_reference_max_rule():
+    """tau > 0: while no later tile's maximum exceeds the first tile's by more than tau (log2
+    units), every probability is taken against the first tile's maximum -- checked with the
+    global formula on a 3-tile row, using torch's E4M3 rounding; tau = 0 is the exact rule."""
+    T, H = 300, 1
+    q, k, v = inputs.qkv_separate(T, H, seed=31)
+    cq, ck, cv, dq, dk, dv = quant3(q, k, v)
+    rows = [(t, 0) for t in range(0, T, 29)]
+    dec = lambda c: torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).double().numpy()
+    lazy, _ = oracle.attn_fp8(cq, ck, cv, dq, dk, dv, [0, T], rows, SCALE, n_kv=128, tau=8.0)
+    for r, (t, h) in enumerate(rows):
+        s = (dec(cq[t, h]) @ dec(ck[:, h]).T) * (float(dq[h]) * float(dk[h]) * SCALE)
+        m0 = s[:128].max()
+        assert s.max() - m0 <= 8 * np.log(2)  # the rule never moves the reference here
+        p = np.exp(s - m0).astype(np.float32)
+        pq = torch.from_numpy(p).to(torch.float8_e4m3fn).double().numpy()
+        want = (pq @ dec(cv[:, h])) * float(dv[h]) / pq.sum()
+        assert np.allclose(lazy[r], want, rtol=1e-12, atol=1e-14)
+    exact0, _ = oracle.attn_fp8(cq, ck, cv, dq, dk, dv, [0, T], rows, SCALE, n_kv=128, tau=0.0)
+    exact1, _ = oracle.attn_fp8(cq, ck, cv, dq, dk, dv, [0, T], rows, SCALE, n_kv=128)
+    assert np.array_equal(exact0, exact1)
+    # a tile whose maximum jumps by more than tau moves the reference: tile 2 holds a key 12 log2
+    # units above the rest, so the result equals the exact rule's on that row
+    k2 = k.clone()
+    k2[260] = q[0] * 4.0
+    cq, ck, cv, dq, dk, dv = quant3(q, k2, v)
+    a, _ = oracle.attn_fp8(cq, ck, cv, dq, dk, dv, [0, T], [(0, 0)], SCALE, tau=8.0)
+    b, _ = oracle.attn_fp8(cq, ck, cv, dq, dk, dv, [0, T], [(0, 0)], SCALE, tau=0.0)
+    s = (dec(cq[0, 0]) @ dec(ck[:, 0]).T) * (float(dq[0]) * float(dk[0]) * SCALE)
+    assert s[256:].max() - s[:256].max() > 8 * np.log(2)
+    assert np.allclose(a, b, rtol=1e-3)

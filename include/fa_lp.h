@@ -142,7 +142,7 @@ FA_LP_API int fa_lp_quantize(fa_lp_plan* plan, const void* q, int64_t q_stride_t
  *                    are written; other rows are left untouched.
  *   stream         : cudaStream_t (as void*).
  * FP8 arithmetic: S = (E4M3 Q codes . E4M3 K codes) accumulated in FP32 on the tensor cores;
- * online softmax over 128-key tiles counted from each segment start, in log2 units with
+ * online softmax over 64-key tiles counted from each segment start, in log2 units with
  * c = dq*dk*softmax_scale*log2(e); the reference maximum m is the first tile's row maximum and
  * moves to a later tile's maximum M only when (M - m)*c > 8 (then O and l are rescaled by
  * 2^((m - M)*c)); P = E4M3_rn(2^(S*c - m*c)) <= 256; l sums the quantized P; O accumulates
@@ -202,10 +202,11 @@ FA_LP_API int fa_lp_copy_quantized(const fa_lp_plan* plan, int which, void* dst,
  */
 FA_LP_API int fa_lp_get_last_error(fa_lp_plan* plan, int* device_status);
 
-/* Upper bound on the spin iterations of every device-side barrier wait of this plan's
- * kernels (default 2^26 probes, seconds or more). A wait that reaches it records an error, the kernel
- * drains its in-flight copies, frees its tensor memory and returns. Small values are for tests of
- * that path. spins >= 1. */
+/* Upper bound on the probes of every device-side barrier wait of this plan's kernels. A probe
+ * parks the waiting thread for at most about 100 microseconds; the default 20000 probes bounds a
+ * wait at about 2 seconds. A wait that reaches the bound records an error (see
+ * fa_lp_get_last_error), makes every CTA of the launch stop, drains in-flight copies and MMAs,
+ * frees tensor memory and returns. Small values are for tests of that path. spins >= 1. */
 FA_LP_API int fa_lp_plan_set_wait_limit(fa_lp_plan* plan, int64_t spins);
 
 /* Free the workspace of `device` (stream-ordered on `stream`). Plans stay valid; the next

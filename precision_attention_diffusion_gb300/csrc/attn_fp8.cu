@@ -8,18 +8,21 @@
 //
 // GB300 design (the SM120 kernel's 128x32 mma.sync tile is prior art, not the blueprint):
 //   * one CTA = one (segment, head) and two 128-row query tiles Q0, Q1 sharing every K/V tile;
-//   * warp 8 issues TMA loads (Q once; K_j and V^T_j into a 3-stage ring, 128-byte swizzle);
-//   * warp 9 allocates the 512 tensor-memory columns and issues tcgen05.mma kind::f8f6f4:
-//       S_t = Q_t K_j^T   (A, B from shared memory, FP32 accumulator in TMEM columns [128t, +128))
-//       O_t += P_t V_j    (A = P_t from TMEM, E4M3, 4 per column; O_t in columns [256+128t, +128))
-//     in the order S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} ..., so that one tile's softmax
-//     overlaps the other tile's tensor work;
+//   * warp 8 issues TMA loads: Q once, then 128-key K and V^T tiles into a 4-stage ring with
+//     128-byte swizzle;
+//   * warp 9 allocates tensor memory; warps 9 and 10 issue the tcgen05.mma kind::f8f6f4 of query
+//     tiles 0 and 1 (two independent in-order streams) on 64-key sub-tiles u:
+//       S_t(u) = Q_t K(u)^T   (M=128, N=64;  A, B from shared memory)
+//       O_t += P_t(u) V(u)    (M=128, N=128; A = P_t from tensor memory)
+//   * tensor memory (all 512 columns): per query tile two 64-column S buffers and a 128-column O;
+//     P_t(u) (64 E4M3 per row = 16 columns) is written over the S buffer it was computed from, and
+//     S_t(u+2) is issued into that buffer right after PV_t(u), so S is always one sub-tile ahead
+//     of the softmax;
 //   * warps 0-3 / 4-7 run the online softmax of Q0 / Q1, one thread per query row (row == TMEM
-//     lane). The reference maximum m is the first tile's maximum and moves to a later tile's
-//     maximum M only when (M - m) c > 8 (reading r5 with tau = 8; the pages leave the rule open):
-//       alpha = 2^((m - m') c);  P_j = E4M3(2^(S_j c - m' c)) <= 256
-//       l = l alpha + sum_j P_j (the quantized P, reading r6);  O = O alpha before P V_j
-//       accumulates (only when some row of the warp moved its reference; alpha == 1 otherwise),
+//     lane). The reference maximum m is the first sub-tile's maximum and moves to a later
+//     sub-tile's maximum M only when (M - m) c > 8 (reading r5 with tau = 8; the pages leave the
+//     rule open): alpha = 2^((m - M) c), O *= alpha (only when a row of the warp moved),
+//     P = E4M3(2^(S c - m c)) <= 256, l = l alpha + sum of the quantized P (reading r6),
 //     where S is the raw E4M3 dot product and c = dq dk softmax_scale log2(e);
 //   * epilogue: out = BF16_rn(O dv / l) for rows inside the segment only.
 // Every barrier wait is bounded; on expiry the kernel records an error, drains its in-flight
@@ -33,16 +36,23 @@
 namespace falp {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr int kThreads = 352;
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTileBytes = 128 * 128;
-constexpr uint32_t kIdesc = idesc_f8f6f4(128, 128, 0, 0);  // E4M3 x E4M3 -> F32, M=N=128
-constexpr long long kDrainSpins = 1ll << 20;
-// Threshold (log2 units) by which a key tile's maximum must exceed the reference maximum before
+constexpr int kMmaWarp = 9;   // warps 9 and 10 issue the MMAs of query tiles 0 and 1
+constexpr int kSub = 64;                            // keys per sub-tile
+constexpr uint32_t kTileBytes = 128 * 128;          // one 128x128 E4M3 tile
+constexpr uint32_t kIdescS = idesc_f8f6f4(128, kSub, 0, 0);   // E4M3 x E4M3 -> F32, N=64
+constexpr uint32_t kIdescPV = idesc_f8f6f4(128, 128, 0, 0);   // N = 128 channels
+constexpr uint32_t kProbeNs = 100000;         // one parked probe: at most ~100 us
+constexpr long long kDrainProbes = 20000;      // drains give up after ~2 s
+// Threshold (log2 units) by which a sub-tile's maximum must exceed the reference maximum before
 // the reference moves (and O, l are rescaled). P = 2^(S c - m c) <= 2^kTau stays inside E4M3.
 constexpr float kTau = 8.0f;
+// tensor-memory columns of query tile t: S buffer b at 128t + 64b (P of that sub-tile is written
+// over its first 16 columns once S has been read), O at 256 + 128t
+__device__ __forceinline__ uint32_t col_s(int t, int b) { return 128u * uint32_t(t) + 64u * uint32_t(b); }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * uint32_t(t); }
 
 struct Smem {
   uint8_t q[2][kTileBytes];
@@ -52,10 +62,10 @@ struct Smem {
   uint64_t bar_k[kStages];
   uint64_t bar_v[kStages];
   uint64_t bar_free[kStages];
-  uint64_t bar_s[2];
-  uint64_t bar_p[2];
-  uint64_t bar_o[2];
-  uint64_t bar_drain;
+  uint64_t bar_s[2][2];  // [t][u & 1]: S_t(u) written (MMA commit)
+  uint64_t bar_p[2][2];  // [t][u & 1]: P_t(u) written, O rescaled (128 arrivals)
+  uint64_t bar_o[2][2];  // [t][u & 1]: PV_t(u) done (MMA commit)
+  uint64_t bar_drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -77,20 +87,19 @@ struct AttnArgs {
 
 enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4 };
 
-// Bounded wait on one mbarrier phase. Returns false when the CTA aborts (this wait expired, or
-// another role's did).
+// Bounded wait on one mbarrier phase. Each probe parks the thread for up to kProbeNs; after
+// a.spin_limit unsuccessful probes the wait expires. Returns false when the CTA aborts (this wait
+// expired, or another wait of this launch did).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Smem& S,
                                            const AttnArgs& a, int role) {
   long long n = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kProbeNs)) {
     if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
-    ++n;
-    // another CTA of this launch gave up: stop too (polled rarely, off the fast path)
-    if ((n & 1023) == 0 && *reinterpret_cast<volatile int*>(a.abort_word) == a.gen) {
+    if (*reinterpret_cast<volatile int*>(a.abort_word) == a.gen) {  // another CTA gave up
       *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
       return false;
     }
-    if (n >= a.spin_limit) {
+    if (++n >= a.spin_limit) {
       *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
       atomicExch(a.abort_word, a.gen);
       atomicCAS(a.err, 0, 0x100 | role);
@@ -102,8 +111,8 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Smem& 
 
 // Wait used while draining after an abort: ignores the abort flag, bounded separately.
 __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
-  for (long long n = 0; n < kDrainSpins; ++n)
-    if (mbar_try_wait(bar, parity)) return;
+  for (long long n = 0; n < kDrainProbes; ++n)
+    if (mbar_try_wait_sleep(bar, parity, kProbeNs)) return;
 }
 
 __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
@@ -136,115 +145,132 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
   }
 }
 
+// MMA role of query tile t, on a whole warp, converged; only the MMA and commit instructions are
+// issued, by one elected lane (lane 0 every time: tcgen05.commit tracks that lane's MMAs). The two
+// query tiles have independent in-order MMA streams. S is computed two sub-tiles ahead: S_t(u+2)
+// goes to the buffer of S_t(u) right after PV_t(u), which read P_t(u) from that buffer (the
+// tensor pipe executes one thread's MMAs in issue order).
 __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const WorkItem& wi,
-                                           const SegInfo& sg, uint32_t tmem) {
-  const int n_kv = sg.nblk;
-  const int nq = wi.nq;
-  const uint32_t s_t[2] = {tmem, tmem + 128};
-  const uint32_t o_t[2] = {tmem + 256, tmem + 384};
-  const uint32_t qa[2] = {smem_u32(S.q[0]), smem_u32(S.q[1])};
-  auto issue_s = [&](int t, int st) {
-    const uint32_t kb = smem_u32(S.k[st]);
+                                           const SegInfo& sg, uint32_t tmem, int t) {
+  const int n_sub = (sg.len + kSub - 1) / kSub;
+  const uint32_t qa = smem_u32(S.q[0]) + uint32_t(t) * kTileBytes;
+  const uint32_t k0 = smem_u32(S.k[0]);
+  const uint32_t v0 = smem_u32(S.v[0]);
+  const uint32_t d_o = tmem + col_o(t);
+  // S_t(u) = Q_t K(u)^T: K rows [64h, 64h + 64) of the stage holding key tile u / 2
+  auto issue_s = [&](int u) {
+    const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
+    const uint32_t kb = k0 + (j % kStages) * kTileBytes + h * (kSub * 128);
+    const uint32_t d = tmem + col_s(t, h);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_f8f6f4_ss(s_t[t], sdesc_kmajor_sw128(qa[t] + 32 * kk), sdesc_kmajor_sw128(kb + 32 * kk),
-                    kIdesc, kk > 0);
-    mma_commit(smem_u32(&S.bar_s[t]));
+      mma_f8f6f4_ss_elect(d, sdesc_kmajor_sw128(qa + 32 * kk), sdesc_kmajor_sw128(kb + 32 * kk),
+                          kIdescS, kk > 0);
+    mma_commit_elect(smem_u32(&S.bar_s[t][h]));
   };
-  auto issue_pv = [&](int t, int st, bool acc) {
-    const uint32_t vb = smem_u32(S.v[st]);
+  // O_t += P_t(u) V(u): keys [64h, 64h + 64) are bytes [64h, 64h + 64) of each V^T row; P from
+  // the first 16 columns of S buffer h
+  auto issue_pv = [&](int u) {
+    const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
+    const uint32_t vb = v0 + (j % kStages) * kTileBytes + h * kSub;
+    const uint32_t pa = tmem + col_s(t, h);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f8f6f4_ts(o_t[t], s_t[t] + 8 * kk, sdesc_kmajor_sw128(vb + 32 * kk), kIdesc,
-                    (acc || kk > 0) ? 1u : 0u);
-    mma_commit(smem_u32(&S.bar_o[t]));
+    for (int kk = 0; kk < 2; ++kk)
+      mma_f8f6f4_ts_elect(d_o, pa + 8 * kk, sdesc_kmajor_sw128(vb + 32 * kk), kIdescPV,
+                          (u > 0 || kk > 0) ? 1u : 0u);
+    mma_commit_elect(smem_u32(&S.bar_o[t][h]));
+  };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_phase(smem_u32(bar), parity, S, a, kRoleMma));
   };
   do {
-    if (!wait_phase(smem_u32(&S.bar_q), 0, S, a, kRoleMma)) break;
-    if (!wait_phase(smem_u32(&S.bar_k[0]), 0, S, a, kRoleMma)) break;
+    if (!wait(&S.bar_q, 0)) break;
+    if (!wait(&S.bar_k[0], 0)) break;
     tc_fence_after();
-    issue_s(0, 0);
-    if (nq == 2) issue_s(1, 0);
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % kStages;
-      const int j1 = j + 1, st1 = j1 % kStages;
-      if (!wait_phase(smem_u32(&S.bar_v[st]), (j / kStages) & 1, S, a, kRoleMma)) break;
-      if (!wait_phase(smem_u32(&S.bar_p[0]), j & 1, S, a, kRoleMma)) break;
+    issue_s(0);
+    if (n_sub > 1) issue_s(1);  // sub-tile 1 lies in key tile 0 as well
+    bool ok = true;
+    for (int u = 0; u < n_sub && ok; ++u) {
+      const int j = u >> 1, h = u & 1;
+      if (h == 0) {
+        ok = wait(&S.bar_v[j % kStages], (j / kStages) & 1);
+        if (!ok) break;
+      }
+      ok = wait(&S.bar_p[t][h], (u >> 1) & 1);
+      if (!ok) break;
       tc_fence_after();
-      issue_pv(0, st, j > 0);
-      if (j1 < n_kv) {
-        if (!wait_phase(smem_u32(&S.bar_k[st1]), (j1 / kStages) & 1, S, a, kRoleMma)) break;
-        tc_fence_after();
-        issue_s(0, st1);
+      issue_pv(u);
+      if (h == 1 || u + 1 == n_sub) mma_commit_elect(smem_u32(&S.bar_free[j % kStages]));
+      const int u2 = u + 2;
+      if (u2 < n_sub) {
+        if ((u2 & 1) == 0) {  // sub-tile u+2 opens key tile j+1
+          const int j2 = u2 >> 1;
+          ok = wait(&S.bar_k[j2 % kStages], (j2 / kStages) & 1);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_s(u2);
       }
-      if (nq == 2) {
-        if (!wait_phase(smem_u32(&S.bar_p[1]), j & 1, S, a, kRoleMma)) break;
-        tc_fence_after();
-        issue_pv(1, st, j > 0);
-      }
-      mma_commit(smem_u32(&S.bar_free[st]));
-      if (nq == 2 && j1 < n_kv) issue_s(1, st1);
     }
   } while (false);
   // Every MMA issued so far must finish before the tensor memory is released.
-  mma_commit(smem_u32(&S.bar_drain));
-  drain_phase(smem_u32(&S.bar_drain), 0);
+  mma_commit_elect(smem_u32(&S.bar_drain[t]));
+  drain_phase(smem_u32(&S.bar_drain[t]), 0);
 }
 
-// Row maximum of 128 values: eight independent 3-input-max chains, then a 3-level combine
-// (depth 10 instead of a 127-deep serial chain).
-__device__ __forceinline__ float row_max128(const float (&s)[128]) {
-  float acc[8];
+// Row maximum of 64 values: four independent 3-input-max chains, then a combine.
+__device__ __forceinline__ float row_max64(const float (&s)[64]) {
+  float acc[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    acc[k] = s[k];
+  for (int k = 0; k < 4; ++k) {
+    acc[k] = max3f(s[k], s[k + 4], s[k + 8]);
 #pragma unroll
-    for (int i = 1; i < 16; i += 2)
-      acc[k] = max3f(acc[k], s[k + 8 * i], s[k + 8 * (i + 1 < 16 ? i + 1 : i)]);
+    for (int i = 3; i < 15; i += 2) acc[k] = max3f(acc[k], s[k + 4 * i], s[k + 4 * (i + 1)]);
+    acc[k] = fmaxf(acc[k], s[k + 60]);
   }
-  return max3f(max3f(acc[0], acc[1], acc[2]), max3f(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+  return fmaxf(max3f(acc[0], acc[1], acc[2]), acc[3]);
 }
 
 __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
                                                      const WorkItem& wi, const SegInfo& sg,
                                                      uint32_t tmem, int t, int wq, int lane) {
-  const int n_kv = sg.nblk;
+  const int n_sub = (sg.len + kSub - 1) / kSub;
   const int h = wi.head;
   const float c = a.descale[h] * a.descale[a.H + h] * a.scale_log2;
   const float dv = a.descale[2 * a.H + h];
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t s_addr = tmem + uint32_t(128 * t) + lane_off;
-  const uint32_t o_addr = tmem + 256u + uint32_t(128 * t) + lane_off;
-  const int last_valid = sg.len - (n_kv - 1) * kTile;  // keys of the last tile, 1..128
-  float m = -INFINITY, l = 0.f;                          // reference maximum (raw units), sum
+  const uint32_t o_addr = tmem + col_o(t) + lane_off;
+  const int last_valid = sg.len - (n_sub - 1) * kSub;  // keys of the last sub-tile, 1..64
+  float m = -INFINITY, l = 0.f;                         // reference maximum (raw units), sum
   bool ok = true;
-  for (int j = 0; j < n_kv; ++j) {
-    ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_s[t]), j & 1, S, a, kRoleSoftmax));
+  for (int u = 0; u < n_sub; ++u) {
+    const int b = u & 1;
+    const uint32_t s_addr = tmem + col_s(t, b) + lane_off;
+    ok = __all_sync(0xffffffffu,
+                    wait_phase(smem_u32(&S.bar_s[t][b]), (u >> 1) & 1, S, a, kRoleSoftmax));
     if (!ok) break;
     tc_fence_after();
-    uint32_t r[4][32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tmem_ld32(s_addr + 32 * i, r[i]);
+    uint32_t r[2][32];
+    tmem_ld32(s_addr, r[0]);
+    tmem_ld32(s_addr + 32, r[1]);
     tmem_wait_ld();
-    float s[128];
+    float s[64];
 #pragma unroll
-    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i >> 5][i & 31]);
-    if (j == n_kv - 1 && last_valid < kTile) {
+    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i >> 5][i & 31]);
+    if (u == n_sub - 1 && last_valid < kSub) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i)
+      for (int i = 0; i < 64; ++i)
         if (i >= last_valid) s[i] = -INFINITY;
     }
-    // Reference maximum: moves only when the tile's maximum exceeds it by more than kTau (log2
-    // units), so P stays below 2^kTau = 256 < 448 and O needs rescaling only on such moves.
-    const float mx = row_max128(s);
+    const float mx = row_max64(s);
     const bool move = (m == -INFINITY) || ((mx - m) * c > kTau);
     const float m_new = move ? mx : m;
     const float alpha = move ? ex2_approx((m - m_new) * c) : 1.f;  // m = -inf gives 0
     const float nmc = -m_new * c;
-    uint32_t pk[32];
+    uint32_t pk[16];
     float rs = 0.f;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {  // 32 keys per group
+    for (int g = 0; g < 2; ++g) {  // 32 keys per group
       uint32_t hs[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {  // 4 keys
@@ -255,19 +281,21 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
         const uint16_t c01 = cvt_e4m3x2(ex2_approx(x0), ex2_approx(x1));
         const uint16_t c23 = cvt_e4m3x2(ex2_approx(x2), ex2_approx(x3));
         pk[8 * g + i] = uint32_t(c01) | (uint32_t(c23) << 16);
-        // the quantized values, back in f16 (exact), summed pairwise
+        // the quantized values, back in f16 (exact), summed pairwise (reading r6: l sums the
+        // quantized P)
         hs[i] = hadd2_u32(cvt_e4m3x2_to_f16x2(c01), cvt_e4m3x2_to_f16x2(c23));
       }
-      const uint32_t h4 = hadd2_u32(hadd2_u32(hadd2_u32(hs[0], hs[1]), hadd2_u32(hs[2], hs[3])),
+      const uint32_t h8 = hadd2_u32(hadd2_u32(hadd2_u32(hs[0], hs[1]), hadd2_u32(hs[2], hs[3])),
                                     hadd2_u32(hadd2_u32(hs[4], hs[5]), hadd2_u32(hs[6], hs[7])));
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h4));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h8));
       rs += f.x + f.y;
     }
     l = l * alpha + rs;
-    tmem_st32(s_addr, pk);
-    if (j > 0 && __any_sync(0xffffffffu, move)) {
-      ok = __all_sync(0xffffffffu,
-                      wait_phase(smem_u32(&S.bar_o[t]), (j - 1) & 1, S, a, kRoleSoftmax));
+    tmem_st16(s_addr, pk);  // P over the first 16 columns of the S buffer just read
+    if (u > 0 && __any_sync(0xffffffffu, move)) {
+      // rescale O between PV_t(u-1) and PV_t(u)
+      ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_o[t][b ^ 1]), ((u - 1) >> 1) & 1,
+                                              S, a, kRoleSoftmax));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -282,12 +310,13 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(smem_u32(&S.bar_p[t]));
+    mbar_arrive(smem_u32(&S.bar_p[t][b]));
     m = m_new;
   }
   if (!ok) return;
-  ok = __all_sync(0xffffffffu,
-                  wait_phase(smem_u32(&S.bar_o[t]), (n_kv - 1) & 1, S, a, kRoleEpilogue));
+  // PV_t(n_sub - 1) done implies every earlier PV of this in-order stream is done
+  ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_o[t][(n_sub - 1) & 1]),
+                                          ((n_sub - 1) >> 1) & 1, S, a, kRoleEpilogue));
   if (!ok) return;
   tc_fence_after();
   const float f = dv / l;
@@ -302,14 +331,15 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
     uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * f,
-                                                     __uint_as_float(o[2 * e + 1]) * f);
-      w[e] = *reinterpret_cast<const uint32_t*>(&b);
+      const __nv_bfloat162 bb = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * f,
+                                                      __uint_as_float(o[2 * e + 1]) * f);
+      w[e] = *reinterpret_cast<const uint32_t*>(&bb);
     }
     if (valid) {
       uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * i);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+      for (int e = 0; e < 4; ++e)
+        d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
     }
   }
 }
@@ -330,14 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&S.bar_k[i]), 1);
       mbar_init(smem_u32(&S.bar_v[i]), 1);
-      mbar_init(smem_u32(&S.bar_free[i]), 1);
+      mbar_init(smem_u32(&S.bar_free[i]), wi.nq);  // one commit per query tile
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&S.bar_s[t]), 1);
-      mbar_init(smem_u32(&S.bar_p[t]), 128);
-      mbar_init(smem_u32(&S.bar_o[t]), 1);
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(smem_u32(&S.bar_s[t][x]), 1);
+        mbar_init(smem_u32(&S.bar_p[t][x]), 128);
+        mbar_init(smem_u32(&S.bar_o[t][x]), 1);
+      }
+      mbar_init(smem_u32(&S.bar_drain[t]), 1);
     }
-    mbar_init(smem_u32(&S.bar_drain), 1);
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -357,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     if (lane == 0) producer(&tm_q, &tm_k, &tm_v, S, a, wi, sg);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer(S, a, wi, sg, tmem);
-    __syncwarp();
+  } else if (warp >= kMmaWarp) {
+    const int t = warp - kMmaWarp;
+    if (t < wi.nq) mma_issuer(S, a, wi, sg, tmem, t);
   } else {
     const int t = warp >> 2;
     if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 3, lane);

@@ -8,7 +8,7 @@
 #include <cstdint>
 #include <vector>
 
-#include "../../include/fa_lp.h"
+#include "fa_lp.h"  // include/ is on the include path
 
 namespace falp {
 
@@ -66,7 +66,7 @@ struct fa_lp_plan {
   std::vector<falp::BlockInfo> blocks;
   std::vector<falp::WorkItem> work;
   falp::WsLayout ws;
-  int64_t spin_limit = int64_t(1) << 26;
+  int64_t spin_limit = 20000;  // parked probes of <= 100 us each: about 2 s per wait
   // device metadata (created on first use on the plan's device)
   void* dmeta = nullptr;
   falp::SegInfo* d_segs = nullptr;

@@ -1,7 +1,7 @@
 """FP8 E4M3 path on the GPU through the C ABI, against the oracle.
 
 Bar (the benchmark spec): quantized codes and descales bit-exact; output within relative RMS 1e-2 of the
-FP8-emulating oracle (C2, replaying the kernel's 128-key tiles and reference-max rule) and within
+FP8-emulating oracle (C2, replaying the kernel's 64-key tiles and reference-max rule) and within
 0.06 of FP64 exact attention (C1) on Gaussian inputs. Per row, the error is also bounded
 (relative RMS of any one row <= 5e-2 of C2) so that a single wrong row cannot hide in the mean.
 """
@@ -63,8 +63,8 @@ def check_codes(fa, plan, cu, q, k, v):
 
 
 # The kernel's online-softmax rule, as documented for fa_lp_forward_varlen in include/fa_lp.h:
-# 128-key tiles from each segment start; the reference maximum moves only by more than 8 (log2).
-KV_TILE, TAU = 128, 8.0
+# 64-key tiles from each segment start; the reference maximum moves only by more than 8 (log2).
+KV_TILE, TAU = 64, 8.0
 
 
 def oracle_fp8(nat, ds, cu, rows):
@@ -186,7 +186,7 @@ def test_device_wait_limit_returns_error_not_hang(fa):
     torch.cuda.synchronize()
     status = plan.last_error()
     assert status != 0 and (status & 0xFF00) == 0x100
-    plan.set_wait_limit(1 << 26)
+    plan.set_wait_limit(20000)
     plan.attention(q.cuda(), k.cuda(), v.cuda(), out=out)
     torch.cuda.synchronize()
     assert plan.last_error() == 0

@@ -202,9 +202,10 @@ FA_LP_API int fa_lp_copy_quantized(const fa_lp_plan* plan, int which, void* dst,
  */
 FA_LP_API int fa_lp_get_last_error(fa_lp_plan* plan, int* device_status);
 
-/* Upper bound on the probes of every device-side barrier wait of this plan's kernels. A probe
- * parks the waiting thread for at most about 100 microseconds; the default 20000 probes bounds a
- * wait at about 2 seconds. A wait that reaches the bound records an error (see
+/* Upper bound on the probes of every device-side barrier wait of this plan's kernels. The first
+ * 64 probes of a wait spin; each later probe parks the waiting thread for at most about 100
+ * microseconds, so the default 20000 probes bounds a wait at about 2 seconds. With a limit below
+ * 64 every probe is a non-blocking poll, so that a test can make a wait expire deterministically. A wait that reaches the bound records an error (see
  * fa_lp_get_last_error), makes every CTA of the launch stop, drains in-flight copies and MMAs,
  * frees tensor memory and returns. Small values are for tests of that path. spins >= 1. */
 FA_LP_API int fa_lp_plan_set_wait_limit(fa_lp_plan* plan, int64_t spins);

@@ -45,6 +45,7 @@ constexpr uint32_t kTileBytes = 128 * 128;          // one 128x128 E4M3 tile
 constexpr uint32_t kIdescS = idesc_f8f6f4(128, kSub, 0, 0);   // E4M3 x E4M3 -> F32, N=64
 constexpr uint32_t kIdescPV = idesc_f8f6f4(128, 128, 0, 0);   // N = 128 channels
 constexpr uint32_t kProbeNs = 100000;         // one parked probe: at most ~100 us
+constexpr int kSpinProbes = 64;                 // plain probes before parking
 constexpr long long kDrainProbes = 20000;      // drains give up after ~2 s
 // Threshold (log2 units) by which a sub-tile's maximum must exceed the reference maximum before
 // the reference moves (and O, l are rescaled). P = 2^(S c - m c) <= 2^kTau stays inside E4M3.
@@ -87,26 +88,45 @@ struct AttnArgs {
 
 enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4 };
 
-// Bounded wait on one mbarrier phase. Each probe parks the thread for up to kProbeNs; after
-// a.spin_limit unsuccessful probes the wait expires. Returns false when the CTA aborts (this wait
-// expired, or another wait of this launch did).
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Smem& S,
-                                           const AttnArgs& a, int role) {
-  long long n = 0;
-  while (!mbar_try_wait_sleep(bar, parity, kProbeNs)) {
-    if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
-    if (*reinterpret_cast<volatile int*>(a.abort_word) == a.gen) {  // another CTA gave up
-      *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
-      return false;
-    }
-    if (++n >= a.spin_limit) {
+// Bounded wait on one mbarrier phase. The first kSpinProbes probes are plain try_waits (the
+// hardware holds the thread briefly and wakes it as the phase completes: the lowest latency for
+// the short waits of the steady state); later probes park the thread for up to kProbeNs each.
+// Every probe counts toward a.spin_limit; reaching it expires the wait. A limit shorter than the
+// spin phase (a test configuration) makes every probe a non-blocking poll, so that the limit
+// counts polls exactly. Returns false when the CTA aborts (this wait expired, or another wait of
+// this launch did). The first probe is inlined; the rest lives out of line to keep code small.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, Smem& S,
+                                             const AttnArgs& a, int role) {
+  const bool exact = a.spin_limit < kSpinProbes;
+  long long n = exact ? 0 : 1;  // the inlined fast path made one probe already
+  for (;;) {
+    if (n >= a.spin_limit) {
       *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
       atomicExch(a.abort_word, a.gen);
       atomicCAS(a.err, 0, 0x100 | role);
       return false;
     }
+    const bool parked = n >= kSpinProbes;
+    bool done;
+    if (exact) done = mbar_test_wait(bar, parity);
+    else if (parked) done = mbar_try_wait_sleep(bar, parity, kProbeNs);
+    else done = mbar_try_wait(bar, parity);
+    if (done) return true;
+    ++n;
+    if (parked) {
+      if (*reinterpret_cast<volatile int*>(&S.abort_flag)) return false;
+      if (*reinterpret_cast<volatile int*>(a.abort_word) == a.gen) {  // another CTA gave up
+        *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
+        return false;
+      }
+    }
   }
-  return true;
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Smem& S,
+                                           const AttnArgs& a, int role) {
+  if (a.spin_limit >= kSpinProbes && mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, S, a, role);
 }
 
 // Wait used while draining after an abort: ignores the abort flag, bounded separately.
@@ -115,25 +135,29 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait_sleep(bar, parity, kProbeNs)) return;
 }
 
+// TMA role, on a whole warp, converged (a lone active lane beside 31 lanes parked at a CTA
+// barrier is scheduled poorly); one elected lane issues the copies.
 __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                          const CUtensorMap* tm_v, Smem& S, const AttnArgs& a,
                                          const WorkItem& wi, const SegInfo& sg) {
   const int n_kv = sg.nblk;
   const int rq = sg.row0 + wi.qt0 * kTile;
-  mbar_arrive_expect_tx(smem_u32(&S.bar_q), uint32_t(wi.nq) * kTileBytes);
-  tma_load_3d(smem_u32(S.q[0]), tm_q, smem_u32(&S.bar_q), 0, rq, wi.head);
-  if (wi.nq == 2) tma_load_3d(smem_u32(S.q[1]), tm_q, smem_u32(&S.bar_q), 0, rq + kTile, wi.head);
+  mbar_arrive_expect_tx_elect(smem_u32(&S.bar_q), uint32_t(wi.nq) * kTileBytes);
+  tma_load_3d_elect(smem_u32(S.q[0]), tm_q, smem_u32(&S.bar_q), 0, rq, wi.head);
+  if (wi.nq == 2)
+    tma_load_3d_elect(smem_u32(S.q[1]), tm_q, smem_u32(&S.bar_q), 0, rq + kTile, wi.head);
   int issued = 0;
   for (int j = 0; j < n_kv; ++j) {
     const int st = j % kStages;
     if (j >= kStages &&
-        !wait_phase(smem_u32(&S.bar_free[st]), ((j / kStages) - 1) & 1, S, a, kRoleProducer))
+        !__all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_free[st]), ((j / kStages) - 1) & 1,
+                                            S, a, kRoleProducer)))
       break;
     const int row = sg.row0 + j * kTile;
-    mbar_arrive_expect_tx(smem_u32(&S.bar_k[st]), kTileBytes);
-    tma_load_3d(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_k[st]), 0, row, wi.head);
-    mbar_arrive_expect_tx(smem_u32(&S.bar_v[st]), kTileBytes);
-    tma_load_3d(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_v[st]), row, 0, wi.head);
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]), kTileBytes);
+    tma_load_3d_elect(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_k[st]), 0, row, wi.head);
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[st]), kTileBytes);
+    tma_load_3d_elect(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_v[st]), row, 0, wi.head);
     issued = j + 1;
   }
   // No copy may still be landing in shared memory when the CTA exits.
@@ -153,31 +177,31 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
 __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const WorkItem& wi,
                                            const SegInfo& sg, uint32_t tmem, int t) {
   const int n_sub = (sg.len + kSub - 1) / kSub;
-  const uint32_t qa = smem_u32(S.q[0]) + uint32_t(t) * kTileBytes;
-  const uint32_t k0 = smem_u32(S.k[0]);
-  const uint32_t v0 = smem_u32(S.v[0]);
+  // Descriptors are built once; the start-address field holds (address >> 4), so moving an
+  // operand by `off` bytes (a K step, a sub-tile, a stage) adds off >> 4 to the descriptor.
+  const uint64_t dq = sdesc_kmajor_sw128(smem_u32(S.q[0]) + uint32_t(t) * kTileBytes);
+  const uint64_t dk = sdesc_kmajor_sw128(smem_u32(S.k[0]));
+  const uint64_t dvv = sdesc_kmajor_sw128(smem_u32(S.v[0]));
   const uint32_t d_o = tmem + col_o(t);
   // S_t(u) = Q_t K(u)^T: K rows [64h, 64h + 64) of the stage holding key tile u / 2
   auto issue_s = [&](int u) {
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
-    const uint32_t kb = k0 + (j % kStages) * kTileBytes + h * (kSub * 128);
+    const uint64_t kb = dk + (((j % kStages) * kTileBytes + h * (kSub * 128)) >> 4);
     const uint32_t d = tmem + col_s(t, h);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-      mma_f8f6f4_ss_elect(d, sdesc_kmajor_sw128(qa + 32 * kk), sdesc_kmajor_sw128(kb + 32 * kk),
-                          kIdescS, kk > 0);
+      mma_f8f6f4_ss_elect(d, dq + 2 * kk, kb + 2 * kk, kIdescS, kk > 0);
     mma_commit_elect(smem_u32(&S.bar_s[t][h]));
   };
   // O_t += P_t(u) V(u): keys [64h, 64h + 64) are bytes [64h, 64h + 64) of each V^T row; P from
   // the first 16 columns of S buffer h
   auto issue_pv = [&](int u) {
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
-    const uint32_t vb = v0 + (j % kStages) * kTileBytes + h * kSub;
+    const uint64_t vb = dvv + (((j % kStages) * kTileBytes + h * kSub) >> 4);
     const uint32_t pa = tmem + col_s(t, h);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk)
-      mma_f8f6f4_ts_elect(d_o, pa + 8 * kk, sdesc_kmajor_sw128(vb + 32 * kk), kIdescPV,
-                          (u > 0 || kk > 0) ? 1u : 0u);
+      mma_f8f6f4_ts_elect(d_o, pa + 8 * kk, vb + 2 * kk, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
     mma_commit_elect(smem_u32(&S.bar_o[t][h]));
   };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -388,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == kTmaWarp) {
-    if (lane == 0) producer(&tm_q, &tm_k, &tm_v, S, a, wi, sg);
+    producer(&tm_q, &tm_k, &tm_v, S, a, wi, sg);
   } else if (warp >= kMmaWarp) {
     const int t = warp - kMmaWarp;
     if (t < wi.nq) mma_issuer(S, a, wi, sg, tmem, t);

@@ -145,8 +145,11 @@ void build_plan(fa_lp_plan* p) {
   p->row_off[ns] = row;
   p->tpad = row;
 
-  // Work list: longest segment first (LPT), then head, then pairs of query tiles, so that the
-  // CTAs running at the same time share one head's K/V in L2.
+  // Work list: longest segment first (LPT); within a segment, blocks of kHeadGroup heads, and in
+  // a block the query-tile pairs of its heads interleaved. The CTAs resident at one time then
+  // read the K/V of a few heads (a working set that stays in L2) while no single K/V line is
+  // requested by all of them at once.
+  constexpr int kHeadGroup = 8;
   std::vector<int> order(ns);
   for (int s = 0; s < ns; ++s) order[s] = s;
   std::stable_sort(order.begin(), order.end(),
@@ -154,8 +157,10 @@ void build_plan(fa_lp_plan* p) {
   for (int s : order) {
     const int nb = p->segs[s].nblk;
     if (nb == 0) continue;
-    for (int h = 0; h < p->heads; ++h)
-      for (int t = 0; t < nb; t += 2) p->work.push_back(WorkItem{s, h, t, std::min(2, nb - t)});
+    for (int h0 = 0; h0 < p->heads; h0 += kHeadGroup)
+      for (int t = 0; t < nb; t += 2)
+        for (int h = h0; h < std::min(p->heads, h0 + kHeadGroup); ++h)
+          p->work.push_back(WorkItem{s, h, t, std::min(2, nb - t)});
   }
 
   // Workspace layout.

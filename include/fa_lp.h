@@ -219,6 +219,32 @@ FA_LP_API int fa_lp_release_workspace(int device, void* stream);
  * the hardware conversions against the format definitions. */
 FA_LP_API int fa_lp_encode(int format, const float* x, int64_t n, uint8_t* codes, void* stream);
 
+/*
+ * fa_lp_fp8_descale_noalloc -- the FP8 per-(tensor, head) descales of fa_lp_quantize
+ * (amax / 448 over all tokens, 1 when amax is 0) for callers that cannot let the library
+ * allocate device memory: programs whose memory belongs to their own pool or allocator,
+ * deployments with a fixed memory footprint after start-up, and latency-critical loops that
+ * cannot afford cudaMalloc's implicit synchronization. The pages have no counterpart of this
+ * call; it is an addition of this library.
+ *   q, k, v       : device pointers to BF16 [tokens, heads, 128] views, as for fa_lp_quantize.
+ *   tokens, heads : T >= 0 and 1 <= H <= 1024 (larger H returns FA_LP_ERR_INVALID_ARG).
+ *   descale       : device pointer, caller-owned f32 [3][heads] (q, k, v), written.
+ *   stream        : cudaStream_t (as void*).
+ * It makes no cudaMalloc or cudaFree and calls no allocating library routine: its scratch is
+ * a fixed 12 KB device array inside the library, held by every GPU that loads it until the
+ * process exits, shared by all calls on a device and cleared by each call. Calls that overlap
+ * on the GPU race on it; order them on one stream or synchronize. The first call on a device
+ * looks up the array's device address; make it before any stream capture begins.
+ * Errors: INVALID_ARG (NULL, misaligned or non-positive strides, heads out of range),
+ * UNSUPPORTED (device not sm_103), CUDA.
+ */
+FA_LP_API int fa_lp_fp8_descale_noalloc(const void* q, int64_t q_stride_tok,
+                                        int64_t q_stride_head, const void* k,
+                                        int64_t k_stride_tok, int64_t k_stride_head,
+                                        const void* v, int64_t v_stride_tok,
+                                        int64_t v_stride_head, int64_t tokens, int heads,
+                                        float* descale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

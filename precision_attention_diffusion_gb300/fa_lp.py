@@ -34,7 +34,7 @@ EXPORTS = (
     "fa_lp_workspace_bytes", "fa_lp_quantize", "fa_lp_forward_varlen", "fa_lp_attention",
     "fa_lp_plan_row_offsets", "fa_lp_get_quantized", "fa_lp_copy_quantized",
     "fa_lp_get_last_error", "fa_lp_plan_set_wait_limit", "fa_lp_release_workspace",
-    "fa_lp_encode",
+    "fa_lp_encode", "fa_lp_fp8_descale_noalloc",
 )
 
 _lib = None
@@ -89,6 +89,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.fa_lp_plan_set_wait_limit.argtypes = [P, i64]
         L.fa_lp_release_workspace.argtypes = [i32, P]
         L.fa_lp_encode.argtypes = [i32, P, i64, P, P]
+        L.fa_lp_fp8_descale_noalloc.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32, P,
+                                                P]
         for name in EXPORTS:
             if name != "fa_lp_status_string":
                 getattr(L, name).restype = i32
@@ -229,6 +231,22 @@ def encode(fmt: int, x: torch.Tensor, stream=None) -> torch.Tensor:
     out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     _check(load().fa_lp_encode(int(fmt), ctypes.c_void_p(x.data_ptr()), x.numel(),
                                ctypes.c_void_p(out.data_ptr()), _stream(stream)), "fa_lp_encode")
+    return out
+
+
+def fp8_descale_noalloc(q, k, v, out=None, stream=None) -> torch.Tensor:
+    """FP8 descales [3, heads] (q, k, v) through the entry point that allocates nothing inside
+    the library; `out` (float32 [3, heads] on the device) may be passed in."""
+    qa, qs, qh = _view(q, "q")
+    ka, ks, kh = _view(k, "k")
+    va, vs, vh = _view(v, "v")
+    heads = q.shape[1]
+    if out is None:
+        out = torch.empty((3, heads), dtype=torch.float32, device=q.device)
+    assert out.dtype == torch.float32 and out.is_contiguous() and out.numel() >= 3 * heads
+    _check(load().fa_lp_fp8_descale_noalloc(qa, qs, qh, ka, ks, kh, va, vs, vh, q.shape[0], heads,
+                                            ctypes.c_void_p(out.data_ptr()), _stream(stream)),
+           "fa_lp_fp8_descale_noalloc")
     return out
 
 

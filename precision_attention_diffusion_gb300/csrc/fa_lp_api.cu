@@ -187,6 +187,7 @@ void build_plan(fa_lp_plan* p) {
     w.v_sf = take(H * 128 * (Tp / 16));
     w.q_mean = take(H * (Tp / 128) * 128 * 4);
     w.k_mean = take(size_t(p->nseg) * H * 128 * 4);
+    w.k_chunk = take(p->blocks.size() * H * 128 * 8);
   }
   w.total = off;
 }

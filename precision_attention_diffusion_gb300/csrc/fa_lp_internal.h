@@ -44,6 +44,7 @@ struct WsLayout {
   size_t q_codes = 0, k_codes = 0, v_codes = 0;  // FP8: [H][Tp][128], [H][Tp][128], [H][128][Tp]
   size_t q_sf = 0, k_sf = 0, v_sf = 0;           // NVFP4 scale bytes
   size_t q_mean = 0, k_mean = 0;                 // NVFP4 means (f32)
+  size_t k_chunk = 0;                            // NVFP4 scratch: f64 [nblk][H][128] chunk sums
   size_t amax = 0, descale = 0;                  // FP8: u32 [3][H], f32 [3][H]
   size_t total = 0;
 };

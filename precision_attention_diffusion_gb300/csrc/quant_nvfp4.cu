@@ -1,0 +1,181 @@
+// quant_nvfp4.cu -- NVFP4 (SageAttention3-style) quantization of BF16 Q/K/V into the workspace.
+//
+// Passage: FlashInfer docs, flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4,
+// description: K rows centred by the segment's per-channel mean, Q rows by their 128-row block's
+// mean; Q / K / V stored as E2M1 codes with one UE4M3 scale per 16 elements (block amax / 6); V
+// transposed with per-16-key scales; segments of any length, including empty ones.
+//
+// Arithmetic (readings r7-r10): means are FP64 sums in canonical order -- 128-token chunks from
+// the segment start summed left to right, then the chunk sums left to right -- and
+// mean = fl32(sum / n); centred x = fl32(x - mean); per group of 16: s = E4M3_rn(fl32(amax / 6)),
+// code = E2M1_rn_sat(fl32(x / deq(s))), codes 0 when s == 0. Divisions are IEEE (__fdiv_rn).
+//
+// Layouts written (padded token axis as for FP8: segment s on rows [row0_s, row0_s + L_s)):
+//   Q, K codes : u8 [H][Tpad][64]    two E2M1 codes per byte, even channel in the low nibble
+//   Q, K scales: u8 [H][Tpad][8]     UE4M3, one per 16 channels
+//   V^T codes  : u8 [H][128][Tpad/2] two keys per byte, even key in the low nibble
+//   V scales   : u8 [H][128][Tpad/16] one per 16 keys (groups start at the segment start)
+//   Q means    : f32 [H][Tpad/128][128]; K means: f32 [num_segments][H][128]
+// Padding rows / keys hold code 0 and scale 0.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_lp_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace falp {
+namespace {
+
+__device__ __forceinline__ float bf16_at(const uint16_t* x, int64_t t, int h, int c, int64_t st,
+                                         int64_t sh) {
+  return __uint_as_float(uint32_t(x[t * st + int64_t(h) * sh + c]) << 16);
+}
+
+__device__ __forceinline__ float e4m3_value(uint8_t code) {
+  const uint32_t h2 = cvt_e4m3x2_to_f16x2(uint16_t(code));
+  return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
+}
+
+// One 16-element group held 4 per lane by 4 consecutive lanes: shared amax, UE4M3 scale, and
+// the 4 codes of this lane packed into 16 bits (element 0 in the low nibble).
+__device__ __forceinline__ uint32_t group16(const float (&x)[4], uint8_t* sf_out) {
+  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  const uint8_t sf = uint8_t(cvt_e4m3x2(__fdiv_rn(a, 6.f), 0.f) & 0xFF);
+  *sf_out = sf;
+  if (sf == 0) return 0u;
+  const float ds = e4m3_value(sf);
+  const uint32_t lo = cvt_e2m1x2(__fdiv_rn(x[0], ds), __fdiv_rn(x[1], ds));
+  const uint32_t hi = cvt_e2m1x2(__fdiv_rn(x[2], ds), __fdiv_rn(x[3], ds));
+  return lo | (hi << 8);
+}
+
+// Pass 1: per (128-row block, head) column sums in FP64, rows in order. For Q (z = 0) the block
+// is one mean's whole extent: write the block mean. For K (z = 1) store the chunk sum.
+__global__ void __launch_bounds__(128) nvfp4_block_sums_kernel(
+    const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
+    int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t nblk,
+    float* __restrict__ qmean, double* __restrict__ kchunk) {
+  const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z, c = threadIdx.x;
+  const BlockInfo bi = blocks[b];
+  const uint16_t* x = z == 0 ? q : k;
+  const int64_t st = z == 0 ? qst : kst, sh = z == 0 ? qsh : ksh;
+  double sum = 0.0;
+  for (int r = 0; r < bi.nvalid; ++r) sum += double(bf16_at(x, bi.tok0 + r, h, c, st, sh));
+  if (z == 0)
+    qmean[(int64_t(h) * nblk + b) * kD + c] = __double2float_rn(sum / double(bi.nvalid));
+  else
+    kchunk[(int64_t(b) * H + h) * kD + c] = sum;
+}
+
+// Pass 2: K segment means from the chunk sums, chunks in order.
+__global__ void __launch_bounds__(128) nvfp4_kmean_kernel(const SegInfo* __restrict__ segs, int H,
+                                                          const double* __restrict__ kchunk,
+                                                          float* __restrict__ kmean) {
+  const int s = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const SegInfo sg = segs[s];
+  float m = 0.f;
+  if (sg.len > 0) {
+    const int b0 = sg.row0 / kTile;
+    double sum = 0.0;
+    for (int i = 0; i < sg.nblk; ++i) sum += kchunk[(int64_t(b0 + i) * H + h) * kD + c];
+    m = __double2float_rn(sum / double(sg.len));
+  }
+  kmean[(int64_t(s) * H + h) * kD + c] = m;
+}
+
+// Pass 3: Q and K codes and scales. One CTA per (128-row block, head, tensor); a warp per row at
+// a time, each lane 4 channels (a 16-channel group = 4 lanes).
+__global__ void __launch_bounds__(256) nvfp4_pack_qk_kernel(
+    const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
+    int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t Tp,
+    int64_t nblk, const float* __restrict__ qmean, const float* __restrict__ kmean,
+    uint8_t* __restrict__ qc, uint8_t* __restrict__ kc, uint8_t* __restrict__ qs,
+    uint8_t* __restrict__ ks) {
+  const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BlockInfo bi = blocks[b];
+  const uint16_t* x = z == 0 ? q : k;
+  const int64_t st = z == 0 ? qst : kst, sh = z == 0 ? qsh : ksh;
+  const float* mean = z == 0 ? qmean + (int64_t(h) * nblk + b) * kD
+                             : kmean + (int64_t(bi.seg) * H + h) * kD;
+  uint8_t* codes = (z == 0 ? qc : kc) + (int64_t(h) * Tp + int64_t(b) * kTile) * 64;
+  uint8_t* scales = (z == 0 ? qs : ks) + (int64_t(h) * Tp + int64_t(b) * kTile) * 8;
+  const int c0 = lane * 4;
+  float mu[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mu[e] = mean[c0 + e];
+  for (int r = warp; r < kTile; r += 8) {
+    uint32_t packed = 0u;
+    uint8_t sf = 0;
+    if (r < bi.nvalid) {
+      const uint2 w = *reinterpret_cast<const uint2*>(x + int64_t(bi.tok0 + r) * st +
+                                                      int64_t(h) * sh + c0);
+      float xc[4];
+      xc[0] = __fsub_rn(__uint_as_float(w.x << 16), mu[0]);
+      xc[1] = __fsub_rn(__uint_as_float(w.x & 0xFFFF0000u), mu[1]);
+      xc[2] = __fsub_rn(__uint_as_float(w.y << 16), mu[2]);
+      xc[3] = __fsub_rn(__uint_as_float(w.y & 0xFFFF0000u), mu[3]);
+      packed = group16(xc, &sf);
+    }
+    reinterpret_cast<uint16_t*>(codes + int64_t(r) * 64)[lane] = uint16_t(packed);
+    if ((lane & 3) == 0) scales[int64_t(r) * 8 + (lane >> 2)] = sf;
+  }
+}
+
+// Pass 4: V^T codes and scales. One CTA per (128-key block, head): the BF16 tile goes through
+// shared memory; then per (channel, 16-key group) a 4-lane team quantizes 16 keys.
+__global__ void __launch_bounds__(256) nvfp4_pack_vt_kernel(
+    const uint16_t* __restrict__ v, int64_t vst, int64_t vsh, const BlockInfo* __restrict__ blocks,
+    int H, int64_t Tp, uint8_t* __restrict__ vt, uint8_t* __restrict__ vs) {
+  __shared__ float tile[kTile][kD + 1];
+  const int b = blockIdx.x, h = blockIdx.y;
+  const BlockInfo bi = blocks[b];
+  for (int i = threadIdx.x; i < kTile * kD; i += 256) {
+    const int r = i >> 7, c = i & 127;
+    tile[r][c] = r < bi.nvalid ? bf16_at(v, bi.tok0 + r, h, c, vst, vsh) : 0.f;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  // 128 channels x 8 groups = 1024 teams of 4 lanes; 64 teams per pass of 256 threads
+  for (int team = threadIdx.x >> 2; team < kD * 8; team += 64) {
+    const int c = team >> 3, g = team & 7;
+    const int k0 = g * 16 + (lane & 3) * 4;
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = tile[k0 + e][c];
+    uint8_t sf;
+    const uint32_t packed = group16(x, &sf);
+    uint8_t* row = vt + (int64_t(h) * kD + c) * (Tp / 2) + int64_t(b) * (kTile / 2);
+    reinterpret_cast<uint16_t*>(row)[g * 4 + (lane & 3)] = uint16_t(packed);
+    if ((lane & 3) == 0) vs[(int64_t(h) * kD + c) * (Tp / 16) + int64_t(b) * 8 + g] = sf;
+  }
+}
+
+}  // namespace
+
+int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t qst,
+                          int64_t qsh, const void* k, int64_t kst, int64_t ksh, const void* v,
+                          int64_t vst, int64_t vsh, cudaStream_t stream) {
+  const int H = p.heads;
+  const int64_t nblk = int64_t(p.blocks.size());
+  const auto* qb = static_cast<const uint16_t*>(q);
+  const auto* kb = static_cast<const uint16_t*>(k);
+  const auto* vb = static_cast<const uint16_t*>(v);
+  float* qmean = reinterpret_cast<float*>(ws + p.ws.q_mean);
+  float* kmean = reinterpret_cast<float*>(ws + p.ws.k_mean);
+  double* kchunk = reinterpret_cast<double*>(ws + p.ws.k_chunk);
+  nvfp4_block_sums_kernel<<<dim3(unsigned(nblk), unsigned(H), 2), 128, 0, stream>>>(
+      qb, qst, qsh, kb, kst, ksh, p.d_blocks, H, nblk, qmean, kchunk);
+  nvfp4_kmean_kernel<<<dim3(unsigned(p.nseg), unsigned(H)), 128, 0, stream>>>(p.d_segs, H,
+                                                                             kchunk, kmean);
+  nvfp4_pack_qk_kernel<<<dim3(unsigned(nblk), unsigned(H), 2), 256, 0, stream>>>(
+      qb, qst, qsh, kb, kst, ksh, p.d_blocks, H, p.tpad, nblk, qmean, kmean, ws + p.ws.q_codes,
+      ws + p.ws.k_codes, ws + p.ws.q_sf, ws + p.ws.k_sf);
+  nvfp4_pack_vt_kernel<<<dim3(unsigned(nblk), unsigned(H)), 256, 0, stream>>>(
+      vb, vst, vsh, p.d_blocks, H, p.tpad, ws + p.ws.v_codes, ws + p.ws.v_sf);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace falp

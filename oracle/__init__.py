@@ -70,8 +70,8 @@ def lib() -> ctypes.CDLL:
             L.orc_nvfp4_quantize_q.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, P, i32]
             L.orc_nvfp4_quantize_k.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, P, i32]
             L.orc_nvfp4_quantize_v.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, i32]
-            L.orc_attn_nvfp4.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, f64, P, i64, P, P,
-                                         i32]
+            L.orc_attn_nvfp4.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, f64, i32, P, i64,
+                                         P, P, i32]
             _lib = L
     return _lib
 
@@ -209,8 +209,13 @@ def nvfp4_quantize(q, k, v, cu, nthreads=0):
     return dict(km=km, qm=qm, cq=cq, sq=sq, ck=ck, sk=sk, cv=cv, sv=sv, qoff=qo, goff=go)
 
 
-def attn_nvfp4(qz, cu, rows, scale, nthreads=0):
-    """C3: NVFP4-emulating attention from nvfp4_quantize()'s dict -> (out fp64, out bf16)."""
+def attn_nvfp4(qz, cu, rows, scale, n_kv=128, nthreads=0):
+    """C3: NVFP4-emulating attention from nvfp4_quantize()'s dict -> (out fp64, out bf16).
+
+    n_kv: width of the online-softmax key tiles (a multiple of 16), counted from each segment
+    start; the running maximum is exact."""
+    if n_kv <= 0 or n_kv % 16:
+        raise ValueError("n_kv must be a positive multiple of 16")
     cu = np.ascontiguousarray(cu, np.int32)
     rows = np.ascontiguousarray(rows, np.int64).reshape(-1, 2)
     T, H = qz["cq"].shape[0], qz["cq"].shape[1]
@@ -218,5 +223,5 @@ def attn_nvfp4(qz, cu, rows, scale, nthreads=0):
     o16 = np.empty((rows.shape[0], D), np.uint16)
     lib().orc_attn_nvfp4(_p(qz["cq"]), _p(qz["sq"]), _p(qz["qm"]), _p(qz["ck"]), _p(qz["sk"]),
                          _p(qz["cv"]), _p(qz["sv"]), T, H, _p(cu), len(cu) - 1, float(scale),
-                         _p(rows), rows.shape[0], _p(o64), _p(o16), _threads(nthreads))
+                         int(n_kv), _p(rows), rows.shape[0], _p(o64), _p(o16), _threads(nthreads))
     return o64, o16

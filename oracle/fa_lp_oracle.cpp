@@ -468,14 +468,15 @@ void orc_nvfp4_quantize_v(const uint16_t* v, int64_t vst, int64_t vsh, int64_t T
 
 // ---------------------------------------------------------------------------------------------
 // C3: NVFP4 emulating attention for a list of query rows. Scores S' = scale * (deq(Qc) deq(Kc)^T
-// + qm deq(Kc)^T) (r12); online softmax over 128-key tiles from the segment start with the exact
-// running max; P' = fl32(2688 exp(S' - m)) (r11); per 16 keys of the tile a UE4M3 scale and E2M1
-// codes (r9); l sums deq(P'); O sums deq(P') deq(V); out = O / l.
+// + qm deq(Kc)^T) (r12); online softmax over tiles of n_kv keys (a multiple of 16) from the
+// segment start with the exact running max (r5 with tau = 0); P' = fl32(2688 exp(S' - m)) (r11);
+// per 16 keys of the tile a UE4M3 scale and E2M1 codes (r9); l sums deq(P'); O sums deq(P')
+// deq(V); out = O / l.
 // ---------------------------------------------------------------------------------------------
 void orc_attn_nvfp4(const uint8_t* cq, const uint8_t* sfq, const float* qm,
                     const uint8_t* ck, const uint8_t* sfk,
                     const uint8_t* cv, const uint8_t* sfv,
-                    int64_t T, int H, const int32_t* cu, int nseg, double scale,
+                    int64_t T, int H, const int32_t* cu, int nseg, double scale, int n_kv,
                     const int64_t* rows, int64_t nrows, double* out64, uint16_t* out16,
                     int nthreads) {
   (void)T;
@@ -483,7 +484,6 @@ void orc_attn_nvfp4(const uint8_t* cq, const uint8_t* sfq, const float* qm,
   std::vector<int64_t> qoff(nseg + 1), goff(nseg + 1);
   orc_nvfp4_qblock_offsets(cu, nseg, qoff.data());
   const int64_t G = orc_nvfp4_vgroup_offsets(cu, nseg, goff.data());
-  const int n_kv = 128;
   parallel_for(nrows, nthreads, [&](int64_t r) {
     const int64_t t = rows[2 * r];
     const int h = static_cast<int>(rows[2 * r + 1]);

@@ -195,3 +195,52 @@ def test_nvfp4_scrambled_negative_control(gauss):
     z = oracle.nvfp4_quantize(bits(q), bits(k[perm].contiguous()), bits(v), [0, T])
     o64, _ = oracle.attn_nvfp4(z, [0, T], rows, SCALE)
     assert rel_rms(o64, exact) > 0.5
+
+
+def _dominant_key_case(pos, T=2048, H=2, seed=11):
+    """Every query row has its largest score at key `pos`: channel 0 of every q is raised by 8 and
+    channel 0 of key `pos` is 30, so q.k_pos exceeds every other score by about 100 (raw units);
+    with softmax scale 0.02 the other keys still carry weight."""
+    q, k, v = inputs.qkv_separate(T, H, seed=seed)
+    q = q.float(); k = k.float()
+    q[:, :, 0] += 8.0
+    k[pos, :, 0] = 30.0
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v
+
+
+def _argmax_keys(q, k, rows):
+    qf, kf = q.double(), k.double()
+    return np.array([int((kf[:, h] @ qf[r, h]).argmax()) for r, h in rows])
+
+
+def test_nvfp4_tile_width_invariance_when_max_is_first():
+    """With the exact running maximum, the tile width only matters through the moments the
+    maximum moves: when each row's maximum lies in the first 16 keys, every tile width (a multiple
+    of 16) quantizes every P' against the same m, so the outputs agree bit for bit."""
+    T = 2048
+    q, k, v = _dominant_key_case(5, T)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), [0, T])
+    rows = inputs.sample_rows([0, T], 2, n_heads=2, n_rows=48, seed=3)
+    assert np.all(_argmax_keys(q, k, rows) == 5)
+    outs = [oracle.attn_nvfp4(z, [0, T], rows, 0.02, n_kv=n)[0] for n in (16, 64, 128, 4096)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    # not degenerate: other keys still carry weight, so the output is not V of the dominant key
+    e2 = oracle.e2m1_decode_table(); e4 = oracle.e4m3_decode_table()
+    dom = e2[z["cv"][5, 0]] * e4[z["sv"][0, :, 0]]
+    assert np.abs(outs[0][np.asarray(rows)[:, 1] == 0] - dom).max() > 1e-2
+
+
+def test_nvfp4_tile_width_matters_when_max_moves():
+    """The same rows with the dominant key at 1000: tiles before it are quantized against smaller
+    maxima, so a 16-key and a 4096-key tiling give different (both valid) outputs."""
+    T = 2048
+    q, k, v = _dominant_key_case(1000, T)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), [0, T])
+    rows = inputs.sample_rows([0, T], 2, n_heads=2, n_rows=48, seed=3)
+    assert np.all(_argmax_keys(q, k, rows) == 1000)
+    a, _ = oracle.attn_nvfp4(z, [0, T], rows, 0.02, n_kv=16)
+    b, _ = oracle.attn_nvfp4(z, [0, T], rows, 0.02, n_kv=4096)
+    exact = oracle.attn_exact(bits(q), bits(k), bits(v), [0, T], rows, 0.02)
+    assert not np.array_equal(a, b)
+    assert rel_rms(a, exact) < 0.25 and rel_rms(b, exact) < 0.25

@@ -12,6 +12,9 @@ flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
+--workload nvfp4_s30272_h56 times the NVFP4 path instead (K with a per-channel offset N(0, 4)),
+against the dense FP4 peak.
+
 N > 1 (torchrun, one process per GPU): independent replicas of the full workload on every rank
 (the path has no exchange step), max-over-ranks time, weak scaling.
 --impl reference: the CPU oracle timed on the host cores over a bounded sample of the same
@@ -34,11 +37,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "E4M3 varlen attn TFLOPS at S=30272,H=56,D=128; % of FP8 tensor peak"
+METRIC_NVFP4 = "NVFP4 varlen attn TFLOPS at S=30272,H=56,D=128; % of FP4 tensor peak"
 UNIT = "TFLOPS"
 D = 128
-# dense FP8 / dense BF16 tensor rate of the part (nominal 4.5 / 2.25 PFLOP/s)
+# dense FP8 and FP4 over dense BF16 tensor rate of the part (nominal 4.5, 13.5 / 2.25 PFLOP/s)
 FP8_OVER_BF16 = 2.0
-KERNELS_PER_STEP = 4  # amax, pack Q/K, pack V^T, attention
+FP4_OVER_BF16 = 6.0
+# kernels per step: FP8 amax, pack Q/K, pack V^T, attention; NVFP4 block sums, K means, pack
+# Q/K, pack V^T, attention
+KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5}
 
 # DRAM traffic of the attention kernel per launch, from an ncu capture, keyed by the SHA-256 of
 # attn_fp8.cu at capture time (null when the kernel changed since the counters were taken).
@@ -64,6 +71,10 @@ def workload(name):
     return list(w["cu"]), int(w["heads"])
 
 
+def mode_of(name):
+    return "nvfp4" if name.startswith("nvfp4") else "fp8"
+
+
 def attn_flops(cu, H):
     return 4.0 * sum((b - a) ** 2 for a, b in zip(cu[:-1], cu[1:])) * H * D
 
@@ -73,12 +84,12 @@ def peaks():
     try:
         with open(path) as f:
             p = json.load(f)
-        return dict(fp8=FP8_OVER_BF16 * float(p["bf16_tflops"]),
-                    fp8_sustained=FP8_OVER_BF16 * float(p["bf16_tflops_sustained"]),
-                    hbm=float(p["hbm_gbs"]), source="measured")
+        bf16, bf16s, hbm, src = (float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]),
+                                 float(p["hbm_gbs"]), "measured")
     except Exception:
-        return dict(fp8=FP8_OVER_BF16 * 1900.0, fp8_sustained=FP8_OVER_BF16 * 1700.0, hbm=6800.0,
-                    source="fallback")
+        bf16, bf16s, hbm, src = 1900.0, 1700.0, 6800.0, "fallback"
+    return dict(fp8=FP8_OVER_BF16 * bf16, fp8_sustained=FP8_OVER_BF16 * bf16s,
+                fp4=FP4_OVER_BF16 * bf16, fp4_sustained=FP4_OVER_BF16 * bf16s, hbm=hbm, source=src)
 
 
 def file_sha(path):
@@ -141,10 +152,10 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------
 # CPU oracle on a bounded sample of the workload (the cpu_baseline object and the reference arm)
 # ------------------------------------------------------------------------------------------------
-def oracle_sample(cu, H, seconds, seed=0):
-    """Time the oracle (as it stands, all host threads) on head 0 of the workload: FP8 quantize
-    of that head's full Q/K/V, then FP8-emulating attention of R query rows of the longest
-    segment. Extrapolates to the whole workload: per head, quantize once + L rows."""
+def oracle_sample(cu, H, seconds, seed=0, mode="fp8"):
+    """Time the oracle (as it stands, all host threads) on head 0 of the workload: quantize
+    that head's full Q/K/V, then emulating attention (FP8 or NVFP4) of R query rows of the
+    longest segment. Extrapolates to the whole workload: per head, quantize once + L rows."""
     import numpy as np
     import torch
 
@@ -158,7 +169,10 @@ def oracle_sample(cu, H, seconds, seed=0):
     q, k, v = inputs.qkv_separate(T, 1, seed=seed)
     bits = lambda x: x.view(torch.int16).numpy().view(np.uint16)
     t0 = time.perf_counter()
-    qz = [oracle.fp8_quantize(bits(x)) for x in (q, k, v)]
+    if mode == "nvfp4":
+        z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    else:
+        qz = [oracle.fp8_quantize(bits(x)) for x in (q, k, v)]
     t_quant = time.perf_counter() - t0
     ncores = os.cpu_count() or 1
     g = np.random.default_rng(seed)
@@ -166,8 +180,11 @@ def oracle_sample(cu, H, seconds, seed=0):
     def attn_rows(n):
         rows = [(int(t), 0) for t in g.integers(a, b, n)]
         t1 = time.perf_counter()
-        oracle.attn_fp8(qz[0][0], qz[1][0], qz[2][0], qz[0][1], qz[1][1], qz[2][1], cu, rows,
-                        1.0 / math.sqrt(D))
+        if mode == "nvfp4":
+            oracle.attn_nvfp4(z, cu, rows, 1.0 / math.sqrt(D), n_kv=64)
+        else:
+            oracle.attn_fp8(qz[0][0], qz[1][0], qz[2][0], qz[0][1], qz[1][1], qz[2][1], cu, rows,
+                            1.0 / math.sqrt(D))
         return time.perf_counter() - t1
 
     n0 = 2 * ncores
@@ -185,8 +202,9 @@ def oracle_sample(cu, H, seconds, seed=0):
     est_s = H * (t_quant + per_row * sum(x * x for x in lens) / L)
     value = attn_flops(cu, H) / est_s / 1e12
     return dict(value=value, unit=UNIT, cores=ncores, kind="oracle",
-                sample=(f"head 0 of {H}: FP8 quantize of its full Q/K/V ({T} tokens, "
-                        f"{t_quant:.2f} s) + FP8-emulating attention of {R} random query rows of "
+                sample=(f"head 0 of {H}: {mode.upper()} quantize of its full Q/K/V ({T} tokens, "
+                        f"{t_quant:.2f} s) + {mode.upper()}-emulating attention of {R} random query "
+                        f"rows of "
                         f"the {L}-token segment ({t_attn:.2f} s); extrapolated to all {H} heads "
                         f"and rows"),
                 seconds=t_quant + t_attn, est_full_workload_s=est_s)
@@ -206,19 +224,21 @@ def run_reference(args):
         return 0
     cu, H = workload(args.workload)
     per_step = max(args.cpu_seconds / 3.0, 3.0)
+    mode = mode_of(args.workload)
     for _ in range(args.warmup):
-        oracle_sample(cu, H, per_step / 2)
+        oracle_sample(cu, H, per_step / 2, mode=mode)
     vals, secs = [], []
     for i in range(args.steps):
-        r = oracle_sample(cu, H, per_step, seed=i)
+        r = oracle_sample(cu, H, per_step, seed=i, mode=mode)
         vals.append(r["value"])
         secs.append(r["est_full_workload_s"])
     v = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup,
+        "impl": "reference", "metric": METRIC_NVFP4 if mode == "nvfp4" else METRIC, "value": v,
+        "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (FP8-emulating oracle)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"f64 ({mode.upper()}-emulating oracle)",
         "data": "synthetic", "config": config_of(args.workload, cu, H),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": r["sample"]},
@@ -230,11 +250,14 @@ def run_reference(args):
 
 def config_of(name, cu, H):
     T = cu[-1]
-    return {"workload": name, "tokens": T, "heads": H, "head_dim": D,
-            "segments": [b - a for a, b in zip(cu[:-1], cu[1:])],
-            "qkv_layout": "strided views of one fused [T,3,H,128] BF16 buffer",
-            "softmax_scale": 1 / math.sqrt(D), "causal": False,
-            "l2": "inputs (1.3 GB) and codes larger than L2: no flush"}
+    c = {"workload": name, "tokens": T, "heads": H, "head_dim": D,
+         "segments": [b - a for a, b in zip(cu[:-1], cu[1:])],
+         "qkv_layout": "strided views of one fused [T,3,H,128] BF16 buffer",
+         "softmax_scale": 1 / math.sqrt(D), "causal": False,
+         "l2": "inputs (1.3 GB) and codes larger than L2: no flush"}
+    if mode_of(name) == "nvfp4":
+        c["k_offset"] = "per-(head, channel) K offset N(0, 4), constant over tokens"
+    return c
 
 
 def run_ours(args):
@@ -254,14 +277,19 @@ def run_ours(args):
     from precision_attention_diffusion_gb300 import fa_lp
 
     cu, H = workload(args.workload)
+    mode = mode_of(args.workload)
     T = cu[-1]
     flops = attn_flops(cu, H)
     g = torch.Generator(device="cuda").manual_seed(1234 + rank)
-    buf = torch.randn((T, 3, H, D), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    buf = torch.randn((T, 3, H, D), generator=g, device="cuda", dtype=torch.float32)
+    if mode == "nvfp4":
+        from precision_attention_diffusion_gb300 import inputs
+        buf[:, 1] += inputs.k_channel_offset(H, seed=rank).cuda()[None]
+    buf = buf.to(torch.bfloat16)
     q, k, v = buf[:, 0], buf[:, 1], buf[:, 2]
     out = torch.empty((T, H, D), dtype=torch.bfloat16, device="cuda")
     cu_dev = torch.tensor(cu, dtype=torch.int32, device="cuda")
-    plan = fa_lp.Plan(cu, H, mode=fa_lp.MODE_FP8)
+    plan = fa_lp.Plan(cu, H, mode=fa_lp.MODE_NVFP4 if mode == "nvfp4" else fa_lp.MODE_FP8)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -356,29 +384,39 @@ def run_ours(args):
 
     pk = peaks()
     achieved = flops / (fwd_ms / 1e3) / 1e12
-    sha = file_sha(os.path.join(ROOT, "precision_attention_diffusion_gb300", "csrc", "attn_fp8.cu"))
+    kname = "attn_nvfp4" if mode == "nvfp4" else "attn_fp8"
+    sha = file_sha(os.path.join(ROOT, "precision_attention_diffusion_gb300", "csrc", kname + ".cu"))
     traffic = NCU_TRAFFIC.get((args.workload, sha))
-    roof = {"bound": "tensor", "achieved": achieved, "peak": pk["fp8"], "unit": "TFLOP/s",
-            "frac": achieved / pk["fp8"], "traffic": traffic,
-            "kernel": "attn_fp8_kernel", "launch_ms": fwd_ms,
-            "peak_note": (f"dense FP8 = {FP8_OVER_BF16:g} x {pk['source']} BF16 cuBLAS burst; "
-                          f"frac of sustained = {achieved / pk['fp8_sustained']:.3f}"),
+    pkey = "fp4" if mode == "nvfp4" else "fp8"
+    ratio = FP4_OVER_BF16 if mode == "nvfp4" else FP8_OVER_BF16
+    roof = {"bound": "tensor", "achieved": achieved, "peak": pk[pkey], "unit": "TFLOP/s",
+            "frac": achieved / pk[pkey], "traffic": traffic,
+            "kernel": kname + "_kernel", "launch_ms": fwd_ms,
+            "peak_note": (f"dense {pkey.upper()} = {ratio:g} x {pk['source']} BF16 cuBLAS burst; "
+                          f"frac of sustained = {achieved / pk[pkey + '_sustained']:.3f}"),
             "algorithmic_flops_per_launch": flops}
-    # quantize passes: HBM-bound; algorithmic bytes = 2 reads of Q/K/V + 1 write of the codes
-    q_bytes = 2 * 3 * T * H * D * 2 + 3 * T * H * D
+    if mode == "nvfp4":
+        # quantize passes: Q, K read twice (means, pack), V once; codes + scales written
+        q_bytes = 5 * T * H * D * 2 + 3 * T * H * (D // 2 + D // 16)
+        dtype = "nvfp4 (e2m1 + ue4m3 per 16, fp32 accumulate, bf16 in/out)"
+    else:
+        # quantize passes: HBM-bound; algorithmic bytes = 2 reads of Q/K/V + 1 write of the codes
+        q_bytes = 2 * 3 * T * H * D * 2 + 3 * T * H * D
+        dtype = "fp8_e4m3 (fp32 accumulate, bf16 in/out)"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "metric": METRIC_NVFP4 if mode == "nvfp4" else METRIC, "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate, bf16 in/out)",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic", "config": config_of(args.workload, cu, H),
         "forward_ms": fwd_ms, "forward_tflops": achieved, "quantize_ms": q_ms,
         "quantize_gbs": q_bytes / (q_ms / 1e3) / 1e9,
         "frac_of_fp8_peak": achieved / pk["fp8"],
         "roofline": roof, "clocks": clocks, "e2e": e2e,
-        "gpu_launches": KERNELS_PER_STEP * K,
+        "gpu_launches": KERNELS_PER_STEP[mode] * K,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds)
+        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds, mode=mode)
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

@@ -147,6 +147,14 @@ FA_LP_API int fa_lp_quantize(fa_lp_plan* plan, const void* q, int64_t q_stride_t
  * moves to a later tile's maximum M only when (M - m)*c > 8 (then O and l are rescaled by
  * 2^((m - M)*c)); P = E4M3_rn(2^(S*c - m*c)) <= 256; l sums the quantized P; O accumulates
  * P * V codes in FP32; out = BF16_rn(O * dv / l).
+ * NVFP4 arithmetic (FlashInfer docs, description: two-level P with the row maximum brought to
+ * 448*6): S = deq(Q codes) . deq(K codes) on the block-scaled FP4 tensor cores (FP32
+ * accumulation), plus qm . deq(K codes) for the query's 128-row block mean qm (FP32); in log2
+ * units s = (S + qm.K) * softmax_scale * log2(e);
+ * online softmax over 64-key tiles from each segment start with the exact running row maximum m
+ * (O and l rescaled by 2^(m_old - m) whenever it moves); P' = 2^(s - m) * 2688; per 16 keys a
+ * UE4M3 scale E4M3_rn(max P' / 6) and E2M1_rn codes of P' / scale; l sums the dequantized P; O
+ * accumulates deq(P) * deq(V) in FP32; out = BF16_rn(O / l).
  * Errors: STATE (no quantize on this plan yet), INVALID_ARG, UNSUPPORTED, CUDA.
  */
 FA_LP_API int fa_lp_forward_varlen(fa_lp_plan* plan, const int32_t* cu_seqlens_dev, void* out,
@@ -171,7 +179,7 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
 #define FA_LP_DESCALE 3     /* FP8: f32 [3][H] = amax/448 of q, k, v                             */
 #define FA_LP_Q_SCALES 4    /* NVFP4: u8 [H][Tpad][8] UE4M3, one per 16 channels                 */
 #define FA_LP_K_SCALES 5    /* NVFP4: u8 [H][Tpad][8]                                            */
-#define FA_LP_V_SCALES 6    /* NVFP4: u8 [H][128][Tpad/16], one per 16 keys                      */
+#define FA_LP_V_SCALES 6    /* NVFP4: u8 [H][Tpad/128][128][8], one per 16 keys per channel      */
 #define FA_LP_Q_MEANS 7     /* NVFP4: f32 [H][Tpad/128][128], block means                        */
 #define FA_LP_K_MEANS 8     /* NVFP4: f32 [num_segments][H][128], segment means                  */
 

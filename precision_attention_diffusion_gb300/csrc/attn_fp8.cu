@@ -242,19 +242,6 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const Wor
   drain_phase(smem_u32(&S.bar_drain[t]), 0);
 }
 
-// Row maximum of 64 values: four independent 3-input-max chains, then a combine.
-__device__ __forceinline__ float row_max64(const float (&s)[64]) {
-  float acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    acc[k] = max3f(s[k], s[k + 4], s[k + 8]);
-#pragma unroll
-    for (int i = 3; i < 15; i += 2) acc[k] = max3f(acc[k], s[k + 4 * i], s[k + 4 * (i + 1)]);
-    acc[k] = fmaxf(acc[k], s[k + 60]);
-  }
-  return fmaxf(max3f(acc[0], acc[1], acc[2]), acc[3]);
-}
-
 __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
                                                      const WorkItem& wi, const SegInfo& sg,
                                                      uint32_t tmem, int t, int wq, int lane) {

@@ -1,0 +1,586 @@
+// attn_nvfp4.cu -- NVFP4 packed-varlen attention forward on 5th-generation tensor cores with
+// block-scaled FP4 operands (tcgen05.mma kind::mxf4nvf4: E2M1 values, one UE4M3 scale per 16
+// elements along the contraction).
+//
+// Passage: FlashInfer docs, flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4,
+// description: SageAttention3-style FP4 attention -- K centred by its segment's per-channel mean
+// (which leaves softmax unchanged), Q centred by its 128-row block mean with qm K^T added back,
+// E2M1 codes with UE4M3 scales per 16 elements, V transposed with per-16-key scales, and a
+// two-level P: the row maximum is brought to 448 * 6 = 2688 and every 16 keys get their own scale.
+//
+// What one CTA computes (readings r5 with tau = 0, r9, r11, r12): for the two 128-row query tiles
+// Q0, Q1 of one (segment, head), over 64-key sub-tiles u from the segment start,
+//   s''(i, j)  = (deq(Qc_i) . deq(Kc_j)) c + c_t(j),  c_t(j) = (qm_t . deq(Kc_j)) c,
+//                with c = softmax_scale log2(e)            (log2 units)
+//   m_i        = running row maximum of s'' (exact: it moves whenever a sub-tile exceeds it)
+//   P'(i, j)   = 2^(s'' - m_i + log2 2688)                  (= 2688 exp(S' - m) of the pages)
+//   per 16 keys: sf = UE4M3(amax / 6), code = E2M1(P' / deq(sf))
+//   l_i        = l_i 2^(m_old - m_new) + sum deq(P),   O_i likewise with deq(P) deq(V)
+//   out        = BF16(O / l) for rows inside the segment.
+//
+// Roles (480 threads):
+//   warp 8      TMA: Q codes (64-byte rows, 64-byte swizzle) and, by plain bulk copies, Q scale
+//               records and Q block means once; then per 128-key tile K codes + K scale record
+//               and V^T codes + V scale record into a 4-stage ring;
+//   warps 9/10  MMA issue for query tile 0/1 (tensor memory allocated by warp 9):
+//                 S_t(u)  = deq(Qc_t) deq(Kc(u))^T   2 MMAs M=128 N=64  K=64, A, B in smem
+//                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=128 K=64, A = P in TMEM
+//   warps 11-14 per sub-tile: K and V scale factors into tensor memory (the MMA reads the B-side
+//               scales of row n from column n / 32 of every lane quarter, so each of the four
+//               warps writes its own quarter), and c_t(j) for both query tiles into shared memory
+//               (FP32 products and sums);
+//   warps 0-7   softmax of tile 0 (warps 0-3) and 1 (warps 4-7), one thread per query row (row ==
+//               tensor-memory lane); P codes and P scales go to tensor memory (A-side scales: row
+//               r in lane r, column r / 32), O is rescaled in tensor memory when a row's maximum
+//               moves, and the same threads run the epilogue.
+// Tensor memory (512 columns): per query tile t a 64-column S, two P slots (8 columns of codes
+// and 4 of scales each) and a 128-column O; then Q, K (two buffers) and V (two buffers) scale
+// blocks. Every barrier wait is bounded; on expiry the kernel records an error, drains its
+// in-flight copies and MMAs, frees its tensor memory and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_sync.cuh"
+#include "fa_lp_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace falp {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 480;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;      // warps 9 and 10
+constexpr int kCorrWarp = 11;    // warps 11-14
+constexpr int kSub = 64;         // keys per sub-tile
+constexpr uint32_t kCodeTile = 128 * 64;  // 128 rows of 128 E2M1 codes
+constexpr uint32_t kSfTile = 128 * 8;     // 128 rows of 8 UE4M3 scales
+constexpr uint32_t kIdescS = idesc_mxf4nvf4(128, kSub);
+constexpr uint32_t kIdescPV = idesc_mxf4nvf4(128, 128);
+constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
+
+// tensor-memory columns
+__device__ __forceinline__ uint32_t col_s(int t) { return 224u * uint32_t(t); }
+__device__ __forceinline__ uint32_t col_p(int t, int x) { return 224u * uint32_t(t) + 64u + 16u * uint32_t(x); }
+__device__ __forceinline__ uint32_t col_psf(int t, int x) { return col_p(t, x) + 8u; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 224u * uint32_t(t) + 96u; }
+__device__ __forceinline__ uint32_t col_qsf(int t) { return 448u + 8u * uint32_t(t); }
+__device__ __forceinline__ uint32_t col_ksf(int b) { return 464u + 8u * uint32_t(b); }
+__device__ __forceinline__ uint32_t col_vsf(int b) { return 480u + 4u * uint32_t(b); }
+
+struct Smem {
+  uint8_t q[2][kCodeTile];
+  uint8_t k[kStages][kCodeTile];
+  uint8_t v[kStages][kCodeTile];   // V^T: 128 channel rows of 128 keys
+  uint8_t qsf[2][kSfTile];
+  uint8_t ksf[kStages][kSfTile];   // [key][8]
+  uint8_t vsf[kStages][kSfTile];   // [channel][8]
+  float qm[2][kD];
+  float c[2][2][kSub];             // [u & 1][t][key]: c_t(j) in log2 units
+  uint64_t bar_q;
+  uint64_t bar_k[kStages];
+  uint64_t bar_v[kStages];
+  uint64_t bar_free[kStages];      // MMA commits of both tiles + the four correction warps
+  uint64_t bar_s[2];               // [t]: S_t(u) written (MMA commit)
+  uint64_t bar_sr[2];              // [t]: S_t(u) read by the softmax (128 arrivals)
+  uint64_t bar_p[2][2];            // [t][u & 1]: P_t(u) written and O rescaled (128 arrivals)
+  uint64_t bar_o[2][2];            // [t][u & 1]: PV_t(u) done (MMA commit)
+  uint64_t bar_c[2];               // [u & 1]: scale factors in TMEM and c(u) in smem (128)
+  uint64_t bar_cfree[2];           // [u & 1]: c(u) read, MMAs of u done (128 nq + nq)
+  uint64_t bar_drain[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+
+struct Nvfp4Args {
+  const SegInfo* segs;
+  const WorkItem* work;
+  const uint8_t* q_sf;     // [H][Tp][8]
+  const uint8_t* k_sf;     // [H][Tp][8]
+  const uint8_t* v_sf;     // [H][Tp/128][128][8]
+  const float* q_mean;     // [H][Tp/128][128]
+  __nv_bfloat16* out;
+  int64_t ost, osh;
+  int64_t tpad;
+  float scale_log2;
+  WaitCtx w;
+};
+
+enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4,
+                  kRoleCorrection = 5 };
+
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, Smem& S,
+                                         const Nvfp4Args& a, int role) {
+  return __all_sync(0xffffffffu, wait_phase(smem_u32(bar), parity, &S.abort_flag, a.w, role));
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  const uint32_t h2 = cvt_e4m3x2_to_f16x2(uint16_t(code & 0xFF));
+  return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// ---------------------------------------------------------------------------------------------
+// TMA / bulk-copy producer (whole warp, converged; one elected lane issues).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                         const CUtensorMap* tm_v, Smem& S, const Nvfp4Args& a,
+                                         const WorkItem& wi, const SegInfo& sg) {
+  const int n_kv = sg.nblk;
+  const int64_t Tp = a.tpad, h = wi.head;
+  const int rq = sg.row0 + wi.qt0 * kTile;
+  mbar_arrive_expect_tx_elect(smem_u32(&S.bar_q), uint32_t(wi.nq) * (kCodeTile + kSfTile + 512));
+  for (int t = 0; t < wi.nq; ++t) {
+    const int row = rq + t * kTile;
+    tma_load_3d_elect(smem_u32(S.q[t]), tm_q, smem_u32(&S.bar_q), 0, row, wi.head);
+    bulk_load_elect(smem_u32(S.qsf[t]), a.q_sf + (h * Tp + row) * 8, kSfTile, smem_u32(&S.bar_q));
+    bulk_load_elect(smem_u32(S.qm[t]), a.q_mean + (h * (Tp / kTile) + row / kTile) * kD, 512,
+                    smem_u32(&S.bar_q));
+  }
+  int issued = 0;
+  for (int j = 0; j < n_kv; ++j) {
+    const int st = j % kStages;
+    if (j >= kStages && !wait_all(&S.bar_free[st], ((j / kStages) - 1) & 1, S, a, kRoleProducer))
+      break;
+    const int row = sg.row0 + j * kTile;
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]), kCodeTile + kSfTile);
+    tma_load_3d_elect(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_k[st]), 0, row, wi.head);
+    bulk_load_elect(smem_u32(S.ksf[st]), a.k_sf + (h * Tp + row) * 8, kSfTile,
+                    smem_u32(&S.bar_k[st]));
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[st]), kCodeTile + kSfTile);
+    tma_load_3d_elect(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_v[st]), row / 2, 0, wi.head);
+    bulk_load_elect(smem_u32(S.vsf[st]), a.v_sf + (h * (Tp / kTile) + row / kTile) * kSfTile,
+                    kSfTile, smem_u32(&S.bar_v[st]));
+    issued = j + 1;
+  }
+  // No copy may still be landing in shared memory when the CTA exits.
+  drain_phase(smem_u32(&S.bar_q), 0);
+  for (int j = max(0, issued - kStages); j < issued; ++j) {
+    const int st = j % kStages;
+    drain_phase(smem_u32(&S.bar_k[st]), (j / kStages) & 1);
+    drain_phase(smem_u32(&S.bar_v[st]), (j / kStages) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// MMA issue for query tile t (whole warp, converged; one elected lane issues). Order per step u:
+// S_t(u) as soon as the softmax has read S_t(u-1) and the scale factors of u are in tensor
+// memory, then PV_t(u-1) once P_t(u-1) is written: the tensor pipe computes the next scores while
+// the softmax works on the current ones.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
+                                           const SegInfo& sg, uint32_t tmem, int t) {
+  const int n_sub = (sg.len + kSub - 1) / kSub;
+  // The start-address field holds (address >> 4): moving an operand by `off` bytes (a K step of
+  // 64 E2M1 codes = 32 bytes, a sub-tile, a stage) adds off >> 4.
+  const uint64_t dq = sdesc_kmajor_sw64(smem_u32(S.q[t]));
+  const uint64_t dk = sdesc_kmajor_sw64(smem_u32(S.k[0]));
+  const uint64_t dv = sdesc_kmajor_sw64(smem_u32(S.v[0]));
+  auto issue_s = [&](int u) {
+    const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
+    const uint64_t kb = dk + (((j % kStages) * kCodeTile + h * (kSub * 64)) >> 4);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+      mma_mxf4_ss_elect(tmem + col_s(t), dq + 2 * kk, kb + 2 * kk, kIdescS,
+                        tmem + col_qsf(t) + 4 * kk, tmem + col_ksf(int(h)) + 4 * kk, kk > 0);
+    mma_commit_elect(smem_u32(&S.bar_s[t]));
+  };
+  // keys [64h, 64h + 64) of a 128-key tile are bytes [32h, 32h + 32) of each V^T row
+  auto issue_pv = [&](int u) {
+    const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
+    const uint64_t vb = dv + (((j % kStages) * kCodeTile) >> 4) + 2 * h;
+    mma_mxf4_ts_elect(tmem + col_o(t), tmem + col_p(t, int(h)), vb, kIdescPV,
+                      tmem + col_psf(t, int(h)), tmem + col_vsf(int(h)), u > 0 ? 1u : 0u);
+    mma_commit_elect(smem_u32(&S.bar_o[t][h]));
+    mma_commit_elect(smem_u32(&S.bar_cfree[h]));
+    if (h == 1 || u + 1 == n_sub) mma_commit_elect(smem_u32(&S.bar_free[j % kStages]));
+  };
+  do {
+    if (!wait_all(&S.bar_q, 0, S, a, kRoleMma)) break;
+    bool ok = true;
+    for (int u = 0; u <= n_sub && ok; ++u) {
+      if (u < n_sub) {
+        const int j = u >> 1;
+        if (u > 0 && !(ok = wait_all(&S.bar_sr[t], (u - 1) & 1, S, a, kRoleMma))) break;
+        if ((u & 1) == 0 &&
+            !(ok = wait_all(&S.bar_k[j % kStages], (j / kStages) & 1, S, a, kRoleMma)))
+          break;
+        if (!(ok = wait_all(&S.bar_c[u & 1], (u >> 1) & 1, S, a, kRoleMma))) break;
+        tc_fence_after();
+        issue_s(u);
+      }
+      if (u > 0) {
+        const int w = u - 1, j = w >> 1;
+        if ((w & 1) == 0 &&
+            !(ok = wait_all(&S.bar_v[j % kStages], (j / kStages) & 1, S, a, kRoleMma)))
+          break;
+        if (!(ok = wait_all(&S.bar_p[t][w & 1], (w >> 1) & 1, S, a, kRoleMma))) break;
+        tc_fence_after();
+        issue_pv(w);
+      }
+    }
+  } while (false);
+  // Every MMA issued so far must finish before the tensor memory is released.
+  mma_commit_elect(smem_u32(&S.bar_drain[t]));
+  drain_phase(smem_u32(&S.bar_drain[t]), 0);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Correction warps: scale factors of K and V into tensor memory, and c_t(j) = (qm_t . deq(Kc_j)) c
+// for both query tiles in FP32. Thread (warp cw, lane) takes channel quarter lane >> 3 (32
+// channels = one 16-byte chunk of the key row, two scale groups) of keys 16 cw + 8 pass +
+// (lane & 7); the four quarters of a key combine by two shuffles (the same sum in all four lanes,
+// float addition being commutative).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void correction(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
+                                           const SegInfo& sg, uint32_t tmem, int cw, int lane) {
+  const int n_sub = (sg.len + kSub - 1) / kSub;
+  const int quarter = (kCorrWarp + cw) & 3;  // tensor-memory lane quarter this warp may access
+  const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+  const int cq = lane >> 3;                  // channel quarter
+  if (!wait_all(&S.bar_q, 0, S, a, kRoleCorrection)) return;
+  // Q scale factors (A side: row r in lane r, column r / 32; K step kk at +4kk).
+  {
+    const int r = quarter * 32 + lane;
+    for (int t = 0; t < wi.nq; ++t) {
+      const uint2 w = *reinterpret_cast<const uint2*>(S.qsf[t] + r * 8);
+      tmem_st1(tmem + col_qsf(t) + uint32_t(quarter) + lane_off, w.x);
+      tmem_st1(tmem + col_qsf(t) + 4u + uint32_t(quarter) + lane_off, w.y);
+    }
+  }
+  // qm_t of channels 32 cq + 2i, 32 cq + 2i + 1
+  float2 qmf[2][16];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      qmf[t][i] = t < wi.nq ? *reinterpret_cast<const float2*>(&S.qm[t][32 * cq + 2 * i])
+                            : make_float2(0.f, 0.f);
+  const float cs = a.scale_log2;
+  for (int u = 0; u < n_sub; ++u) {
+    const int j = u >> 1, h = u & 1, st = j % kStages, b = u & 1;
+    if (h == 0) {
+      if (!wait_all(&S.bar_k[st], (j / kStages) & 1, S, a, kRoleCorrection)) break;
+      if (!wait_all(&S.bar_v[st], (j / kStages) & 1, S, a, kRoleCorrection)) break;
+    }
+    if (u >= 2 && !wait_all(&S.bar_cfree[b], ((u - 2) >> 1) & 1, S, a, kRoleCorrection)) break;
+    // B-side scale factors, every lane quarter: K rows (keys) 32c + lane in column c of K step kk;
+    // V rows (channels) 32c + lane in column c, word h of the channel's 8-byte record.
+    {
+      const uint2 k0 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + lane) * 8);
+      const uint2 k1 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + 32 + lane) * 8);
+      const uint32_t kw[8] = {k0.x, k1.x, 0u, 0u, k0.y, k1.y, 0u, 0u};
+      tmem_st8(tmem + col_ksf(b) + lane_off, kw);
+      const uint32_t* vs = reinterpret_cast<const uint32_t*>(S.vsf[st]);
+      tmem_st4(tmem + col_vsf(b) + lane_off, vs[lane * 2 + h], vs[(32 + lane) * 2 + h],
+               vs[(64 + lane) * 2 + h], vs[(96 + lane) * 2 + h]);
+    }
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int key = 16 * cw + 8 * pass + (lane & 7);
+      const int row = 64 * h + key;  // row of the 128-key tile
+      // 64-byte swizzle: 16-byte chunk c of row r is stored at chunk c ^ ((r >> 1) & 3)
+      const uint4 cv = *reinterpret_cast<const uint4*>(S.k[st] + row * 64 +
+                                                       ((cq ^ ((row >> 1) & 3)) << 4));
+      const uint32_t sfh = *reinterpret_cast<const uint16_t*>(S.ksf[st] + row * 8 + 2 * cq);
+      const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
+      float tot0 = 0.f, tot1 = 0.f;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {  // 16 channels = 8 bytes = words 2g, 2g + 1
+        float a0x = 0.f, a0y = 0.f, a1x = 0.f, a1y = 0.f;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const uint32_t byte = (w[2 * g + (p >> 2)] >> (8 * (p & 3))) & 0xFFu;
+          const float2 f = f16x2_to_f32x2(cvt_e2m1x2_to_f16x2(byte));
+          const float2 m0 = qmf[0][8 * g + p], m1 = qmf[1][8 * g + p];
+          fma2v(a0x, a0y, f.x, f.y, m0.x, m0.y, a0x, a0y);
+          fma2v(a1x, a1y, f.x, f.y, m1.x, m1.y, a1x, a1y);
+        }
+        const float ds = e4m3_to_f32(sfh >> (8 * g));
+        tot0 = fmaf(a0x + a0y, ds, tot0);
+        tot1 = fmaf(a1x + a1y, ds, tot1);
+      }
+      tot0 += __shfl_xor_sync(0xffffffffu, tot0, 8);
+      tot0 += __shfl_xor_sync(0xffffffffu, tot0, 16);
+      tot1 += __shfl_xor_sync(0xffffffffu, tot1, 8);
+      tot1 += __shfl_xor_sync(0xffffffffu, tot1, 16);
+      if (cq == 0) S.c[b][0][key] = tot0 * cs;
+      else if (cq == 1) S.c[b][1][key] = tot1 * cs;
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&S.bar_c[b]));
+    if (h == 1 || u + 1 == n_sub) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.bar_free[st]));
+    }
+  }
+  tmem_wait_st();
+}
+
+// Maximum of 16 values (3-input max tree).
+__device__ __forceinline__ float max16(const float (&p)[16]) {
+  const float a = max3f(p[0], p[1], p[2]), b = max3f(p[3], p[4], p[5]);
+  const float c = max3f(p[6], p[7], p[8]), d = max3f(p[9], p[10], p[11]);
+  const float e = max3f(p[12], p[13], p[14]);
+  return fmaxf(max3f(a, b, c), max3f(d, e, p[15]));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Softmax of query tile t (one thread per row, row == tensor-memory lane) and the epilogue.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a,
+                                                     const WorkItem& wi, const SegInfo& sg,
+                                                     uint32_t tmem, int t, int wq, int lane) {
+  const int n_sub = (sg.len + kSub - 1) / kSub;
+  const float cs = a.scale_log2;
+  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const uint32_t s_addr = tmem + col_s(t) + lane_off;
+  const uint32_t o_addr = tmem + col_o(t) + lane_off;
+  const int last_valid = sg.len - (n_sub - 1) * kSub;  // keys of the last sub-tile, 1..64
+  float m = -INFINITY, l = 0.f;                         // running maximum (log2 units), sum
+  bool ok = true;
+  for (int u = 0; u < n_sub; ++u) {
+    const int x = u & 1;
+    if (!(ok = wait_all(&S.bar_s[t], uint32_t(u) & 1, S, a, kRoleSoftmax))) break;
+    tc_fence_after();
+    uint32_t r[2][32];
+    tmem_ld32(s_addr, r[0]);
+    tmem_ld32(s_addr + 32, r[1]);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&S.bar_sr[t]));  // S_t(u+1) may now overwrite S
+    if (!(ok = wait_all(&S.bar_c[x], (u >> 1) & 1, S, a, kRoleSoftmax))) break;
+    // s'' = S c + c_t(j)
+    float s[64];
+    const float4* cp = reinterpret_cast<const float4*>(S.c[x][t]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float4 cc = cp[i];
+      const int k0 = 4 * i;
+      fma2v(s[k0], s[k0 + 1], __uint_as_float(r[k0 >> 5][k0 & 31]),
+            __uint_as_float(r[k0 >> 5][(k0 + 1) & 31]), cs, cs, cc.x, cc.y);
+      fma2v(s[k0 + 2], s[k0 + 3], __uint_as_float(r[k0 >> 5][(k0 + 2) & 31]),
+            __uint_as_float(r[k0 >> 5][(k0 + 3) & 31]), cs, cs, cc.z, cc.w);
+    }
+    mbar_arrive(smem_u32(&S.bar_cfree[x]));
+    if (u == n_sub - 1 && last_valid < kSub) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (i >= last_valid) s[i] = -INFINITY;
+    }
+    const float mx = row_max64(s);
+    const bool move = mx > m;  // exact running maximum
+    const float m_new = move ? mx : m;
+    const float alpha = move ? ex2_approx(m - m_new) : 1.f;  // m = -inf gives 0
+    const float bias = kLog2_2688 - m_new;
+    uint32_t pk[8];
+    uint32_t sfw = 0u;
+    float rs = 0.f;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {  // 16 keys per scale group
+      float pp[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        float x0, x1;
+        fma2(x0, x1, s[16 * g + i], s[16 * g + i + 1], 1.f, bias);
+        pp[i] = ex2_approx(x0);  // P' = 2688 2^(s'' - m)
+        pp[i + 1] = ex2_approx(x1);
+      }
+      // second level: UE4M3 scale of the group, E2M1 codes of P' / deq(scale)
+      const uint32_t sf = cvt_e4m3x2(__fdiv_rn(max16(pp), 6.f), 0.f) & 0xFFu;
+      const float ds = e4m3_to_f32(sf);
+      const float rds = sf ? __frcp_rn(ds) : 0.f;
+      uint32_t w0 = 0u, w1 = 0u, hs = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float y0, y1;
+        fma2(y0, y1, pp[2 * i], pp[2 * i + 1], rds, 0.f);
+        const uint32_t byte = cvt_e2m1x2(y0, y1);
+        if (i < 4) w0 |= byte << (8 * i);
+        else w1 |= byte << (8 * (i - 4));
+        // the quantized values, back in f16 (exact; a group sums to at most 96 in steps of 0.5)
+        hs = hadd2_u32(hs, cvt_e2m1x2_to_f16x2(byte));
+      }
+      pk[2 * g] = w0;
+      pk[2 * g + 1] = w1;
+      const float2 hf = f16x2_to_f32x2(hs);
+      rs = fmaf(hf.x + hf.y, ds, rs);  // l sums the dequantized P (reading r6)
+      sfw |= sf << (8 * g);
+    }
+    l = l * alpha + rs;
+    // P slot x was last read by PV_t(u-2)
+    if (u >= 2) {
+      if (!(ok = wait_all(&S.bar_o[t][x], ((u - 2) >> 1) & 1, S, a, kRoleSoftmax))) break;
+      tc_fence_after();
+    }
+    tmem_st8(tmem + col_p(t, x) + lane_off, pk);
+    tmem_st1(tmem + col_psf(t, x) + uint32_t(wq) + lane_off, sfw);
+    if (u > 0 && __any_sync(0xffffffffu, move)) {
+      // rescale O between PV_t(u-1) and PV_t(u)
+      if (!(ok = wait_all(&S.bar_o[t][x ^ 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + 32 * i, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st32(o_addr + 32 * i, o);
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&S.bar_p[t][x]));
+    m = m_new;
+  }
+  if (!ok) {
+    tmem_wait_st();
+    return;
+  }
+  // PV_t(n_sub - 1) done implies every earlier PV of this in-order stream is done
+  if (!wait_all(&S.bar_o[t][(n_sub - 1) & 1], ((n_sub - 1) >> 1) & 1, S, a, kRoleEpilogue))
+    return;
+  tc_fence_after();
+  const float f = __frcp_rn(l);
+  const int qrow = (wi.qt0 + t) * kTile + wq * 32 + lane;
+  const bool valid = qrow < sg.len;
+  __nv_bfloat16* dst = a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(wi.head) * a.osh;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t o[32];
+    tmem_ld32(o_addr + 32 * i, o);
+    tmem_wait_ld();
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const __nv_bfloat162 bb = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * f,
+                                                      __uint_as_float(o[2 * e + 1]) * f);
+      w[e] = *reinterpret_cast<const uint32_t*>(&bb);
+    }
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * i);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ Nvfp4Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem wi = a.work[blockIdx.x];
+  const SegInfo sg = a.segs[wi.seg];
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&S.bar_q), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&S.bar_k[i]), 1);
+      mbar_init(smem_u32(&S.bar_v[i]), 1);
+      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 4);  // MMA commits + correction warps
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&S.bar_s[t]), 1);
+      mbar_init(smem_u32(&S.bar_sr[t]), 128);
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(smem_u32(&S.bar_p[t][x]), 128);
+        mbar_init(smem_u32(&S.bar_o[t][x]), 1);
+      }
+      mbar_init(smem_u32(&S.bar_drain[t]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&S.bar_c[b]), 128);
+      mbar_init(smem_u32(&S.bar_cfree[b]), 128 * wi.nq + wi.nq);
+    }
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&S.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == kTmaWarp) {
+    producer(&tm_q, &tm_k, &tm_v, S, a, wi, sg);
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    const int t = warp - kMmaWarp;
+    if (t < wi.nq) mma_issuer(S, a, wi, sg, tmem, t);
+  } else if (warp >= kCorrWarp) {
+    correction(S, a, wi, sg, tmem, warp - kCorrWarp, lane);
+  } else {
+    const int t = warp >> 2;
+    if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 3, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
+                           cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes)) != cudaSuccess)
+      return FA_LP_ERR_CUDA;
+    attr_set = true;
+  }
+  const uint64_t H = uint64_t(p.heads), Tp = uint64_t(p.tpad);
+  CUtensorMap tq, tk, tv;
+  // Q, K codes: [H][Tp][64 bytes]; V^T codes: [H][128][Tp / 2 bytes]; boxes of 128 rows x 64 B
+  int st = encode_tmap_3d_u8(&tq, ws + p.ws.q_codes, 64, Tp, H, 64, Tp * 64, 64, 128,
+                             CU_TENSOR_MAP_SWIZZLE_64B);
+  if (st == FA_LP_OK)
+    st = encode_tmap_3d_u8(&tk, ws + p.ws.k_codes, 64, Tp, H, 64, Tp * 64, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+  if (st == FA_LP_OK)
+    st = encode_tmap_3d_u8(&tv, ws + p.ws.v_codes, Tp / 2, 128, H, Tp / 2, 128 * (Tp / 2), 64,
+                           128, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (st != FA_LP_OK) return st;
+  Nvfp4Args a;
+  a.segs = p.d_segs;
+  a.work = p.d_work;
+  a.q_sf = ws + p.ws.q_sf;
+  a.k_sf = ws + p.ws.k_sf;
+  a.v_sf = ws + p.ws.v_sf;
+  a.q_mean = reinterpret_cast<const float*>(ws + p.ws.q_mean);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ost = ost;
+  a.osh = osh;
+  a.tpad = p.tpad;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.w.err = p.d_err;
+  a.w.abort_word = p.d_err + 1;
+  a.w.gen = next_launch_generation();
+  a.w.spin_limit = p.spin_limit;
+  attn_nvfp4_kernel<<<unsigned(p.work.size()), kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace falp

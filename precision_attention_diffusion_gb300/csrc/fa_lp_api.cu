@@ -455,7 +455,7 @@ int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
     case FA_LP_V_CODES: return set(p->ws.v_codes, H, 128, Tp / 2, 1);
     case FA_LP_Q_SCALES: return set(p->ws.q_sf, H, Tp, 8, 1);
     case FA_LP_K_SCALES: return set(p->ws.k_sf, H, Tp, 8, 1);
-    case FA_LP_V_SCALES: return set(p->ws.v_sf, H, 128, Tp / 16, 1);
+    case FA_LP_V_SCALES: return set(p->ws.v_sf, H, Tp / 128, 1024, 1);
     case FA_LP_Q_MEANS: return set(p->ws.q_mean, H, Tp / 128, 128, 4);
     case FA_LP_K_MEANS: return set(p->ws.k_mean, p->nseg, H, 128, 4);
     default: return FA_LP_ERR_INVALID_ARG;

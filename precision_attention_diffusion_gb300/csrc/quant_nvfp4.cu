@@ -14,7 +14,8 @@
 //   Q, K codes : u8 [H][Tpad][64]    two E2M1 codes per byte, even channel in the low nibble
 //   Q, K scales: u8 [H][Tpad][8]     UE4M3, one per 16 channels
 //   V^T codes  : u8 [H][128][Tpad/2] two keys per byte, even key in the low nibble
-//   V scales   : u8 [H][128][Tpad/16] one per 16 keys (groups start at the segment start)
+//   V scales   : u8 [H][Tpad/128][128][8] one per 16 keys (groups start at the segment start);
+//                each 128-key tile's scales are one contiguous 1 KB record
 //   Q means    : f32 [H][Tpad/128][128]; K means: f32 [num_segments][H][128]
 // Padding rows / keys hold code 0 and scale 0.
 #include <cuda_bf16.h>
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(256) nvfp4_pack_vt_kernel(
     const uint32_t packed = group16(x, &sf);
     uint8_t* row = vt + (int64_t(h) * kD + c) * (Tp / 2) + int64_t(b) * (kTile / 2);
     reinterpret_cast<uint16_t*>(row)[g * 4 + (lane & 3)] = uint16_t(packed);
-    if ((lane & 3) == 0) vs[(int64_t(h) * kD + c) * (Tp / 16) + int64_t(b) * 8 + g] = sf;
+    if ((lane & 3) == 0) vs[((int64_t(h) * (Tp / kTile) + b) * kD + c) * 8 + g] = sf;
   }
 }
 

@@ -106,6 +106,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32
       : "memory");
 }
 
+// Plain (non-tensor) bulk copy global -> shared of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing on an mbarrier; one elected lane issues.
+__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      "\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -287,6 +300,54 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
       : "memory");
 }
 
+// Shared-memory descriptor, K-major operand with 64-byte rows staged by TMA with 64-byte
+// swizzling: 8-row groups 512 bytes apart, tile base 512-aligned, layout code 4 (SWIZZLE_64B).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(512 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf4nvf4 (block-scaled FP4): A and B E2M1 (format code 1),
+// scale factors UE4M3 (bit 23 = 0), scale-factor ids 0 (all four 16-element blocks of a K=64
+// step), both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A B^T with one UE4M3 scale per 16 elements of K (scale_vec::4X). The scale
+// factors of one K=64 step occupy 4 tensor-memory columns: row 32c + i in column c; A's in the
+// row's own lane quarter (lane 32c + i), B's repeated in every lane quarter (lane i + 32q).
+__device__ __forceinline__ void mma_mxf4_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %3, "
+      "[%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 async operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -318,6 +379,25 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_to_f16x2(uint16_t v) {
   return r;
 }
 
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
+                                         uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// One byte of two E2M1 codes (low nibble first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t cvt_e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(byte));
+  return r;
+}
+
 // Two fp32 -> two E2M1 codes in one byte (round to nearest even, saturate to +-6);
 // `lo` lands in the low nibble.
 __device__ __forceinline__ uint8_t cvt_e2m1x2(float lo, float hi) {
@@ -337,6 +417,19 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
+// Row maximum of 64 values: four independent 3-input-max chains, then a combine.
+__device__ __forceinline__ float row_max64(const float (&s)[64]) {
+  float acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    acc[k] = max3f(s[k], s[k + 4], s[k + 8]);
+#pragma unroll
+    for (int i = 3; i < 15; i += 2) acc[k] = max3f(acc[k], s[k + 4 * i], s[k + 4 * (i + 1)]);
+    acc[k] = fmaxf(acc[k], s[k + 60]);
+  }
+  return fmaxf(max3f(acc[0], acc[1], acc[2]), acc[3]);
+}
+
 // (d0, d1) = (a0, a1) * b + c on the packed fp32x2 FMA (one issue slot for two results).
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
   asm("{\n\t.reg .b64 x, y, z, w;\n\t"
@@ -347,6 +440,26 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       "mov.b64 {%0, %1}, w;\n\t}"
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1) on the packed fp32x2 FMA.
+__device__ __forceinline__ void fma2v(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Packed f16x2 fused multiply-add on raw 32-bit registers.
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
 }
 
 // Packed f16x2 addition on raw 32-bit registers.

@@ -1,15 +1,28 @@
-"""NVFP4 quantization (FlashInfer docs, minimax_h3_sm120_varlen_attention_nvfp4, description) on
-the GPU through the C ABI, bit-exact against the oracle: K segment means, Q block means, E2M1
-codes and UE4M3 scales of Q, K and V^T, padding bytes zero."""
+"""NVFP4 path (FlashInfer docs, minimax_h3_sm120_varlen_attention_nvfp4, description) on the GPU
+through the C ABI, against the oracle.
+
+Quantization is bit-exact: K segment means, Q block means, E2M1 codes and UE4M3 scales of Q, K
+and V^T, padding bytes zero. The attention output must be within atol 1.0 / rtol 0.1 of FP64
+exact attention (C1), the bar the pages state, and close to the NVFP4-emulating oracle (C3, with
+the kernel's 64-key tiles): relative RMS <= TOL_EMU overall and <= TOL_ROW for every row. C3 takes
+exact products where the kernel rounds (FP32 scores, sums and qm K^T term, exp2 on the MUFU,
+P' / deq(scale) as a product with the reciprocal); those roundings move the rare E2M1 code of P
+that sits within about 1e-6 of a rounding boundary, and one such code of a heavy key moves its
+row by up to a few percent.
+"""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from precision_attention_diffusion_gb300 import inputs
-from parity import bits, padded_rows
+from parity import SCALE, all_rows, bits, out_rows, padded_rows, rel_rms
 
 pytestmark = pytest.mark.gpu
+
+KV_TILE = 64       # the kernel's online-softmax tile (exact running maximum)
+TOL_EMU = 1e-2     # relative RMS against the NVFP4-emulating oracle
+TOL_ROW = 5e-2     # worst single row against the emulating oracle
 
 
 @pytest.fixture(scope="module")
@@ -67,7 +80,9 @@ def check_nvfp4_quant(fa, q, k, v, cu, H):
         got = g["Q_MEANS"][:, b0:b0 + nb].transpose(1, 0, 2)          # [nb][H][128]
         want = z["qm"][z["qoff"][s]:z["qoff"][s] + nb]
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), f"q means seg {s}"
-        assert np.array_equal(g["V_SCALES"][:, :, g0:g0 + ng],
+        H = g["V_SCALES"].shape[0]
+        vs = g["V_SCALES"].reshape(H, -1, 128, 8).transpose(0, 2, 1, 3).reshape(H, 128, -1)
+        assert np.array_equal(vs[:, :, g0:g0 + ng],
                               z["sv"][:, :, z["goff"][s]:z["goff"][s] + ng]), f"v scales seg {s}"
     return plan, z
 
@@ -99,3 +114,81 @@ def test_nvfp4_quantize_h3_shape(fa):
     S, H = 30272, 56
     q, k, v = inputs.qkv_separate(S, H, seed=0)
     check_nvfp4_quant(fa, q, with_k_offset(k, H, 0), v, [0, S], H)
+
+
+def run_nvfp4(fa, q, k, v, cu, H):
+    plan = fa.Plan(cu, H, mode=fa.MODE_NVFP4)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    cu_dev = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    plan.attention(q.cuda(), k.cuda(), v.cuda(), cu_dev, out=out)
+    torch.cuda.synchronize()
+    return plan, out
+
+
+def check_nvfp4_out(out, q, k, v, z, cu, rows):
+    got = out_rows(out, rows)
+    emu, _ = oracle.attn_nvfp4(z, cu, rows, SCALE, n_kv=KV_TILE)
+    exact = oracle.attn_exact(bits(q), bits(k), bits(v), cu, rows, SCALE)
+    e_emu = rel_rms(got, emu)
+    per_row = np.linalg.norm(got - emu, axis=1) / np.maximum(np.linalg.norm(emu, axis=1), 1e-30)
+    assert np.all(np.isfinite(got))
+    assert e_emu <= TOL_EMU, f"rel RMS vs emulating oracle {e_emu:.3e}"
+    assert per_row.max() <= TOL_ROW, f"worst row {per_row.max():.3e}"
+    assert np.allclose(got, exact, atol=1.0, rtol=0.1), "outside atol 1.0 / rtol 0.1 of exact"
+    return e_emu, rel_rms(got, exact)
+
+
+def test_nvfp4_attention_small(fa):
+    cu, H = [0, 256], 2
+    q, k, v = inputs.qkv_separate(256, H, seed=0)
+    k = with_k_offset(k, H, 0)
+    plan, out = run_nvfp4(fa, q, k, v, cu, H)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    check_nvfp4_out(out, q, k, v, z, cu, all_rows(cu, H))
+
+
+def test_nvfp4_attention_ragged_varlen(fa):
+    """Empty segments, a 17-token segment, segments ending inside a 64-key sub-tile and inside a
+    128-row query tile; rows of every segment, every head."""
+    cu, H = [0, 0, 17, 300, 300, 1400, 1500], 3
+    q, k, v = inputs.qkv_separate(1500, H, seed=2)
+    k = with_k_offset(k, H, 2)
+    sentinel = torch.full((1500, H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    plan = fa.Plan(cu, H, mode=fa.MODE_NVFP4)
+    plan.attention(q.cuda(), k.cuda(), v.cuda(), torch.tensor(cu, dtype=torch.int32,
+                                                               device="cuda"), out=sentinel)
+    torch.cuda.synchronize()
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    check_nvfp4_out(sentinel, q, k, v, z, cu, all_rows(cu, H))
+
+
+def test_nvfp4_attention_strided_views(fa):
+    buf, q, k, v = inputs.qkv_fused(333, 4, seed=4)
+    cu = [0, 100, 333]
+    plan, out = run_nvfp4(fa, q, k, v, cu, 4)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    check_nvfp4_out(out, q, k, v, z, cu, all_rows(cu, 4))
+
+
+def test_nvfp4_constant_v(fa):
+    """Constant V = 0.75 (= 6 * 2^-3, exact in E2M1 x UE4M3) returns 0.75 in every row: l sums the
+    same dequantized P that multiplies V."""
+    T, H = 700, 2
+    q, k, _ = inputs.qkv_separate(T, H, seed=3)
+    v = torch.full((T, H, 128), 0.75, dtype=torch.bfloat16)
+    plan, out = run_nvfp4(fa, q, k, v, [0, T], H)
+    assert torch.all(out.float() == 0.75)
+
+
+def test_nvfp4_attention_h3_shape(fa):
+    """S=30272, H=56 with the per-(head, channel) K offset N(0, 4): codes bit-exact, and a seeded
+    sample of 4 heads x 48 rows against C3 and exact attention."""
+    S, H = 30272, 56
+    cu = [0, S]
+    q, k, v = inputs.qkv_separate(S, H, seed=0)
+    k = with_k_offset(k, H, 0)
+    plan, out = run_nvfp4(fa, q, k, v, cu, H)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    rows = inputs.sample_rows(cu, H, n_heads=4, n_rows=48, seed=5)
+    e_emu, e_exact = check_nvfp4_out(out, q, k, v, z, cu, rows)
+    assert e_exact < 0.25, e_exact

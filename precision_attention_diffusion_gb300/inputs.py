@@ -23,8 +23,9 @@ WORKLOADS = {
     "fp8_s30272_h56": dict(cu=[0, 30272], heads=56),
     # packed varlen with empty, sub-tile and trailing-padding segments
     "fp8_varlen_32768_h56": dict(cu=[0, 0, 17, 4113, 4113, 31800, 32768], heads=56),
-    # NVFP4 at the H3 shape
+    # NVFP4 at the H3 shape, and a small case of the same kernel (profiling)
     "nvfp4_s30272_h56": dict(cu=[0, 30272], heads=56),
+    "nvfp4_s4096_h56": dict(cu=[0, 4096], heads=56),
 }
 
 

@@ -14,7 +14,9 @@
 //                with c = softmax_scale log2(e)            (log2 units)
 //   m_i        = running row maximum of s'' (exact: it moves whenever a sub-tile exceeds it)
 //   P'(i, j)   = 2^(s'' - m_i + log2 2688)                  (= 2688 exp(S' - m) of the pages)
-//   per 16 keys: sf = UE4M3(amax / 6), code = E2M1(P' / deq(sf))
+//   per 16 keys: sf = UE4M3(max P' / 6), code = E2M1(P' / deq(sf)), both evaluated in the
+//                exponent: max P' / 6 = 2^(max s'' - m + log2 448), P' / deq(sf) =
+//                2^(s'' - m + log2 2688 - log2 deq(sf)) (one exp2 per key, no division)
 //   l_i        = l_i 2^(m_old - m_new) + sum deq(P),   O_i likewise with deq(P) deq(V)
 //   out        = BF16(O / l) for rows inside the segment.
 //
@@ -58,6 +60,7 @@ constexpr uint32_t kSfTile = 128 * 8;     // 128 rows of 8 UE4M3 scales
 constexpr uint32_t kIdescS = idesc_mxf4nvf4(128, kSub);
 constexpr uint32_t kIdescPV = idesc_mxf4nvf4(128, 128);
 constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
+constexpr float kLog2_6 = 2.5849625007211562f;
 
 // tensor-memory columns
 __device__ __forceinline__ uint32_t col_s(int t) { return 224u * uint32_t(t); }
@@ -85,8 +88,10 @@ struct Smem {
   uint64_t bar_sr[2];              // [t]: S_t(u) read by the softmax (128 arrivals)
   uint64_t bar_p[2][2];            // [t][u & 1]: P_t(u) written and O rescaled (128 arrivals)
   uint64_t bar_o[2][2];            // [t][u & 1]: PV_t(u) done (MMA commit)
-  uint64_t bar_c[2];               // [u & 1]: scale factors in TMEM and c(u) in smem (128)
-  uint64_t bar_cfree[2];           // [u & 1]: c(u) read, MMAs of u done (128 nq + nq)
+  uint64_t bar_sf[2];              // [u & 1]: K and V scale factors of u in TMEM (128)
+  uint64_t bar_sffree[2];          // [u & 1]: MMAs of u done, scale buffers free (nq commits)
+  uint64_t bar_c[2];               // [u & 1]: c(u) in smem (128)
+  uint64_t bar_cfree[2];           // [u & 1]: c(u) read by the softmax (128 nq)
   uint64_t bar_drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -196,7 +201,7 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
     mma_mxf4_ts_elect(tmem + col_o(t), tmem + col_p(t, int(h)), vb, kIdescPV,
                       tmem + col_psf(t, int(h)), tmem + col_vsf(int(h)), u > 0 ? 1u : 0u);
     mma_commit_elect(smem_u32(&S.bar_o[t][h]));
-    mma_commit_elect(smem_u32(&S.bar_cfree[h]));
+    mma_commit_elect(smem_u32(&S.bar_sffree[h]));
     if (h == 1 || u + 1 == n_sub) mma_commit_elect(smem_u32(&S.bar_free[j % kStages]));
   };
   do {
@@ -209,7 +214,7 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
         if ((u & 1) == 0 &&
             !(ok = wait_all(&S.bar_k[j % kStages], (j / kStages) & 1, S, a, kRoleMma)))
           break;
-        if (!(ok = wait_all(&S.bar_c[u & 1], (u >> 1) & 1, S, a, kRoleMma))) break;
+        if (!(ok = wait_all(&S.bar_sf[u & 1], (u >> 1) & 1, S, a, kRoleMma))) break;
         tc_fence_after();
         issue_s(u);
       }
@@ -267,7 +272,7 @@ __device__ __forceinline__ void correction(Smem& S, const Nvfp4Args& a, const Wo
       if (!wait_all(&S.bar_k[st], (j / kStages) & 1, S, a, kRoleCorrection)) break;
       if (!wait_all(&S.bar_v[st], (j / kStages) & 1, S, a, kRoleCorrection)) break;
     }
-    if (u >= 2 && !wait_all(&S.bar_cfree[b], ((u - 2) >> 1) & 1, S, a, kRoleCorrection)) break;
+    if (u >= 2 && !wait_all(&S.bar_sffree[b], ((u - 2) >> 1) & 1, S, a, kRoleCorrection)) break;
     // B-side scale factors, every lane quarter: K rows (keys) 32c + lane in column c of K step kk;
     // V rows (channels) 32c + lane in column c, word h of the channel's 8-byte record.
     {
@@ -279,6 +284,10 @@ __device__ __forceinline__ void correction(Smem& S, const Nvfp4Args& a, const Wo
       tmem_st4(tmem + col_vsf(b) + lane_off, vs[lane * 2 + h], vs[(32 + lane) * 2 + h],
                vs[(64 + lane) * 2 + h], vs[(96 + lane) * 2 + h]);
     }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&S.bar_sf[b]));  // the MMAs of u may start
+    if (u >= 2 && !wait_all(&S.bar_cfree[b], ((u - 2) >> 1) & 1, S, a, kRoleCorrection)) break;
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
       const int key = 16 * cw + 8 * pass + (lane & 7);
@@ -311,8 +320,6 @@ __device__ __forceinline__ void correction(Smem& S, const Nvfp4Args& a, const Wo
       if (cq == 0) S.c[b][0][key] = tot0 * cs;
       else if (cq == 1) S.c[b][1][key] = tot1 * cs;
     }
-    tmem_wait_st();
-    tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_c[b]));
     if (h == 1 || u + 1 == n_sub) {
       __syncwarp();
@@ -373,41 +380,44 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
       for (int i = 0; i < 64; ++i)
         if (i >= last_valid) s[i] = -INFINITY;
     }
-    const float mx = row_max64(s);
+    // group maxima (16 keys) and row maximum of s''
+    float gm[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = s[16 * g + e];
+      gm[g] = max16(v);
+    }
+    const float mx = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
     const bool move = mx > m;  // exact running maximum
     const float m_new = move ? mx : m;
     const float alpha = move ? ex2_approx(m - m_new) : 1.f;  // m = -inf gives 0
-    const float bias = kLog2_2688 - m_new;
+    const float bias = kLog2_2688 - m_new;                  // s'' + bias = log2 P'
     uint32_t pk[8];
     uint32_t sfw = 0u;
     float rs = 0.f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {  // 16 keys per scale group
-      float pp[16];
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        float x0, x1;
-        fma2(x0, x1, s[16 * g + i], s[16 * g + i + 1], 1.f, bias);
-        pp[i] = ex2_approx(x0);  // P' = 2688 2^(s'' - m)
-        pp[i + 1] = ex2_approx(x1);
-      }
-      // second level: UE4M3 scale of the group, E2M1 codes of P' / deq(scale)
-      const uint32_t sf = cvt_e4m3x2(__fdiv_rn(max16(pp), 6.f), 0.f) & 0xFFu;
+      // second level: UE4M3 scale of the group = E4M3(max P' / 6), max P' / 6 = 2^(gm + bias) / 6;
+      // codes E2M1(P' / deq(scale)) = E2M1(2^(s'' + bias - log2 deq(scale))); scale 0 -> codes 0
+      const uint32_t sf = cvt_e4m3x2(ex2_approx(gm[g] + (bias - kLog2_6)), 0.f) & 0xFFu;
       const float ds = e4m3_to_f32(sf);
-      const float rds = sf ? __frcp_rn(ds) : 0.f;
-      uint32_t w0 = 0u, w1 = 0u, hs = 0u;
+      const float gb = sf ? bias - lg2_approx(ds) : -INFINITY;
+      uint32_t b[8], hs = 0u;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        float y0, y1;
-        fma2(y0, y1, pp[2 * i], pp[2 * i + 1], rds, 0.f);
-        const uint32_t byte = cvt_e2m1x2(y0, y1);
-        if (i < 4) w0 |= byte << (8 * i);
-        else w1 |= byte << (8 * (i - 4));
-        // the quantized values, back in f16 (exact; a group sums to at most 96 in steps of 0.5)
-        hs = hadd2_u32(hs, cvt_e2m1x2_to_f16x2(byte));
+        float x0, x1;
+        fma2(x0, x1, s[16 * g + 2 * i], s[16 * g + 2 * i + 1], 1.f, gb);
+        uint32_t h2;
+        b[i] = cvt_e2m1x2_and_f16x2(ex2_approx(x0), ex2_approx(x1), h2);
+        // the quantized values in f16 (exact; a group sums to at most 96 in steps of 0.5)
+        hs = hadd2_u32(hs, h2);
       }
-      pk[2 * g] = w0;
-      pk[2 * g + 1] = w1;
+      pk[2 * g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040),
+                              0x5410);
+      pk[2 * g + 1] = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
+                                  __byte_perm(b[6], b[7], 0x0040), 0x5410);
       const float2 hf = f16x2_to_f32x2(hs);
       rs = fmaf(hf.x + hf.y, ds, rs);  // l sums the dequantized P (reading r6)
       sfw |= sf << (8 * g);
@@ -430,7 +440,12 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
         tmem_ld32(o_addr + 32 * i, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        for (int e = 0; e < 32; e += 2) {
+          float a0, a1;
+          fma2(a0, a1, __uint_as_float(o[e]), __uint_as_float(o[e + 1]), alpha, 0.f);
+          o[e] = __float_as_uint(a0);
+          o[e + 1] = __float_as_uint(a1);
+        }
         tmem_st32(o_addr + 32 * i, o);
       }
     }
@@ -501,8 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&S.bar_drain[t]), 1);
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&S.bar_sf[b]), 128);
+      mbar_init(smem_u32(&S.bar_sffree[b]), wi.nq);
       mbar_init(smem_u32(&S.bar_c[b]), 128);
-      mbar_init(smem_u32(&S.bar_cfree[b]), 128 * wi.nq + wi.nq);
+      mbar_init(smem_u32(&S.bar_cfree[b]), 128 * wi.nq);
     }
     S.abort_flag = 0;
     fence_mbar_init();

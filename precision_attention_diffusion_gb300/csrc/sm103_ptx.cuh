@@ -410,6 +410,25 @@ __device__ __forceinline__ uint8_t cvt_e2m1x2(float lo, float hi) {
   return static_cast<uint8_t>(r);
 }
 
+// Two fp32 -> two E2M1 codes (round to nearest even, saturate to +-6): the code byte (`lo` in the
+// low nibble) and the two quantized values back in f16x2 (exact).
+__device__ __forceinline__ uint32_t cvt_e2m1x2_and_f16x2(float lo, float hi, uint32_t& h2) {
+  uint32_t b;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, t;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(b), "=r"(h2)
+      : "f"(hi), "f"(lo));
+  return b;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Three-input maximum (sm_100+).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;

@@ -53,17 +53,32 @@ __device__ __forceinline__ uint32_t group16(const float (&x)[4], uint8_t* sf_out
 }
 
 // Pass 1: per (128-row block, head) column sums in FP64, rows in order. For Q (z = 0) the block
-// is one mean's whole extent: write the block mean. For K (z = 1) store the chunk sum.
-__global__ void __launch_bounds__(128) nvfp4_block_sums_kernel(
+// is one mean's whole extent: write the block mean. For K (z = 1) store the chunk sum. The block's
+// rows are staged in shared memory with 16-byte loads (the global reads are coalesced and in
+// flight together); then thread c adds column c's rows in order.
+__global__ void __launch_bounds__(256) nvfp4_block_sums_kernel(
     const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
     int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t nblk,
     float* __restrict__ qmean, double* __restrict__ kchunk) {
-  const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z, c = threadIdx.x;
+  __shared__ __align__(16) uint16_t tile[kTile][kD + 8];  // +8: rows start on distinct banks
+  const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const BlockInfo bi = blocks[b];
   const uint16_t* x = z == 0 ? q : k;
   const int64_t st = z == 0 ? qst : kst, sh = z == 0 ? qsh : ksh;
+  // 128 rows x 16 chunks of 8 BF16
+  for (int i = threadIdx.x; i < kTile * 16; i += 256) {
+    const int r = i >> 4, c8 = (i & 15) * 8;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (r < bi.nvalid)
+      w = __ldg(reinterpret_cast<const uint4*>(x + int64_t(bi.tok0 + r) * st + int64_t(h) * sh +
+                                               c8));
+    *reinterpret_cast<uint4*>(&tile[r][c8]) = w;
+  }
+  __syncthreads();
+  const int c = threadIdx.x;
+  if (c >= kD) return;
   double sum = 0.0;
-  for (int r = 0; r < bi.nvalid; ++r) sum += double(bf16_at(x, bi.tok0 + r, h, c, st, sh));
+  for (int r = 0; r < bi.nvalid; ++r) sum += double(__uint_as_float(uint32_t(tile[r][c]) << 16));
   if (z == 0)
     qmean[(int64_t(h) * nblk + b) * kD + c] = __double2float_rn(sum / double(bi.nvalid));
   else
@@ -167,7 +182,7 @@ int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64
   float* qmean = reinterpret_cast<float*>(ws + p.ws.q_mean);
   float* kmean = reinterpret_cast<float*>(ws + p.ws.k_mean);
   double* kchunk = reinterpret_cast<double*>(ws + p.ws.k_chunk);
-  nvfp4_block_sums_kernel<<<dim3(unsigned(nblk), unsigned(H), 2), 128, 0, stream>>>(
+  nvfp4_block_sums_kernel<<<dim3(unsigned(nblk), unsigned(H), 2), 256, 0, stream>>>(
       qb, qst, qsh, kb, kst, ksh, p.d_blocks, H, nblk, qmean, kchunk);
   nvfp4_kmean_kernel<<<dim3(unsigned(p.nseg), unsigned(H)), 128, 0, stream>>>(p.d_segs, H,
                                                                              kchunk, kmean);

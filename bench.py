@@ -47,9 +47,15 @@ FP4_OVER_BF16 = 6.0
 # Q/K, pack V^T, attention
 KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5}
 
-# DRAM traffic of the attention kernel per launch, from an ncu capture, keyed by the SHA-256 of
-# attn_fp8.cu at capture time (null when the kernel changed since the counters were taken).
-NCU_TRAFFIC = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes) of one attention launch from
+# an ncu capture of the full-size workload (profiles/attn_traffic_s30272_h56.md), keyed by the
+# workload and the SHA-256 of the kernel source at capture time (null once the kernel changed).
+NCU_TRAFFIC = {
+    ("fp8_s30272_h56", "fba5a605fc1a59db655064b8167a3e1ed78b5d2dc713322bb339e89570419bf1"):
+        2.10e9 + 425.25e6,
+    ("nvfp4_s30272_h56", "0525d6d7756763fc300a6d1d0b24d9d5a7b2fe520b4dd6e839a290400fb0a20b"):
+        432.69e6 + 397.73e6,
+}
 
 
 def parse_args():
@@ -388,13 +394,17 @@ def run_ours(args):
     sha = file_sha(os.path.join(ROOT, "precision_attention_diffusion_gb300", "csrc", kname + ".cu"))
     traffic = NCU_TRAFFIC.get((args.workload, sha))
     pkey = "fp4" if mode == "nvfp4" else "fp8"
+    # DRAM bytes the attention launch must move: the quantized operands once, the BF16 output once
+    Tp = sum(-(-(b - a) // 128) * 128 for a, b in zip(cu[:-1], cu[1:]))
+    codes_bytes = (3 * Tp * H * (D // 2 + D // 16) if mode == "nvfp4" else 3 * Tp * H * D)
     ratio = FP4_OVER_BF16 if mode == "nvfp4" else FP8_OVER_BF16
     roof = {"bound": "tensor", "achieved": achieved, "peak": pk[pkey], "unit": "TFLOP/s",
             "frac": achieved / pk[pkey], "traffic": traffic,
             "kernel": kname + "_kernel", "launch_ms": fwd_ms,
             "peak_note": (f"dense {pkey.upper()} = {ratio:g} x {pk['source']} BF16 cuBLAS burst; "
                           f"frac of sustained = {achieved / pk[pkey + '_sustained']:.3f}"),
-            "algorithmic_flops_per_launch": flops}
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": codes_bytes + T * H * D * 2}
     if mode == "nvfp4":
         # quantize passes: Q, K read twice (means, pack), V once; codes + scales written
         q_bytes = 5 * T * H * D * 2 + 3 * T * H * (D // 2 + D // 16)

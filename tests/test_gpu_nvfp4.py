@@ -192,3 +192,26 @@ def test_nvfp4_attention_h3_shape(fa):
     rows = inputs.sample_rows(cu, H, n_heads=4, n_rows=48, seed=5)
     e_emu, e_exact = check_nvfp4_out(out, q, k, v, z, cu, rows)
     assert e_exact < 0.25, e_exact
+
+
+def test_nvfp4_device_wait_limit_returns_error_not_hang(fa):
+    """The NVFP4 kernel's bounded waits: with a limit of one probe the first wait that is not
+    already complete expires, the kernel records an error (0x100 | role) and returns, and the
+    context stays usable for a correct run afterwards."""
+    cu, H = [0, 640], 2
+    q, k, v = inputs.qkv_separate(640, H, seed=8)
+    plan = fa.Plan(cu, H, mode=fa.MODE_NVFP4)
+    plan.last_error()  # clear
+    plan.set_wait_limit(1)
+    out = torch.zeros(640, H, 128, dtype=torch.bfloat16, device="cuda")
+    cu_dev = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    plan.attention(q.cuda(), k.cuda(), v.cuda(), cu_dev, out=out)
+    torch.cuda.synchronize()
+    status = plan.last_error()
+    assert status != 0 and (status & 0xFF00) == 0x100
+    plan.set_wait_limit(20000)
+    plan.attention(q.cuda(), k.cuda(), v.cuda(), cu_dev, out=out)
+    torch.cuda.synchronize()
+    assert plan.last_error() == 0
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    check_nvfp4_out(out, q, k, v, z, cu, all_rows(cu, H))

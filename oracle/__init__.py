@@ -61,17 +61,18 @@ def lib() -> ctypes.CDLL:
             L.orc_e2m1_encode_array.argtypes = [P, i64, P]
             L.orc_fp8_quantize.argtypes = [P, i64, i32, i64, i64, P, P, i32]
             L.orc_attn_exact.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32, P, i32,
-                                         f64, P, i64, P, i32]
+                                         f64, P, i64, P, P, i32]
             L.orc_attn_fp8.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, i32, i32, f64, P,
-                                       i64, P, P, i32]
+                                       i64, P, P, P, i32]
             L.orc_nvfp4_kmean.argtypes = [P, i64, i64, i64, i32, P, i32, P, i32]
             L.orc_nvfp4_qblock_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_qblock_offsets.restype = i64
             L.orc_nvfp4_vgroup_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_vgroup_offsets.restype = i64
             L.orc_nvfp4_quantize_q.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, P, i32]
             L.orc_nvfp4_quantize_k.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, P, i32]
             L.orc_nvfp4_quantize_v.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, i32]
-            L.orc_attn_nvfp4.argtypes = [P, P, P, P, P, P, P, i64, i32, P, i32, f64, i32, P, i64,
-                                         P, P, i32]
+            L.orc_attn_nvfp4.argtypes = [P, P, P, P, P, P, P, P, i64, i32, P, i32, f64, i32, P,
+                                         i64, P, P, P, i32]
+            L.orc_nvfp4_qkm.argtypes = [P, i64, i64, i64, i32, P, i32, P, P, i32]
             _lib = L
     return _lib
 
@@ -141,34 +142,38 @@ def fp8_quantize(x, nthreads=0):
     return codes, d
 
 
-def attn_exact(q, k, v, cu, rows, scale, nthreads=0):
-    """C1: exact FP64 attention for rows [(token, head)] -> [n,128] float64."""
+def attn_exact(q, k, v, cu, rows, scale, nthreads=0, lse=False):
+    """C1: exact FP64 attention for rows [(token, head)] -> [n,128] float64; with lse=True also
+    the row's log-sum-exp log sum_j exp(q.k_j scale) -> (out, lse [n])."""
     (qa, qst, qsh), (ka, kst, ksh), (va, vst, vsh) = _bf16_view(q), _bf16_view(k), _bf16_view(v)
     cu = np.ascontiguousarray(cu, np.int32)
     rows = np.ascontiguousarray(rows, np.int64).reshape(-1, 2)
     out = np.empty((rows.shape[0], D), np.float64)
+    ls = np.empty(rows.shape[0], np.float64)
     lib().orc_attn_exact(_p(qa), qst, qsh, _p(ka), kst, ksh, _p(va), vst, vsh, q.shape[0],
                          q.shape[1], _p(cu), len(cu) - 1, float(scale), _p(rows), rows.shape[0],
-                         _p(out), _threads(nthreads))
-    return out
+                         _p(out), _p(ls), _threads(nthreads))
+    return (out, ls) if lse else out
 
 
 def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, tau=0.0,
-             nthreads=0):
+             nthreads=0, lse=False):
     """C2: FP8-emulating attention from codes/descales -> (out fp64 [n,128], out bf16 bits).
     n_kv: key-tile width; tau: threshold (log2 units) for moving the reference maximum, 0 = the
-    exact running maximum; p_shift: power-of-two shift applied to P before E4M3 rounding."""
+    exact running maximum; p_shift: power-of-two shift applied to P before E4M3 rounding.
+    lse=True appends the row's m + log(l) (reading r15) -> (o64, o16, lse [n])."""
     cq, ck, cv = (np.ascontiguousarray(a, np.uint8) for a in (cq, ck, cv))
     dq, dk, dv = (np.ascontiguousarray(a, np.float32) for a in (dq, dk, dv))
     cu = np.ascontiguousarray(cu, np.int32)
     rows = np.ascontiguousarray(rows, np.int64).reshape(-1, 2)
     o64 = np.empty((rows.shape[0], D), np.float64)
     o16 = np.empty((rows.shape[0], D), np.uint16)
+    ls = np.empty(rows.shape[0], np.float64)
     lib().orc_attn_fp8(_p(cq), _p(ck), _p(cv), _p(dq), _p(dk), _p(dv), cq.shape[0], cq.shape[1],
                        _p(cu), len(cu) - 1, float(scale), int(n_kv), int(p_shift), float(tau),
                        _p(rows),
-                       rows.shape[0], _p(o64), _p(o16), _threads(nthreads))
-    return o64, o16
+                       rows.shape[0], _p(o64), _p(o16), _p(ls), _threads(nthreads))
+    return (o64, o16, ls) if lse else (o64, o16)
 
 
 # ------------------------------------------------------------------------------------------------
@@ -186,7 +191,8 @@ def nvfp4_offsets(cu):
 
 def nvfp4_quantize(q, k, v, cu, nthreads=0):
     """a6+a7 -> dict with km [nseg,H,128] f32, qm [QB,H,128] f32, q/k/v codes [T,H,128] (one
-    4-bit code per byte), q/k scales [T,H,8] (UE4M3 bytes), v scales [H,128,G] (UE4M3 bytes)."""
+    4-bit code per byte), q/k scales [T,H,8] (UE4M3 bytes), v scales [H,128,G] (UE4M3 bytes),
+    qkm [T,H] f64 = q . km (for the LSE, reading r15)."""
     (qa, qst, qsh), (ka, kst, ksh), (va, vst, vsh) = _bf16_view(q), _bf16_view(k), _bf16_view(v)
     T, H = q.shape[0], q.shape[1]
     cu = np.ascontiguousarray(cu, np.int32)
@@ -206,14 +212,17 @@ def nvfp4_quantize(q, k, v, cu, nthreads=0):
     cv = np.zeros((T, H, D), np.uint8)
     sv = np.zeros((H, D, int(go[-1])), np.uint8)
     L.orc_nvfp4_quantize_v(_p(va), vst, vsh, T, H, _p(cu), ns, _p(cv), _p(sv), nt)
-    return dict(km=km, qm=qm, cq=cq, sq=sq, ck=ck, sk=sk, cv=cv, sv=sv, qoff=qo, goff=go)
+    qkm = np.empty((T, H), np.float64)
+    L.orc_nvfp4_qkm(_p(qa), qst, qsh, T, H, _p(cu), ns, _p(km), _p(qkm), nt)
+    return dict(km=km, qm=qm, cq=cq, sq=sq, ck=ck, sk=sk, cv=cv, sv=sv, qoff=qo, goff=go, qkm=qkm)
 
 
-def attn_nvfp4(qz, cu, rows, scale, n_kv=128, nthreads=0):
+def attn_nvfp4(qz, cu, rows, scale, n_kv=128, nthreads=0, lse=False):
     """C3: NVFP4-emulating attention from nvfp4_quantize()'s dict -> (out fp64, out bf16).
 
     n_kv: width of the online-softmax key tiles (a multiple of 16), counted from each segment
-    start; the running maximum is exact."""
+    start; the running maximum is exact. lse=True appends m + log(l / 2688) + q . km scale with
+    the BF16 q (reading r15: the LSE of the uncentred scores)."""
     if n_kv <= 0 or n_kv % 16:
         raise ValueError("n_kv must be a positive multiple of 16")
     cu = np.ascontiguousarray(cu, np.int32)
@@ -221,7 +230,10 @@ def attn_nvfp4(qz, cu, rows, scale, n_kv=128, nthreads=0):
     T, H = qz["cq"].shape[0], qz["cq"].shape[1]
     o64 = np.empty((rows.shape[0], D), np.float64)
     o16 = np.empty((rows.shape[0], D), np.uint16)
-    lib().orc_attn_nvfp4(_p(qz["cq"]), _p(qz["sq"]), _p(qz["qm"]), _p(qz["ck"]), _p(qz["sk"]),
+    ls = np.empty(rows.shape[0], np.float64)
+    lib().orc_attn_nvfp4(_p(qz["cq"]), _p(qz["sq"]), _p(qz["qm"]), _p(qz["qkm"]), _p(qz["ck"]),
+                         _p(qz["sk"]),
                          _p(qz["cv"]), _p(qz["sv"]), T, H, _p(cu), len(cu) - 1, float(scale),
-                         int(n_kv), _p(rows), rows.shape[0], _p(o64), _p(o16), _threads(nthreads))
-    return o64, o16
+                         int(n_kv), _p(rows), rows.shape[0], _p(o64), _p(o16), _p(ls),
+                         _threads(nthreads))
+    return (o64, o16, ls) if lse else (o64, o16)

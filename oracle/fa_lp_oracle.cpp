@@ -34,6 +34,8 @@
 //  r10 E2M1: round to nearest even on {0,.5,1,1.5,2,3,4,6}, saturate to 6, sign of zero kept.
 //  r11 NVFP4 P first level: P' = fl32(2688 * exp(S' - m_running)).
 //  r12 the qm K^T term uses the dequantized centred K.
+//  r15 LSE of a row = m + log(l) in the natural units of S = q.k scale: the log of the normalizer
+//      of the (quantized) softmax the output divides by (exact attention: log sum exp(s)).
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared -pthread (no fast-math), so that fp32
 // products and quotients are single IEEE round-to-nearest operations on any host.
@@ -260,7 +262,7 @@ void orc_attn_exact(const uint16_t* q, int64_t qst, int64_t qsh,
                     const uint16_t* k, int64_t kst, int64_t ksh,
                     const uint16_t* v, int64_t vst, int64_t vsh,
                     int64_t T, int H, const int32_t* cu, int nseg, double scale,
-                    const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+                    const int64_t* rows, int64_t nrows, double* out, double* lse, int nthreads) {
   (void)T; (void)H;
   parallel_for(nrows, nthreads, [&](int64_t r) {
     const int64_t t = rows[2 * r];
@@ -284,6 +286,7 @@ void orc_attn_exact(const uint16_t* q, int64_t qst, int64_t qsh,
       for (int c = 0; c < kD; ++c) o[c] += p * load_bf16(v, j, h, c, vst, vsh);
     }
     for (int c = 0; c < kD; ++c) out[r * kD + c] = o[c] / l;
+    if (lse) lse[r] = m + std::log(l);  // log sum_j exp(s_j), s = q.k scale
   });
 }
 
@@ -299,7 +302,7 @@ void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
                   const float* dq, const float* dk, const float* dv,
                   int64_t T, int H, const int32_t* cu, int nseg, double scale, int n_kv,
                   int p_shift, double tau, const int64_t* rows, int64_t nrows, double* out64,
-                  uint16_t* out16, int nthreads) {
+                  uint16_t* out16, double* lse, int nthreads) {
   (void)T;
   const double inf = std::numeric_limits<double>::infinity();
   const double pscale = std::ldexp(1.0, p_shift);
@@ -342,6 +345,8 @@ void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
       out64[r * kD + c] = y;
       if (out16) out16[r * kD + c] = f64_to_bf16(y);
     }
+    // r15: the log of the quantized softmax normalizer, in the natural units of S
+    if (lse) lse[r] = m + std::log(l);
   });
 }
 
@@ -426,6 +431,22 @@ void orc_nvfp4_quantize_q(const uint16_t* q, int64_t qst, int64_t qsh, int64_t T
   });
 }
 
+// r15 helper: q . km per (token, head), BF16 q and the fp32 segment mean, summed in FP64 over the
+// channels in order. out: [T][H].
+void orc_nvfp4_qkm(const uint16_t* q, int64_t qst, int64_t qsh, int64_t T, int H,
+                   const int32_t* cu, int nseg, const float* km, double* out, int nthreads) {
+  parallel_for(T * H, nthreads, [&](int64_t idx) {
+    const int64_t t = idx / H;
+    const int h = static_cast<int>(idx % H);
+    const int s = segment_of(cu, nseg, t);
+    double acc = 0.0;
+    for (int c = 0; c < kD; ++c)
+      acc += static_cast<double>(load_bf16(q, t, h, c, qst, qsh)) *
+             static_cast<double>(km[(static_cast<int64_t>(s) * H + h) * kD + c]);
+    out[t * H + h] = acc;
+  });
+}
+
 // a7 for K: centring by the segment mean km (from orc_nvfp4_kmean), then per 16 channels.
 void orc_nvfp4_quantize_k(const uint16_t* k, int64_t kst, int64_t ksh, int64_t T, int H,
                           const int32_t* cu, int nseg, const float* km, uint8_t* codes,
@@ -473,12 +494,12 @@ void orc_nvfp4_quantize_v(const uint16_t* v, int64_t vst, int64_t vsh, int64_t T
 // per 16 keys of the tile a UE4M3 scale and E2M1 codes (r9); l sums deq(P'); O sums deq(P')
 // deq(V); out = O / l.
 // ---------------------------------------------------------------------------------------------
-void orc_attn_nvfp4(const uint8_t* cq, const uint8_t* sfq, const float* qm,
+void orc_attn_nvfp4(const uint8_t* cq, const uint8_t* sfq, const float* qm, const double* qkm,
                     const uint8_t* ck, const uint8_t* sfk,
                     const uint8_t* cv, const uint8_t* sfv,
                     int64_t T, int H, const int32_t* cu, int nseg, double scale, int n_kv,
                     const int64_t* rows, int64_t nrows, double* out64, uint16_t* out16,
-                    int nthreads) {
+                    double* lse, int nthreads) {
   (void)T;
   const double inf = std::numeric_limits<double>::infinity();
   std::vector<int64_t> qoff(nseg + 1), goff(nseg + 1);
@@ -542,6 +563,9 @@ void orc_attn_nvfp4(const uint8_t* cq, const uint8_t* sfq, const float* qm,
       out64[r * kD + c] = y;
       if (out16) out16[r * kD + c] = f64_to_bf16(y);
     }
+    // r15: l sums deq(P') = 2688 exp(S' - m) quantized, so the normalizer is l / 2688; the scores
+    // are those of the centred K, and q . km scale (BF16 q) restores the uncentred ones
+    if (lse) lse[r] = m + std::log(l) - std::log(2688.0) + qkm[t * H + h] * scale;
   });
 }
 

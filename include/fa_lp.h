@@ -160,6 +160,25 @@ FA_LP_API int fa_lp_quantize(fa_lp_plan* plan, const void* q, int64_t q_stride_t
 FA_LP_API int fa_lp_forward_varlen(fa_lp_plan* plan, const int32_t* cu_seqlens_dev, void* out,
                          int64_t out_stride_tok, int64_t out_stride_head, void* stream);
 
+/*
+ * fa_lp_forward_varlen_lse -- fa_lp_forward_varlen that also returns each row's log-sum-exp.
+ * Passage: SGLang PR #40175, review thread (the SM120 kernel returns output and LSE; the plan's
+ * buffers are "FP8, output/LSE"). The pages give no formula; reading taken here: the natural log of
+ * the normalizer the output is divided by, in the units of S = q.k * softmax_scale:
+ *   FP8   : LSE = m_ref + ln(l), l = sum of the quantized P = 2^((S - m_ref) log2 e), i.e.
+ *           log sum_j exp(s_j) up to the E4M3 rounding of P;
+ *   NVFP4 : LSE = m + ln(l / 2688) + (q . km) * softmax_scale, l = sum of deq(P'), q the BF16 query
+ *           and km its segment's K mean, so that the K centring is undone.
+ *   lse             : device pointer, FP32; the row of token t, head h is written to
+ *                     lse[h * lse_stride_head + t] for tokens inside segments only (others are
+ *                     left untouched). Caller-owned. NULL: behaves as fa_lp_forward_varlen.
+ *   lse_stride_head : elements between heads, >= tokens. lse must be 4-byte aligned.
+ * Other arguments, errors and ordering as fa_lp_forward_varlen.
+ */
+FA_LP_API int fa_lp_forward_varlen_lse(fa_lp_plan* plan, const int32_t* cu_seqlens_dev, void* out,
+                                       int64_t out_stride_tok, int64_t out_stride_head, float* lse,
+                                       int64_t lse_stride_head, void* stream);
+
 /* fa_lp_attention -- fa_lp_quantize followed by fa_lp_forward_varlen on the same stream: the
  * one-call form out = attention(q, k, v, cu_seqlens) of the FlashInfer op's signature. */
 FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_tok,
@@ -182,6 +201,7 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
 #define FA_LP_V_SCALES 6    /* NVFP4: u8 [H][Tpad/128][128][8], one per 16 keys per channel      */
 #define FA_LP_Q_MEANS 7     /* NVFP4: f32 [H][Tpad/128][128], block means                        */
 #define FA_LP_K_MEANS 8     /* NVFP4: f32 [num_segments][H][128], segment means                  */
+#define FA_LP_Q_KM 9        /* NVFP4: f32 [H][Tpad], q . km of each query row (LSE term)         */
 
 typedef struct fa_lp_array_desc {
   const void* data;  /* device address                                                     */

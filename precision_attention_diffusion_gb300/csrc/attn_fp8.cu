@@ -78,6 +78,8 @@ struct AttnArgs {
   const float* descale;  // [3][H]
   __nv_bfloat16* out;
   int64_t ost, osh;
+  float* lse;        // optional: FP32 row log-sum-exp at lse[h * lse_sh + token]
+  int64_t lse_sh;
   float scale_log2;
   int H;
   int* err;          // sticky error word of the plan (read and cleared by the host)
@@ -333,6 +335,9 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
   const float f = dv / l;
   const int qrow = (wi.qt0 + t) * kTile + wq * 32 + lane;
   const bool valid = qrow < sg.len;
+  // LSE in the units of S = q.k scale: m c (log2 units) + log2(l), times ln 2
+  if (a.lse && valid)
+    a.lse[int64_t(h) * a.lse_sh + sg.tok0 + qrow] = (m * c + log2f(l)) * 0.6931471805599453f;
   __nv_bfloat16* dst = a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(h) * a.osh;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
-                         cudaStream_t stream) {
+                         float* lse, int64_t lse_sh, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -444,6 +449,8 @@ int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t os
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ost = ost;
   a.osh = osh;
+  a.lse = lse;
+  a.lse_sh = lse_sh;
   a.scale_log2 = p.scale * 1.4426950408889634f;
   a.H = p.heads;
   a.err = p.d_err;

@@ -105,8 +105,12 @@ struct Nvfp4Args {
   const uint8_t* k_sf;     // [H][Tp][8]
   const uint8_t* v_sf;     // [H][Tp/128][128][8]
   const float* q_mean;     // [H][Tp/128][128]
+  const float* q_km;       // [H][Tp]: q . km per query row
   __nv_bfloat16* out;
   int64_t ost, osh;
+  float* lse;              // optional: FP32 row log-sum-exp at lse[h * lse_sh + token]
+  int64_t lse_sh;
+  float scale;
   int64_t tpad;
   float scale_log2;
   WaitCtx w;
@@ -465,6 +469,11 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
   const float f = __frcp_rn(l);
   const int qrow = (wi.qt0 + t) * kTile + wq * 32 + lane;
   const bool valid = qrow < sg.len;
+  // LSE of the uncentred scores: (m + log2(l) - log2 2688) ln 2 + (q . km) scale
+  if (a.lse && valid)
+    a.lse[int64_t(wi.head) * a.lse_sh + sg.tok0 + qrow] =
+        (m + log2f(l) - kLog2_2688) * 0.6931471805599453f +
+        a.q_km[int64_t(wi.head) * a.tpad + sg.row0 + qrow] * a.scale;
   __nv_bfloat16* dst = a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(wi.head) * a.osh;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -560,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
-                           cudaStream_t stream) {
+                           float* lse, int64_t lse_sh, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -587,6 +596,10 @@ int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t 
   a.k_sf = ws + p.ws.k_sf;
   a.v_sf = ws + p.ws.v_sf;
   a.q_mean = reinterpret_cast<const float*>(ws + p.ws.q_mean);
+  a.q_km = reinterpret_cast<const float*>(ws + p.ws.q_km);
+  a.lse = lse;
+  a.lse_sh = lse_sh;
+  a.scale = p.scale;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ost = ost;
   a.osh = osh;

@@ -188,6 +188,7 @@ void build_plan(fa_lp_plan* p) {
     w.q_mean = take(H * (Tp / 128) * 128 * 4);
     w.k_mean = take(size_t(p->nseg) * H * 128 * 4);
     w.k_chunk = take(p->blocks.size() * H * 128 * 8);
+    w.q_km = take(H * Tp * 4);
   }
   w.total = off;
 }
@@ -386,12 +387,16 @@ int fa_lp_quantize(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const
   return FA_LP_OK;
 }
 
-int fa_lp_forward_varlen(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out, int64_t ost,
-                         int64_t osh, void* stream_) {
+int fa_lp_forward_varlen_lse(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out,
+                             int64_t ost, int64_t osh, float* lse, int64_t lse_stride_head,
+                             void* stream_) {
   (void)cu_seqlens_dev;
   if (!p) return FA_LP_ERR_INVALID_ARG;
   if (!p->quantized) return FA_LP_ERR_STATE;
   if (p->tokens > 0 && bad_view(out, ost, osh)) return FA_LP_ERR_INVALID_ARG;
+  if (lse && p->tokens > 0 &&
+      (lse_stride_head < p->tokens || reinterpret_cast<uintptr_t>(lse) % 4 != 0))
+    return FA_LP_ERR_INVALID_ARG;
   int st = check_current_device(p);
   if (st != FA_LP_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -404,9 +409,15 @@ int fa_lp_forward_varlen(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out
   }
   if (p->work.empty()) return FA_LP_OK;
   return (p->mode == FA_LP_MODE_FP8)
-             ? falp::launch_fp8_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, stream)
-             : falp::launch_nvfp4_attention(*p, static_cast<uint8_t*>(base), out, ost, osh,
-                                            stream);
+             ? falp::launch_fp8_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, lse,
+                                          lse_stride_head, stream)
+             : falp::launch_nvfp4_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, lse,
+                                            lse_stride_head, stream);
+}
+
+int fa_lp_forward_varlen(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out, int64_t ost,
+                         int64_t osh, void* stream_) {
+  return fa_lp_forward_varlen_lse(p, cu_seqlens_dev, out, ost, osh, nullptr, 0, stream_);
 }
 
 int fa_lp_attention(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
@@ -458,6 +469,7 @@ int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
     case FA_LP_V_SCALES: return set(p->ws.v_sf, H, Tp / 128, 1024, 1);
     case FA_LP_Q_MEANS: return set(p->ws.q_mean, H, Tp / 128, 128, 4);
     case FA_LP_K_MEANS: return set(p->ws.k_mean, p->nseg, H, 128, 4);
+    case FA_LP_Q_KM: return set(p->ws.q_km, 1, H, Tp, 4);
     default: return FA_LP_ERR_INVALID_ARG;
   }
 }

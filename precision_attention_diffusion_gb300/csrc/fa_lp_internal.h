@@ -45,6 +45,7 @@ struct WsLayout {
   size_t q_sf = 0, k_sf = 0, v_sf = 0;           // NVFP4 scale bytes
   size_t q_mean = 0, k_mean = 0;                 // NVFP4 means (f32)
   size_t k_chunk = 0;                            // NVFP4 scratch: f64 [nblk][H][128] chunk sums
+  size_t q_km = 0;                               // NVFP4: f32 [H][Tp] q . km (row LSE term)
   size_t amax = 0, descale = 0;                  // FP8: u32 [3][H], f32 [3][H]
   size_t total = 0;
 };
@@ -93,12 +94,12 @@ int launch_fp8_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t
                         int64_t qsh, const void* k, int64_t kst, int64_t ksh, const void* v,
                         int64_t vst, int64_t vsh, cudaStream_t stream);
 int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
-                         cudaStream_t stream);
+                         float* lse, int64_t lse_sh, cudaStream_t stream);
 int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t qst,
                           int64_t qsh, const void* k, int64_t kst, int64_t ksh, const void* v,
                           int64_t vst, int64_t vsh, cudaStream_t stream);
 int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
-                           cudaStream_t stream);
+                           float* lse, int64_t lse_sh, cudaStream_t stream);
 int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
 
 // Distinct positive id per kernel launch (device-side abort words compare against it).

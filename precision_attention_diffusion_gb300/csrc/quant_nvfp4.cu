@@ -17,6 +17,7 @@
 //   V scales   : u8 [H][Tpad/128][128][8] one per 16 keys (groups start at the segment start);
 //                each 128-key tile's scales are one contiguous 1 KB record
 //   Q means    : f32 [H][Tpad/128][128]; K means: f32 [num_segments][H][128]
+//   q . km     : f32 [H][Tpad], the BF16 query row times its segment's K mean (for the row LSE)
 // Padding rows / keys hold code 0 and scale 0.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(256) nvfp4_pack_qk_kernel(
     int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t Tp,
     int64_t nblk, const float* __restrict__ qmean, const float* __restrict__ kmean,
     uint8_t* __restrict__ qc, uint8_t* __restrict__ kc, uint8_t* __restrict__ qs,
-    uint8_t* __restrict__ ks) {
+    uint8_t* __restrict__ ks, float* __restrict__ qkm) {
   const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BlockInfo bi = blocks[b];
@@ -119,15 +120,25 @@ __global__ void __launch_bounds__(256) nvfp4_pack_qk_kernel(
   uint8_t* codes = (z == 0 ? qc : kc) + (int64_t(h) * Tp + int64_t(b) * kTile) * 64;
   uint8_t* scales = (z == 0 ? qs : ks) + (int64_t(h) * Tp + int64_t(b) * kTile) * 8;
   const int c0 = lane * 4;
-  float mu[4];
+  float mu[4], kmu[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) mu[e] = mean[c0 + e];
+  for (int e = 0; e < 4; ++e) {
+    mu[e] = mean[c0 + e];
+    kmu[e] = kmean[(int64_t(bi.seg) * H + h) * kD + c0 + e];  // for q . km (Q only)
+  }
   for (int r = warp; r < kTile; r += 8) {
     uint32_t packed = 0u;
     uint8_t sf = 0;
+    float qk = 0.f;
     if (r < bi.nvalid) {
       const uint2 w = *reinterpret_cast<const uint2*>(x + int64_t(bi.tok0 + r) * st +
                                                       int64_t(h) * sh + c0);
+      if (z == 0) {
+        qk = __uint_as_float(w.x << 16) * kmu[0];
+        qk = fmaf(__uint_as_float(w.x & 0xFFFF0000u), kmu[1], qk);
+        qk = fmaf(__uint_as_float(w.y << 16), kmu[2], qk);
+        qk = fmaf(__uint_as_float(w.y & 0xFFFF0000u), kmu[3], qk);
+      }
       float xc[4];
       xc[0] = __fsub_rn(__uint_as_float(w.x << 16), mu[0]);
       xc[1] = __fsub_rn(__uint_as_float(w.x & 0xFFFF0000u), mu[1]);
@@ -137,6 +148,11 @@ __global__ void __launch_bounds__(256) nvfp4_pack_qk_kernel(
     }
     reinterpret_cast<uint16_t*>(codes + int64_t(r) * 64)[lane] = uint16_t(packed);
     if ((lane & 3) == 0) scales[int64_t(r) * 8 + (lane >> 2)] = sf;
+    if (z == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, o);
+      if (lane == 0) qkm[int64_t(h) * Tp + int64_t(b) * kTile + r] = qk;
+    }
   }
 }
 
@@ -188,7 +204,7 @@ int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64
                                                                              kchunk, kmean);
   nvfp4_pack_qk_kernel<<<dim3(unsigned(nblk), unsigned(H), 2), 256, 0, stream>>>(
       qb, qst, qsh, kb, kst, ksh, p.d_blocks, H, p.tpad, nblk, qmean, kmean, ws + p.ws.q_codes,
-      ws + p.ws.k_codes, ws + p.ws.q_sf, ws + p.ws.k_sf);
+      ws + p.ws.k_codes, ws + p.ws.q_sf, ws + p.ws.k_sf, reinterpret_cast<float*>(ws + p.ws.q_km));
   nvfp4_pack_vt_kernel<<<dim3(unsigned(nblk), unsigned(H)), 256, 0, stream>>>(
       vb, vst, vsh, p.d_blocks, H, p.tpad, ws + p.ws.v_codes, ws + p.ws.v_sf);
   return cuda_status(cudaGetLastError());

@@ -26,7 +26,7 @@ FA_LP_ERR_STATE = 6
 MODE_FP8 = 0
 MODE_NVFP4 = 1
 
-Q_CODES, K_CODES, V_CODES, DESCALE, Q_SCALES, K_SCALES, V_SCALES, Q_MEANS, K_MEANS = range(9)
+Q_CODES, K_CODES, V_CODES, DESCALE, Q_SCALES, K_SCALES, V_SCALES, Q_MEANS, K_MEANS, Q_KM = range(10)
 
 # Every symbol include/fa_lp.h declares.
 EXPORTS = (
@@ -34,7 +34,7 @@ EXPORTS = (
     "fa_lp_workspace_bytes", "fa_lp_quantize", "fa_lp_forward_varlen", "fa_lp_attention",
     "fa_lp_plan_row_offsets", "fa_lp_get_quantized", "fa_lp_copy_quantized",
     "fa_lp_get_last_error", "fa_lp_plan_set_wait_limit", "fa_lp_release_workspace",
-    "fa_lp_encode", "fa_lp_fp8_descale_noalloc",
+    "fa_lp_encode", "fa_lp_fp8_descale_noalloc", "fa_lp_forward_varlen_lse",
 )
 
 _lib = None
@@ -81,6 +81,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.fa_lp_workspace_bytes.argtypes = [P, ctypes.POINTER(sz)]
         L.fa_lp_quantize.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P]
         L.fa_lp_forward_varlen.argtypes = [P, P, P, i64, i64, P]
+        L.fa_lp_forward_varlen_lse.argtypes = [P, P, P, i64, i64, P, i64, P]
         L.fa_lp_attention.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, P, i64, i64, P]
         L.fa_lp_plan_row_offsets.argtypes = [P, ctypes.POINTER(i64)]
         L.fa_lp_get_quantized.argtypes = [P, i32, ctypes.POINTER(_ArrayDesc)]
@@ -191,11 +192,23 @@ class Plan:
         _check(load().fa_lp_quantize(self._h, qa, qs, qh, ka, ks, kh, va, vs, vh, _stream(stream)),
                "fa_lp_quantize")
 
-    def forward(self, out, cu_seqlens_dev=None, stream=None):
+    def forward(self, out, cu_seqlens_dev=None, stream=None, lse=None):
+        """Attention over the last quantize; `lse` (optional, float32 [heads, >= tokens] on the
+        device) receives each row's log-sum-exp."""
         oa, os_, oh = _view(out, "out")
         cu = ctypes.c_void_p(cu_seqlens_dev.data_ptr()) if cu_seqlens_dev is not None else None
-        _check(load().fa_lp_forward_varlen(self._h, cu, oa, os_, oh, _stream(stream)),
-               "fa_lp_forward_varlen")
+        if lse is None:
+            _check(load().fa_lp_forward_varlen(self._h, cu, oa, os_, oh, _stream(stream)),
+                   "fa_lp_forward_varlen")
+            return out
+        if (lse.dtype != torch.float32 or lse.dim() != 2 or lse.stride(1) != 1 or not lse.is_cuda
+                or lse.shape[0] != self.heads or lse.shape[1] < self.tokens):
+            raise ValueError("lse must be a CUDA float32 [heads, >= tokens] tensor with unit "
+                             "token stride")
+        _check(load().fa_lp_forward_varlen_lse(self._h, cu, oa, os_, oh,
+                                               ctypes.c_void_p(lse.data_ptr()),
+                                               int(lse.stride(0)), _stream(stream)),
+               "fa_lp_forward_varlen_lse")
         return out
 
     def attention(self, q, k, v, cu_seqlens_dev=None, out=None, stream=None):

@@ -246,3 +246,31 @@ def test_fp8_packed_varlen_32768(fa):
     check_outputs(out, q, k, v, nat, ds, cu, full)
     rows = inputs.sample_rows(cu, H, n_heads=4, n_rows=256, seed=1)
     check_outputs(out, q, k, v, nat, ds, cu, rows)
+
+
+def test_fp8_lse_ragged_varlen(fa):
+    """Row log-sum-exp (fa_lp_forward_varlen_lse, reading r15) on empty, short and long segments:
+    within 1e-3 of the FP8-emulating oracle's m + log(l), within the E4M3 bound of exact
+    attention's LSE; columns past the last token untouched."""
+    cu, H = [0, 0, 17, 300, 300, 1400, 1500], 3
+    T = cu[-1]
+    q, k, v = inputs.qkv_separate(T, H, seed=12)
+    plan = fa.Plan(cu, H)
+    plan.quantize(q.cuda(), k.cuda(), v.cuda())
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    lse_buf = torch.full((H, T + 5), 7.0, dtype=torch.float32, device="cuda")
+    plan.forward(out, torch.tensor(cu, dtype=torch.int32, device="cuda"), lse=lse_buf)
+    torch.cuda.synchronize()
+    got = lse_buf.cpu().numpy()
+    assert np.all(got[:, T:] == 7.0)
+    rows = all_rows(cu, H)
+    nat, ds = check_codes(fa, plan, cu, q, k, v)
+    _, _, emu = oracle.attn_fp8(nat["q"], nat["k"], nat["v"], ds[0], ds[1], ds[2], cu, rows,
+                                SCALE, n_kv=KV_TILE, tau=TAU, lse=True)
+    _, exact = oracle.attn_exact(bits(q), bits(k), bits(v), cu, rows, SCALE, lse=True)
+    g = np.array([got[h, t] for t, h in rows], np.float64)
+    assert np.abs(g - emu).max() < 1e-3, np.abs(g - emu).max()
+    # against exact attention: E4M3 rounding moves each P by at most 2^-4 (so log l by at most
+    # ln(1 + 2^-4) = 0.061) plus the score quantization; short segments do not average it out
+    d = np.abs(g - exact)
+    assert d.max() < 0.1 and d.mean() < 0.02, (d.max(), d.mean())

@@ -215,3 +215,36 @@ def test_nvfp4_device_wait_limit_returns_error_not_hang(fa):
     assert plan.last_error() == 0
     z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
     check_nvfp4_out(out, q, k, v, z, cu, all_rows(cu, H))
+
+
+def test_nvfp4_lse_ragged_varlen(fa):
+    """NVFP4 row log-sum-exp (reading r15: the K centring undone with the BF16 q . km): within
+    1e-3 of the NVFP4-emulating oracle and within the E2M1 bound of exact attention's LSE on
+    offset keys."""
+    cu, H = [0, 0, 17, 300, 300, 1400, 1500], 3
+    T = cu[-1]
+    q, k, v = inputs.qkv_separate(T, H, seed=13)
+    k = with_k_offset(k, H, 13)
+    plan = fa.Plan(cu, H, mode=fa.MODE_NVFP4)
+    plan.quantize(q.cuda(), k.cuda(), v.cuda())
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    lse_buf = torch.full((H, T + 5), 7.0, dtype=torch.float32, device="cuda")
+    plan.forward(out, torch.tensor(cu, dtype=torch.int32, device="cuda"), lse=lse_buf)
+    torch.cuda.synchronize()
+    got = lse_buf.cpu().numpy()
+    assert np.all(got[:, T:] == 7.0)
+    rows = all_rows(cu, H)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    # q . km as the kernel stored it, against the oracle's FP64 value
+    offs = plan.row_offsets()
+    prow, _ = padded_rows(cu, offs)
+    qkm = plan.quantized(fa.Q_KM).cpu().numpy()[0]            # [H][Tp]
+    assert np.allclose(qkm[:, prow].T, z["qkm"], rtol=1e-5, atol=1e-4)
+    _, _, emu = oracle.attn_nvfp4(z, cu, rows, SCALE, n_kv=KV_TILE, lse=True)
+    _, exact = oracle.attn_exact(bits(q), bits(k), bits(v), cu, rows, SCALE, lse=True)
+    g = np.array([got[h, t] for t, h in rows], np.float64)
+    assert np.abs(g - emu).max() < 1e-3, np.abs(g - emu).max()
+    # against exact attention: an E2M1 code of P' is off by at most 1/5 of its value (between 4
+    # and 6), so log l moves by at most ln(1.25) = 0.22 plus the score quantization
+    d = np.abs(g - exact)
+    assert d.max() < 0.25 and d.mean() < 0.04, (d.max(), d.mean())

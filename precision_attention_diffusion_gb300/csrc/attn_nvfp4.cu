@@ -10,7 +10,8 @@
 //
 // What one CTA computes (readings r5 with tau = 0, r9, r11, r12): for the two 128-row query tiles
 // Q0, Q1 of one (segment, head), over 64-key sub-tiles u from the segment start,
-//   s''(i, j)  = (deq(Qc_i) . deq(Kc_j)) c + c_t(j),  c_t(j) = (qm_t . deq(Kc_j)) c,
+//   s''(i, j)  = (deq(Qc_i) . deq(Kc_j)) c + Tq_t(j),  Tq_t(j) = (qm_t . deq(Kc_j)) c (the
+//                table qmk_nvfp4.cu writes during quantization),
 //                with c = softmax_scale log2(e)            (log2 units)
 //   m_i        = running row maximum of s'' (exact: it moves whenever a sub-tile exceeds it)
 //   P'(i, j)   = 2^(s'' - m_i + log2 2688)                  (= 2688 exp(S' - m) of the pages)
@@ -21,16 +22,16 @@
 //   out        = BF16(O / l) for rows inside the segment.
 //
 // Roles (480 threads):
-//   warp 8      TMA: Q codes (64-byte rows, 64-byte swizzle) and, by plain bulk copies, Q scale
-//               records and Q block means once; then per 128-key tile K codes + K scale record
-//               and V^T codes + V scale record into a 4-stage ring;
+//   warp 8      TMA: Q codes (64-byte rows, 64-byte swizzle) and, by plain bulk copies, the Q
+//               scale records once; then per 128-key tile K codes + K scale record + the query
+//               tiles' 128-entry rows of the qm K^T table, and V^T codes + V scale record, into
+//               a 4-stage ring;
 //   warps 9/10  MMA issue for query tile 0/1 (tensor memory allocated by warp 9):
 //                 S_t(u)  = deq(Qc_t) deq(Kc(u))^T   2 MMAs M=128 N=64  K=64, A, B in smem
 //                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=128 K=64, A = P in TMEM
 //   warps 11-14 per sub-tile: K and V scale factors into tensor memory (the MMA reads the B-side
 //               scales of row n from column n / 32 of every lane quarter, so each of the four
-//               warps writes its own quarter), and c_t(j) for both query tiles into shared memory
-//               (FP32 products and sums);
+//               warps writes its own quarter);
 //   warps 0-7   softmax of tile 0 (warps 0-3) and 1 (warps 4-7), one thread per query row (row ==
 //               tensor-memory lane); P codes and P scales go to tensor memory (A-side scales: row
 //               r in lane r, column r / 32), O is rescaled in tensor memory when a row's maximum
@@ -78,20 +79,17 @@ struct Smem {
   uint8_t qsf[2][kSfTile];
   uint8_t ksf[kStages][kSfTile];   // [key][8]
   uint8_t vsf[kStages][kSfTile];   // [channel][8]
-  float qm[2][kD];
-  float c[2][2][kSub];             // [u & 1][t][key]: c_t(j) in log2 units
+  float cq[kStages][2][kTile];     // [stage][t][key]: the qm K^T table row of query tile t
   uint64_t bar_q;
   uint64_t bar_k[kStages];
   uint64_t bar_v[kStages];
-  uint64_t bar_free[kStages];      // MMA commits of both tiles + the four correction warps
+  uint64_t bar_free[kStages];      // MMA commits + scale-factor warps + softmax warps
   uint64_t bar_s[2];               // [t]: S_t(u) written (MMA commit)
   uint64_t bar_sr[2];              // [t]: S_t(u) read by the softmax (128 arrivals)
   uint64_t bar_p[2][2];            // [t][u & 1]: P_t(u) written and O rescaled (128 arrivals)
   uint64_t bar_o[2][2];            // [t][u & 1]: PV_t(u) done (MMA commit)
   uint64_t bar_sf[2];              // [u & 1]: K and V scale factors of u in TMEM (128)
   uint64_t bar_sffree[2];          // [u & 1]: MMAs of u done, scale buffers free (nq commits)
-  uint64_t bar_c[2];               // [u & 1]: c(u) in smem (128)
-  uint64_t bar_cfree[2];           // [u & 1]: c(u) read by the softmax (128 nq)
   uint64_t bar_drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -104,7 +102,8 @@ struct Nvfp4Args {
   const uint8_t* q_sf;     // [H][Tp][8]
   const uint8_t* k_sf;     // [H][Tp][8]
   const uint8_t* v_sf;     // [H][Tp/128][128][8]
-  const float* q_mean;     // [H][Tp/128][128]
+  const float* qmk;        // qm K^T table: segment s at c_off[s], [H][nb_s][128 nb_s]
+  const int64_t* c_off;
   const float* q_km;       // [H][Tp]: q . km per query row
   __nv_bfloat16* out;
   int64_t ost, osh;
@@ -117,7 +116,7 @@ struct Nvfp4Args {
 };
 
 enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4,
-                  kRoleCorrection = 5 };
+                  kRoleScales = 5 };
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, Smem& S,
                                          const Nvfp4Args& a, int role) {
@@ -142,24 +141,29 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
   const int n_kv = sg.nblk;
   const int64_t Tp = a.tpad, h = wi.head;
   const int rq = sg.row0 + wi.qt0 * kTile;
-  mbar_arrive_expect_tx_elect(smem_u32(&S.bar_q), uint32_t(wi.nq) * (kCodeTile + kSfTile + 512));
+  mbar_arrive_expect_tx_elect(smem_u32(&S.bar_q), uint32_t(wi.nq) * (kCodeTile + kSfTile));
   for (int t = 0; t < wi.nq; ++t) {
     const int row = rq + t * kTile;
     tma_load_3d_elect(smem_u32(S.q[t]), tm_q, smem_u32(&S.bar_q), 0, row, wi.head);
     bulk_load_elect(smem_u32(S.qsf[t]), a.q_sf + (h * Tp + row) * 8, kSfTile, smem_u32(&S.bar_q));
-    bulk_load_elect(smem_u32(S.qm[t]), a.q_mean + (h * (Tp / kTile) + row / kTile) * kD, 512,
-                    smem_u32(&S.bar_q));
   }
+  // rows of the qm K^T table of this (segment, head) for the CTA's query tiles
+  const int64_t lp = int64_t(sg.nblk) * kTile;
+  const float* tab = a.qmk + a.c_off[wi.seg] + (h * sg.nblk + wi.qt0) * lp;
   int issued = 0;
   for (int j = 0; j < n_kv; ++j) {
     const int st = j % kStages;
     if (j >= kStages && !wait_all(&S.bar_free[st], ((j / kStages) - 1) & 1, S, a, kRoleProducer))
       break;
     const int row = sg.row0 + j * kTile;
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]), kCodeTile + kSfTile);
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]),
+                                kCodeTile + kSfTile + uint32_t(wi.nq) * kTile * 4);
     tma_load_3d_elect(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_k[st]), 0, row, wi.head);
     bulk_load_elect(smem_u32(S.ksf[st]), a.k_sf + (h * Tp + row) * 8, kSfTile,
                     smem_u32(&S.bar_k[st]));
+    for (int t = 0; t < wi.nq; ++t)
+      bulk_load_elect(smem_u32(S.cq[st][t]), tab + t * lp + int64_t(j) * kTile, kTile * 4,
+                      smem_u32(&S.bar_k[st]));
     mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[st]), kCodeTile + kSfTile);
     tma_load_3d_elect(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_v[st]), row / 2, 0, wi.head);
     bulk_load_elect(smem_u32(S.vsf[st]), a.v_sf + (h * (Tp / kTile) + row / kTile) * kSfTile,
@@ -239,19 +243,17 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
 }
 
 // ---------------------------------------------------------------------------------------------
-// Correction warps: scale factors of K and V into tensor memory, and c_t(j) = (qm_t . deq(Kc_j)) c
-// for both query tiles in FP32. Thread (warp cw, lane) takes channel quarter lane >> 3 (32
-// channels = one 16-byte chunk of the key row, two scale groups) of keys 16 cw + 8 pass +
-// (lane & 7); the four quarters of a key combine by two shuffles (the same sum in all four lanes,
-// float addition being commutative).
+// Scale-factor warps: the Q scale factors once, then per sub-tile the K and V scale factors into
+// tensor memory. Each warp writes its own lane quarter (the MMA reads A-side scales of row r from
+// lane r and B-side scales from every lane quarter).
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void correction(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
-                                           const SegInfo& sg, uint32_t tmem, int cw, int lane) {
+__device__ __forceinline__ void scale_factor_warps(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
+                                                   const SegInfo& sg, uint32_t tmem, int cw,
+                                                   int lane) {
   const int n_sub = (sg.len + kSub - 1) / kSub;
   const int quarter = (kCorrWarp + cw) & 3;  // tensor-memory lane quarter this warp may access
   const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-  const int cq = lane >> 3;                  // channel quarter
-  if (!wait_all(&S.bar_q, 0, S, a, kRoleCorrection)) return;
+  if (!wait_all(&S.bar_q, 0, S, a, kRoleScales)) return;
   // Q scale factors (A side: row r in lane r, column r / 32; K step kk at +4kk).
   {
     const int r = quarter * 32 + lane;
@@ -261,70 +263,25 @@ __device__ __forceinline__ void correction(Smem& S, const Nvfp4Args& a, const Wo
       tmem_st1(tmem + col_qsf(t) + 4u + uint32_t(quarter) + lane_off, w.y);
     }
   }
-  // qm_t of channels 32 cq + 2i, 32 cq + 2i + 1
-  float2 qmf[2][16];
-#pragma unroll
-  for (int t = 0; t < 2; ++t)
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      qmf[t][i] = t < wi.nq ? *reinterpret_cast<const float2*>(&S.qm[t][32 * cq + 2 * i])
-                            : make_float2(0.f, 0.f);
-  const float cs = a.scale_log2;
   for (int u = 0; u < n_sub; ++u) {
     const int j = u >> 1, h = u & 1, st = j % kStages, b = u & 1;
     if (h == 0) {
-      if (!wait_all(&S.bar_k[st], (j / kStages) & 1, S, a, kRoleCorrection)) break;
-      if (!wait_all(&S.bar_v[st], (j / kStages) & 1, S, a, kRoleCorrection)) break;
+      if (!wait_all(&S.bar_k[st], (j / kStages) & 1, S, a, kRoleScales)) break;
+      if (!wait_all(&S.bar_v[st], (j / kStages) & 1, S, a, kRoleScales)) break;
     }
-    if (u >= 2 && !wait_all(&S.bar_sffree[b], ((u - 2) >> 1) & 1, S, a, kRoleCorrection)) break;
+    if (u >= 2 && !wait_all(&S.bar_sffree[b], ((u - 2) >> 1) & 1, S, a, kRoleScales)) break;
     // B-side scale factors, every lane quarter: K rows (keys) 32c + lane in column c of K step kk;
     // V rows (channels) 32c + lane in column c, word h of the channel's 8-byte record.
-    {
-      const uint2 k0 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + lane) * 8);
-      const uint2 k1 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + 32 + lane) * 8);
-      const uint32_t kw[8] = {k0.x, k1.x, 0u, 0u, k0.y, k1.y, 0u, 0u};
-      tmem_st8(tmem + col_ksf(b) + lane_off, kw);
-      const uint32_t* vs = reinterpret_cast<const uint32_t*>(S.vsf[st]);
-      tmem_st4(tmem + col_vsf(b) + lane_off, vs[lane * 2 + h], vs[(32 + lane) * 2 + h],
-               vs[(64 + lane) * 2 + h], vs[(96 + lane) * 2 + h]);
-    }
+    const uint2 k0 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + lane) * 8);
+    const uint2 k1 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + 32 + lane) * 8);
+    const uint32_t kw[8] = {k0.x, k1.x, 0u, 0u, k0.y, k1.y, 0u, 0u};
+    tmem_st8(tmem + col_ksf(b) + lane_off, kw);
+    const uint32_t* vs = reinterpret_cast<const uint32_t*>(S.vsf[st]);
+    tmem_st4(tmem + col_vsf(b) + lane_off, vs[lane * 2 + h], vs[(32 + lane) * 2 + h],
+             vs[(64 + lane) * 2 + h], vs[(96 + lane) * 2 + h]);
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_sf[b]));  // the MMAs of u may start
-    if (u >= 2 && !wait_all(&S.bar_cfree[b], ((u - 2) >> 1) & 1, S, a, kRoleCorrection)) break;
-#pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
-      const int key = 16 * cw + 8 * pass + (lane & 7);
-      const int row = 64 * h + key;  // row of the 128-key tile
-      // 64-byte swizzle: 16-byte chunk c of row r is stored at chunk c ^ ((r >> 1) & 3)
-      const uint4 cv = *reinterpret_cast<const uint4*>(S.k[st] + row * 64 +
-                                                       ((cq ^ ((row >> 1) & 3)) << 4));
-      const uint32_t sfh = *reinterpret_cast<const uint16_t*>(S.ksf[st] + row * 8 + 2 * cq);
-      const uint32_t w[4] = {cv.x, cv.y, cv.z, cv.w};
-      float tot0 = 0.f, tot1 = 0.f;
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {  // 16 channels = 8 bytes = words 2g, 2g + 1
-        float a0x = 0.f, a0y = 0.f, a1x = 0.f, a1y = 0.f;
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const uint32_t byte = (w[2 * g + (p >> 2)] >> (8 * (p & 3))) & 0xFFu;
-          const float2 f = f16x2_to_f32x2(cvt_e2m1x2_to_f16x2(byte));
-          const float2 m0 = qmf[0][8 * g + p], m1 = qmf[1][8 * g + p];
-          fma2v(a0x, a0y, f.x, f.y, m0.x, m0.y, a0x, a0y);
-          fma2v(a1x, a1y, f.x, f.y, m1.x, m1.y, a1x, a1y);
-        }
-        const float ds = e4m3_to_f32(sfh >> (8 * g));
-        tot0 = fmaf(a0x + a0y, ds, tot0);
-        tot1 = fmaf(a1x + a1y, ds, tot1);
-      }
-      tot0 += __shfl_xor_sync(0xffffffffu, tot0, 8);
-      tot0 += __shfl_xor_sync(0xffffffffu, tot0, 16);
-      tot1 += __shfl_xor_sync(0xffffffffu, tot1, 8);
-      tot1 += __shfl_xor_sync(0xffffffffu, tot1, 16);
-      if (cq == 0) S.c[b][0][key] = tot0 * cs;
-      else if (cq == 1) S.c[b][1][key] = tot1 * cs;
-    }
-    mbar_arrive(smem_u32(&S.bar_c[b]));
     if (h == 1 || u + 1 == n_sub) {
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.bar_free[st]));
@@ -365,10 +322,11 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_sr[t]));  // S_t(u+1) may now overwrite S
-    if (!(ok = wait_all(&S.bar_c[x], (u >> 1) & 1, S, a, kRoleSoftmax))) break;
-    // s'' = S c + c_t(j)
+    // s'' = S c + the table's qm K^T term (it arrived with the key tile)
+    const int kt = u >> 1, kst = kt % kStages;
+    if (!(ok = wait_all(&S.bar_k[kst], (kt / kStages) & 1, S, a, kRoleSoftmax))) break;
     float s[64];
-    const float4* cp = reinterpret_cast<const float4*>(S.c[x][t]);
+    const float4* cp = reinterpret_cast<const float4*>(S.cq[kst][t] + kSub * x);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float4 cc = cp[i];
@@ -378,7 +336,10 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
       fma2v(s[k0 + 2], s[k0 + 3], __uint_as_float(r[k0 >> 5][(k0 + 2) & 31]),
             __uint_as_float(r[k0 >> 5][(k0 + 3) & 31]), cs, cs, cc.z, cc.w);
     }
-    mbar_arrive(smem_u32(&S.bar_cfree[x]));
+    if (x == 1 || u + 1 == n_sub) {  // this warp is done with the stage's table rows
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.bar_free[kst]));
+    }
     if (u == n_sub - 1 && last_valid < kSub) {
 #pragma unroll
       for (int i = 0; i < 64; ++i)
@@ -513,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&S.bar_k[i]), 1);
       mbar_init(smem_u32(&S.bar_v[i]), 1);
-      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 4);  // MMA commits + correction warps
+      // MMA commits + scale-factor warps + softmax warps (they read the stage's table rows)
+      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 4 + 4 * wi.nq);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&S.bar_s[t]), 1);
@@ -527,8 +489,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&S.bar_sf[b]), 128);
       mbar_init(smem_u32(&S.bar_sffree[b]), wi.nq);
-      mbar_init(smem_u32(&S.bar_c[b]), 128);
-      mbar_init(smem_u32(&S.bar_cfree[b]), 128 * wi.nq);
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -553,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp - kMmaWarp;
     if (t < wi.nq) mma_issuer(S, a, wi, sg, tmem, t);
   } else if (warp >= kCorrWarp) {
-    correction(S, a, wi, sg, tmem, warp - kCorrWarp, lane);
+    scale_factor_warps(S, a, wi, sg, tmem, warp - kCorrWarp, lane);
   } else {
     const int t = warp >> 2;
     if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 3, lane);
@@ -595,7 +555,8 @@ int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t 
   a.q_sf = ws + p.ws.q_sf;
   a.k_sf = ws + p.ws.k_sf;
   a.v_sf = ws + p.ws.v_sf;
-  a.q_mean = reinterpret_cast<const float*>(ws + p.ws.q_mean);
+  a.qmk = reinterpret_cast<const float*>(ws + p.ws.qmk);
+  a.c_off = p.d_coff;
   a.q_km = reinterpret_cast<const float*>(ws + p.ws.q_km);
   a.lse = lse;
   a.lse_sh = lse_sh;

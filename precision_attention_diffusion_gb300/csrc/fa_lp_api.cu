@@ -23,6 +23,7 @@
 using falp::BlockInfo;
 using falp::SegInfo;
 using falp::WorkItem;
+using falp::QmkItem;
 
 namespace {
 
@@ -86,10 +87,14 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   const size_t n_seg = p->segs.size() * sizeof(SegInfo);
   const size_t n_blk = p->blocks.size() * sizeof(BlockInfo);
   const size_t n_wrk = p->work.size() * sizeof(WorkItem);
+  const size_t n_qmk = p->qmk_items.size() * sizeof(QmkItem);
+  const size_t n_cof = p->c_off.size() * sizeof(int64_t);
   const size_t o_seg = 0;
   const size_t o_blk = align_up(o_seg + n_seg, 256);
   const size_t o_wrk = align_up(o_blk + n_blk, 256);
-  const size_t o_err = align_up(o_wrk + n_wrk, 256);
+  const size_t o_qmk = align_up(o_wrk + n_wrk, 256);
+  const size_t o_cof = align_up(o_qmk + n_qmk, 256);
+  const size_t o_err = align_up(o_cof + n_cof, 256);
   const size_t total = o_err + 256;
   void* d = nullptr;
   if (cudaMalloc(&d, total) != cudaSuccess) {
@@ -100,6 +105,8 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   if (n_seg) std::memcpy(host.data() + o_seg, p->segs.data(), n_seg);
   if (n_blk) std::memcpy(host.data() + o_blk, p->blocks.data(), n_blk);
   if (n_wrk) std::memcpy(host.data() + o_wrk, p->work.data(), n_wrk);
+  if (n_qmk) std::memcpy(host.data() + o_qmk, p->qmk_items.data(), n_qmk);
+  if (n_cof) std::memcpy(host.data() + o_cof, p->c_off.data(), n_cof);
   if (cudaMemcpyAsync(d, host.data(), total, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaFree(d);
@@ -111,6 +118,8 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   p->d_segs = reinterpret_cast<SegInfo*>(b + o_seg);
   p->d_blocks = reinterpret_cast<BlockInfo*>(b + o_blk);
   p->d_work = reinterpret_cast<WorkItem*>(b + o_wrk);
+  p->d_qmk = reinterpret_cast<QmkItem*>(b + o_qmk);
+  p->d_coff = reinterpret_cast<int64_t*>(b + o_cof);
   p->d_err = reinterpret_cast<int*>(b + o_err);
   if (log_enabled())
     std::fprintf(stderr, "[fa_lp] plan %p: device tables %zu bytes on device %d\n", (void*)p,
@@ -189,6 +198,22 @@ void build_plan(fa_lp_plan* p) {
     w.k_mean = take(size_t(p->nseg) * H * 128 * 4);
     w.k_chunk = take(p->blocks.size() * H * 128 * 8);
     w.q_km = take(H * Tp * 4);
+    // qm K^T table: segment s holds [H][nb_s][128 nb_s] floats (quadratic in the segment length:
+    // 1.6 GB for one 30272-token segment at H = 56)
+    p->c_off.assign(ns, 0);
+    size_t floats = 0;
+    for (int s = 0; s < ns; ++s) {
+      const int64_t nb = p->segs[s].nblk;
+      p->c_off[s] = int64_t(floats);
+      floats += size_t(H) * size_t(nb) * size_t(nb) * 128;
+      const int64_t ntiles = (nb * 128 + 255) / 256;
+      for (int64_t mt = 0; mt * 128 < nb; ++mt)
+        for (int64_t nt = 0; nt < ntiles; nt += falp::kQmkTilesPer)
+          p->qmk_items.push_back(falp::QmkItem{
+              s, int32_t(mt), int32_t(nt),
+              int32_t(std::min<int64_t>(falp::kQmkTilesPer, ntiles - nt))});
+    }
+    w.qmk = take(floats * 4);
   }
   w.total = off;
 }
@@ -470,6 +495,11 @@ int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
     case FA_LP_Q_MEANS: return set(p->ws.q_mean, H, Tp / 128, 128, 4);
     case FA_LP_K_MEANS: return set(p->ws.k_mean, p->nseg, H, 128, 4);
     case FA_LP_Q_KM: return set(p->ws.q_km, 1, H, Tp, 4);
+    case FA_LP_QMK_TABLE: {
+      int64_t n = 0;
+      for (const auto& sg : p->segs) n += int64_t(H) * sg.nblk * sg.nblk * 128;
+      return set(p->ws.qmk, 1, 1, n, 4);
+    }
     default: return FA_LP_ERR_INVALID_ARG;
   }
 }

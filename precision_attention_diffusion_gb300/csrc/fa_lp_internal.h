@@ -39,6 +39,15 @@ struct WorkItem {
   int32_t nq;       // 1 or 2 query tiles
 };
 
+// Tile of the NVFP4 qm K^T table: (segment, 128-block M tile, 256-key N tile).
+struct QmkItem {
+  int32_t seg;
+  int32_t mt;       // 128-block M tile
+  int32_t nt;       // first 256-key N tile
+  int32_t ntiles;   // N tiles of this CTA
+};
+constexpr int kQmkTilesPer = 8;  // N tiles per table CTA
+
 // Workspace layout of one plan (byte offsets from the workspace base, 1024-aligned).
 struct WsLayout {
   size_t q_codes = 0, k_codes = 0, v_codes = 0;  // FP8: [H][Tp][128], [H][Tp][128], [H][128][Tp]
@@ -46,6 +55,7 @@ struct WsLayout {
   size_t q_mean = 0, k_mean = 0;                 // NVFP4 means (f32)
   size_t k_chunk = 0;                            // NVFP4 scratch: f64 [nblk][H][128] chunk sums
   size_t q_km = 0;                               // NVFP4: f32 [H][Tp] q . km (row LSE term)
+  size_t qmk = 0;                                // NVFP4: f32 qm K^T table (per segment)
   size_t amax = 0, descale = 0;                  // FP8: u32 [3][H], f32 [3][H]
   size_t total = 0;
 };
@@ -67,6 +77,8 @@ struct fa_lp_plan {
   std::vector<falp::SegInfo> segs;
   std::vector<falp::BlockInfo> blocks;
   std::vector<falp::WorkItem> work;
+  std::vector<falp::QmkItem> qmk_items;          // NVFP4 qm K^T table tiles
+  std::vector<int64_t> c_off;                    // NVFP4: float offset of each segment's table
   falp::WsLayout ws;
   int64_t spin_limit = 20000;  // parked probes of <= 100 us each: about 2 s per wait
   // device metadata (created on first use on the plan's device)
@@ -74,6 +86,8 @@ struct fa_lp_plan {
   falp::SegInfo* d_segs = nullptr;
   falp::BlockInfo* d_blocks = nullptr;
   falp::WorkItem* d_work = nullptr;
+  falp::QmkItem* d_qmk = nullptr;
+  int64_t* d_coff = nullptr;
   int* d_err = nullptr;  // [0]: sticky device status, [1]: abort word (launch generation)
   bool quantized = false;
   int refcount = 1;
@@ -100,6 +114,7 @@ int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64
                           int64_t vst, int64_t vsh, cudaStream_t stream);
 int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
                            float* lse, int64_t lse_sh, cudaStream_t stream);
+int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, cudaStream_t stream);
 int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
 
 // Distinct positive id per kernel launch (device-side abort words compare against it).

@@ -207,7 +207,9 @@ int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64
       ws + p.ws.k_codes, ws + p.ws.q_sf, ws + p.ws.k_sf, reinterpret_cast<float*>(ws + p.ws.q_km));
   nvfp4_pack_vt_kernel<<<dim3(unsigned(nblk), unsigned(H)), 256, 0, stream>>>(
       vb, vst, vsh, p.d_blocks, H, p.tpad, ws + p.ws.v_codes, ws + p.ws.v_sf);
-  return cuda_status(cudaGetLastError());
+  const int st = cuda_status(cudaGetLastError());
+  if (st != FA_LP_OK) return st;
+  return launch_nvfp4_qmk(p, ws, stream);  // the qm K^T table from the means and K codes
 }
 
 }  // namespace falp

@@ -280,6 +280,18 @@ __device__ __forceinline__ void mma_f8f6f4_ss_elect(uint32_t d_tmem, uint64_t ad
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (F16 or BF16 operands, F32 accumulate).
+__device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_f8f6f4_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
                                                     uint64_t bdesc, uint32_t idesc,
                                                     uint32_t accumulate) {

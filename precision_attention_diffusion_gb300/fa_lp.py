@@ -26,7 +26,8 @@ FA_LP_ERR_STATE = 6
 MODE_FP8 = 0
 MODE_NVFP4 = 1
 
-Q_CODES, K_CODES, V_CODES, DESCALE, Q_SCALES, K_SCALES, V_SCALES, Q_MEANS, K_MEANS, Q_KM = range(10)
+(Q_CODES, K_CODES, V_CODES, DESCALE, Q_SCALES, K_SCALES, V_SCALES, Q_MEANS, K_MEANS, Q_KM,
+ QMK_TABLE) = range(11)
 
 # Every symbol include/fa_lp.h declares.
 EXPORTS = (

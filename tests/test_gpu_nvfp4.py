@@ -248,3 +248,38 @@ def test_nvfp4_lse_ragged_varlen(fa):
     # and 6), so log l moves by at most ln(1.25) = 0.22 plus the score quantization
     d = np.abs(g - exact)
     assert d.max() < 0.25 and d.mean() < 0.04, (d.max(), d.mean())
+
+
+def test_nvfp4_qmk_table(fa):
+    """The qm K^T table on the BF16 tensor cores (qm in three BF16 pieces, deq(Kc) exact): every
+    entry of every segment against numpy on the oracle's quantized operands, relative to the
+    magnitude of the products summed."""
+    cu, H = [0, 0, 17, 300, 300, 1400, 1500], 3
+    T = cu[-1]
+    q, k, v = inputs.qkv_separate(T, H, seed=14)
+    k = with_k_offset(k, H, 14)
+    plan = fa.Plan(cu, H, mode=fa.MODE_NVFP4)
+    plan.quantize(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    tab = plan.quantized(fa.QMK_TABLE).cpu().numpy().reshape(-1).astype(np.float64)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    e2, e4 = oracle.e2m1_decode_table(), oracle.e4m3_decode_table()
+    kd = e2[z["ck"]] * np.repeat(e4[z["sk"]], 16, axis=2)          # [T, H, 128]
+    c = SCALE * 1.4426950408889634
+    off = 0
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        nb = (b - a + 127) // 128
+        if nb == 0:
+            continue
+        lp = nb * 128
+        got = tab[off:off + H * nb * lp].reshape(H, nb, lp)
+        qm = z["qm"][z["qoff"][s]:z["qoff"][s] + nb].astype(np.float64)   # [nb, H, 128]
+        kseg = np.zeros((lp, H, 128))
+        kseg[:b - a] = kd[a:b]
+        want = np.einsum("bhc,jhc->hbj", qm, kseg) * c
+        mag = np.einsum("bhc,jhc->hbj", np.abs(qm), np.abs(kseg)) * c
+        assert np.all(np.abs(got - want) <= 1e-6 * mag + 1e-30), f"segment {s}"
+        assert np.all(got[:, :, b - a:] == 0)
+        off += H * nb * lp
+    assert off == tab.size

@@ -263,19 +263,21 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
                     wait_phase(smem_u32(&S.bar_s[t][b]), (u >> 1) & 1, S, a, kRoleSoftmax));
     if (!ok) break;
     tc_fence_after();
+    // the loads also return each half's maximum (the tensor-memory load unit reduces)
     uint32_t r[2][32];
-    tmem_ld32(s_addr, r[0]);
-    tmem_ld32(s_addr + 32, r[1]);
+    const float mx0 = tmem_ld32_max(s_addr, r[0]);
+    const float mx1 = tmem_ld32_max(s_addr + 32, r[1]);
     tmem_wait_ld();
     float s[64];
 #pragma unroll
     for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i >> 5][i & 31]);
-    if (u == n_sub - 1 && last_valid < kSub) {
+    float mx = fmaxf(mx0, mx1);
+    if (u == n_sub - 1 && last_valid < kSub) {  // keys past the segment: mask, then reduce
 #pragma unroll
       for (int i = 0; i < 64; ++i)
         if (i >= last_valid) s[i] = -INFINITY;
+      mx = row_max64(s);
     }
-    const float mx = row_max64(s);
     const bool move = (m == -INFINITY) || ((mx - m) * c > kTau);
     const float m_new = move ? mx : m;
     const float alpha = move ? ex2_approx((m - m_new) * c) : 1.f;  // m = -inf gives 0

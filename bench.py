@@ -51,10 +51,10 @@ KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5}
 # an ncu capture of the full-size workload (profiles/attn_traffic_s30272_h56.md), keyed by the
 # workload and the SHA-256 of the kernel source at capture time (null once the kernel changed).
 NCU_TRAFFIC = {
-    ("fp8_s30272_h56", "fba5a605fc1a59db655064b8167a3e1ed78b5d2dc713322bb339e89570419bf1"):
-        2.10e9 + 425.25e6,
-    ("nvfp4_s30272_h56", "0525d6d7756763fc300a6d1d0b24d9d5a7b2fe520b4dd6e839a290400fb0a20b"):
-        432.69e6 + 397.73e6,
+    ("fp8_s30272_h56", "477a3a0bd384a21293607f7b92bde901f4d9f3e5e755fddca8c4d1e8fb611690"):
+        2.12e9 + 425.24e6,
+    ("nvfp4_s30272_h56", "f6a361be72e9c338d50c9168ffec701aa8fbacfaac1ac073329a484f014e965e"):
+        2.39e9 + 425.11e6,
 }
 
 

@@ -328,7 +328,10 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
     mbar_arrive(smem_u32(&S.bar_p[t][b]));
     m = m_new;
   }
-  if (!ok) return;
+  if (!ok) {
+    tmem_wait_st();  // a P store or O rescale may still be in flight
+    return;
+  }
   // PV_t(n_sub - 1) done implies every earlier PV of this in-order stream is done
   ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_o[t][(n_sub - 1) & 1]),
                                           ((n_sub - 1) >> 1) & 1, S, a, kRoleEpilogue));

@@ -53,15 +53,24 @@ __device__ __forceinline__ uint32_t group16(const float (&x)[4], uint8_t* sf_out
   return lo | (hi << 8);
 }
 
-// Pass 1: per (128-row block, head) column sums in FP64, rows in order. For Q (z = 0) the block
-// is one mean's whole extent: write the block mean. For K (z = 1) store the chunk sum. The block's
-// rows are staged in shared memory with 16-byte loads (the global reads are coalesced and in
-// flight together); then thread c adds column c's rows in order.
+// Pass 1: per (128-row block, head) column sums, equal to the FP64 sums of the rows in order. For
+// Q (z = 0) the block is one mean's whole extent: write the block mean. For K (z = 1) store the
+// chunk sum. The block's rows are staged in shared memory with 16-byte loads; two threads share a
+// column (rows 0-63 and 64-127).
+//
+// A nonzero BF16 value is +-s 2^k with an integer significand s < 256 and k = exponent - 134
+// (subnormals: k = -133). If a column's k span at most 38, every partial sum of the column is a
+// multiple of 2^kmin below 2^53 in magnitude, so each FP64 addition of the in-order sum is exact
+// and that sum is the exact sum: computed here as an int64 fixed-point sum in any order, then
+// converted exactly. Otherwise (rare: values 2^38 apart in one column) the column is summed in
+// FP64, rows in order, as the definition reads.
 __global__ void __launch_bounds__(256) nvfp4_block_sums_kernel(
     const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
     int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t nblk,
     float* __restrict__ qmean, double* __restrict__ kchunk) {
   __shared__ __align__(16) uint16_t tile[kTile][kD + 8];  // +8: rows start on distinct banks
+  __shared__ int kmin_s[2][kD], kmax_s[2][kD];
+  __shared__ long long part_s[kD];
   const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const BlockInfo bi = blocks[b];
   const uint16_t* x = z == 0 ? q : k;
@@ -76,10 +85,44 @@ __global__ void __launch_bounds__(256) nvfp4_block_sums_kernel(
     *reinterpret_cast<uint4*>(&tile[r][c8]) = w;
   }
   __syncthreads();
-  const int c = threadIdx.x;
-  if (c >= kD) return;
+  const int c = threadIdx.x & (kD - 1), half = threadIdx.x >> 7;
+  const int r0 = half * 64, r1 = min(r0 + 64, bi.nvalid);
+  int kmn = 0x7fffffff, kmx = -0x7fffffff;
+  for (int r = r0; r < r1; ++r) {
+    const uint32_t v = tile[r][c];
+    if ((v & 0x7FFFu) == 0) continue;
+    const int e = int((v >> 7) & 0xFFu);
+    const int kk = e ? e - 134 : -133;
+    kmn = min(kmn, kk);
+    kmx = max(kmx, kk);
+  }
+  kmin_s[half][c] = kmn;
+  kmax_s[half][c] = kmx;
+  __syncthreads();
+  kmn = min(kmin_s[0][c], kmin_s[1][c]);
+  kmx = max(kmax_s[0][c], kmax_s[1][c]);
+  // all zero, or every partial sum exact in FP64 (the same decision for both threads of c)
+  const bool exact = kmx < kmn || kmx - kmn <= 38;
+  long long acc = 0;
+  if (exact) {
+    for (int r = r0; r < r1; ++r) {
+      const uint32_t v = tile[r][c];
+      if ((v & 0x7FFFu) == 0) continue;
+      const int e = int((v >> 7) & 0xFFu);
+      const long long sig = (e ? 128 : 0) + (v & 0x7Fu);
+      const long long mag = sig << ((e ? e - 134 : -133) - kmn);
+      acc += (v & 0x8000u) ? -mag : mag;
+    }
+  }
+  if (half == 1) part_s[c] = acc;
+  __syncthreads();
+  if (half == 1) return;
   double sum = 0.0;
-  for (int r = 0; r < bi.nvalid; ++r) sum += double(__uint_as_float(uint32_t(tile[r][c]) << 16));
+  if (exact) {
+    if (kmx >= kmn) sum = ldexp(double(acc + part_s[c]), kmn);
+  } else {
+    for (int r = 0; r < bi.nvalid; ++r) sum += double(__uint_as_float(uint32_t(tile[r][c]) << 16));
+  }
   if (z == 0)
     qmean[(int64_t(h) * nblk + b) * kD + c] = __double2float_rn(sum / double(bi.nvalid));
   else

@@ -283,3 +283,23 @@ def test_nvfp4_qmk_table(fa):
         assert np.all(got[:, :, b - a:] == 0)
         off += H * nb * lp
     assert off == tab.size
+
+
+def test_nvfp4_means_wide_exponent_columns(fa):
+    """Column sums take an exact integer path when a column's exponents span at most 38 bits and
+    the in-order FP64 path otherwise; both must give the oracle's FP64 in-order sums bit for bit.
+    Channel 5 mixes 2^20 and 2^-20 (span 40: FP64 path), channel 9 mixes 2^15 and 2^-12 (exact
+    path with a wide shift), channel 11 holds subnormal BF16 values."""
+    cu, H = [0, 300, 700], 2
+    q, k, v = inputs.qkv_separate(700, H, seed=15)
+    q, k = q.float(), k.float()
+    for x in (q, k):
+        x[3, :, 5] = 2.0 ** 20
+        x[4, :, 5] = 2.0 ** -20
+        x[410, :, 5] = -(2.0 ** 21)
+        x[411, :, 5] = 3 * 2.0 ** -22
+        x[7, :, 9] = 2.0 ** 15
+        x[8, :, 9] = 2.0 ** -12
+        x[20:30, :, 11] = 2.0 ** -130
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    check_nvfp4_quant(fa, q, k, v, cu, H)

@@ -217,6 +217,19 @@ def oracle_sample(cu, H, seconds, seed=0, mode="fp8"):
 
 
 # ------------------------------------------------------------------------------------------------
+def max_over_ranks(x: float) -> float:
+    """Maximum of x over the ranks of the default process group (x itself without one). The
+    tensor lives on the device for NCCL and on the host for gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -344,11 +357,7 @@ def run_ours(args):
     total_ms = ev[0].elapsed_time(ev[1])
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in evf)
     q_ms = statistics.mean(a.elapsed_time(b) for a, b in evq)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms)
     if plan.last_error():
         raise RuntimeError("device wait expired in the timed region")
     ms_per_step = total_ms / K
@@ -379,11 +388,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / K
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms)
         e2e = {"value": ws * flops / (e_ms / 1e3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms, "h2d_bytes_per_step": hbuf.numel() * hbuf.element_size(),
                "d2h_bytes_per_step": hout.numel() * hout.element_size()}

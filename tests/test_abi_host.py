@@ -116,3 +116,25 @@ def test_calls_validate_before_touching_the_device(lib):
         assert lib.fa_lp_encode(3, None, 0, None, None) == 1
     finally:
         lib.fa_lp_plan_destroy(h)
+
+
+def test_nvfp4_workspace_holds_the_qmk_table(lib):
+    """NVFP4 plans size their workspace for the qm K^T table: H nb_s^2 128 floats per segment
+    (quadratic in the segment length), on top of the codes, scales and means."""
+    def ws_of(cu, heads):
+        st, h = _create(lib, cu, heads=heads, mode=1)
+        assert st == 0
+        try:
+            ws = ctypes.c_size_t()
+            assert lib.fa_lp_workspace_bytes(h, ctypes.byref(ws)) == 0
+            return ws.value
+        finally:
+            assert lib.fa_lp_plan_destroy(h) == 0
+    one = ws_of([0, 30272], 56)
+    table = 56 * 237 * 237 * 128 * 4
+    assert table <= one <= table + 2 * 30336 * 56 * 128
+    # the same tokens in two segments: half the blocks each, a quarter of the table each
+    two = ws_of([0, 15136, 30272], 56)
+    assert two <= one - 0.49 * table
+    # an empty segment adds no table
+    assert ws_of([0, 0, 30272], 56) <= one + 4096

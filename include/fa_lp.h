@@ -203,7 +203,7 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
 #define FA_LP_K_MEANS 8     /* NVFP4: f32 [num_segments][H][128], segment means                  */
 #define FA_LP_Q_KM 9        /* NVFP4: f32 [H][Tpad], q . km of each query row (LSE term)         */
 #define FA_LP_QMK_TABLE 10  /* NVFP4: f32 [1][1][n]: per segment s (in order) [H][nb_s][128 nb_s]  */
-                            /* = (qm_block . deq(Kc_key)) * softmax_scale * log2(e)               */
+                            /* = qm_block . deq(Kc_key) (raw units of the scores)                 */
 
 typedef struct fa_lp_array_desc {
   const void* data;  /* device address                                                     */

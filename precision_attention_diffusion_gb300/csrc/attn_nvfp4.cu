@@ -60,6 +60,9 @@ constexpr uint32_t kCodeTile = 128 * 64;  // 128 rows of 128 E2M1 codes
 constexpr uint32_t kSfTile = 128 * 8;     // 128 rows of 8 UE4M3 scales
 constexpr uint32_t kIdescS = idesc_mxf4nvf4(128, kSub);
 constexpr uint32_t kIdescPV = idesc_mxf4nvf4(128, 128);
+// kind::f16: D f32, A and B BF16, K-major, M=128, N=64
+constexpr uint32_t kIdescFold = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(kSub) >> 3) << 17) |
+                                ((128u >> 4) << 24);
 constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
 constexpr float kLog2_6 = 2.5849625007211562f;
 
@@ -76,6 +79,11 @@ struct Smem {
   uint8_t q[2][kCodeTile];
   uint8_t k[kStages][kCodeTile];
   uint8_t v[kStages][kCodeTile];   // V^T: 128 channel rows of 128 keys
+  // qm K^T fold into S (one kind::f16 MMA per sub-tile): A = 128 identical rows [1, 1, 1, 0...]
+  // (one core matrix repeated, then a zero core matrix), B = per key the table entry as three
+  // BF16 pieces (64 keys x 16 bytes, then 1 KB of zeros for K 8..15)
+  uint8_t fa[256];
+  uint8_t fb[2][2][2048];          // [u & 1][t]
   uint8_t qsf[2][kSfTile];
   uint8_t ksf[kStages][kSfTile];   // [key][8]
   uint8_t vsf[kStages][kSfTile];   // [channel][8]
@@ -83,7 +91,7 @@ struct Smem {
   uint64_t bar_q;
   uint64_t bar_k[kStages];
   uint64_t bar_v[kStages];
-  uint64_t bar_free[kStages];      // MMA commits + scale-factor warps + softmax warps
+  uint64_t bar_free[kStages];      // MMA commits + scale-factor warps
   uint64_t bar_s[2];               // [t]: S_t(u) written (MMA commit)
   uint64_t bar_sr[2];              // [t]: S_t(u) read by the softmax (128 arrivals)
   uint64_t bar_p[2][2];            // [t][u & 1]: P_t(u) written and O rescaled (128 arrivals)
@@ -193,6 +201,7 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
   const uint64_t dq = sdesc_kmajor_sw64(smem_u32(S.q[t]));
   const uint64_t dk = sdesc_kmajor_sw64(smem_u32(S.k[0]));
   const uint64_t dv = sdesc_kmajor_sw64(smem_u32(S.v[0]));
+  const uint64_t dfa = sdesc_kmajor_noswz(smem_u32(S.fa), 128, 0);
   auto issue_s = [&](int u) {
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
     const uint64_t kb = dk + (((j % kStages) * kCodeTile + h * (kSub * 64)) >> 4);
@@ -200,6 +209,9 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
     for (int kk = 0; kk < 2; ++kk)
       mma_mxf4_ss_elect(tmem + col_s(t), dq + 2 * kk, kb + 2 * kk, kIdescS,
                         tmem + col_qsf(t) + 4 * kk, tmem + col_ksf(int(h)) + 4 * kk, kk > 0);
+    // S += 1 . (hi + mid + lo) of the table: the qm K^T term, exact to FP32 accumulation
+    mma_f16_ss_elect(tmem + col_s(t), dfa, sdesc_kmajor_noswz(smem_u32(S.fb[h][t]), 1024, 128),
+                     kIdescFold, 1u);
     mma_commit_elect(smem_u32(&S.bar_s[t]));
   };
   // keys [64h, 64h + 64) of a 128-key tile are bytes [32h, 32h + 32) of each V^T row
@@ -279,6 +291,23 @@ __device__ __forceinline__ void scale_factor_warps(Smem& S, const Nvfp4Args& a, 
     const uint32_t* vs = reinterpret_cast<const uint32_t*>(S.vsf[st]);
     tmem_st4(tmem + col_vsf(b) + lane_off, vs[lane * 2 + h], vs[(32 + lane) * 2 + h],
              vs[(64 + lane) * 2 + h], vs[(96 + lane) * 2 + h]);
+    // fold B tile of query tile ft: key row `key` = the table entry as three BF16 pieces
+    {
+      const int idx = cw * 32 + lane, ft = idx >> 6, key = idx & 63;
+      if (ft < wi.nq) {
+        float x = S.cq[st][ft][kSub * h + key];
+        uint32_t pc[3];
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(x);
+          pc[p] = uint32_t(__bfloat16_as_ushort(v));
+          x = x - __bfloat162float(v);  // exact: x and its BF16 rounding share the top bits
+        }
+        *reinterpret_cast<uint4*>(S.fb[b][ft] + (key >> 3) * 128 + (key & 7) * 16) =
+            make_uint4(pc[0] | (pc[1] << 16), pc[2], 0u, 0u);
+      }
+      fence_proxy_async_smem();  // the fold MMA reads the tile through the async proxy
+    }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_sf[b]));  // the MMAs of u may start
@@ -316,43 +345,34 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
     const int x = u & 1;
     if (!(ok = wait_all(&S.bar_s[t], uint32_t(u) & 1, S, a, kRoleSoftmax))) break;
     tc_fence_after();
-    uint32_t r[2][32];
-    tmem_ld32(s_addr, r[0]);
-    tmem_ld32(s_addr + 32, r[1]);
+    // S already holds the qm K^T term (the fold MMA); the loads also return the maxima of the
+    // four 16-key groups (the tensor-memory load unit reduces)
+    uint32_t r[4][16];
+    float gm[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) gm[g] = tmem_ld16_max(s_addr + 16 * g, r[g]);
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_sr[t]));  // S_t(u+1) may now overwrite S
-    // s'' = S c + the table's qm K^T term (it arrived with the key tile)
-    const int kt = u >> 1, kst = kt % kStages;
-    if (!(ok = wait_all(&S.bar_k[kst], (kt / kStages) & 1, S, a, kRoleSoftmax))) break;
+    // s'' = S c (c > 0, so the group maxima scale the same way, exactly)
     float s[64];
-    const float4* cp = reinterpret_cast<const float4*>(S.cq[kst][t] + kSub * x);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float4 cc = cp[i];
-      const int k0 = 4 * i;
-      fma2v(s[k0], s[k0 + 1], __uint_as_float(r[k0 >> 5][k0 & 31]),
-            __uint_as_float(r[k0 >> 5][(k0 + 1) & 31]), cs, cs, cc.x, cc.y);
-      fma2v(s[k0 + 2], s[k0 + 3], __uint_as_float(r[k0 >> 5][(k0 + 2) & 31]),
-            __uint_as_float(r[k0 >> 5][(k0 + 3) & 31]), cs, cs, cc.z, cc.w);
-    }
-    if (x == 1 || u + 1 == n_sub) {  // this warp is done with the stage's table rows
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.bar_free[kst]));
-    }
-    if (u == n_sub - 1 && last_valid < kSub) {
+    for (int i = 0; i < 64; i += 2)
+      fma2(s[i], s[i + 1], __uint_as_float(r[i >> 4][i & 15]),
+           __uint_as_float(r[i >> 4][(i + 1) & 15]), cs, 0.f);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) gm[g] *= cs;
+    if (u == n_sub - 1 && last_valid < kSub) {  // keys past the segment: mask, then reduce
 #pragma unroll
       for (int i = 0; i < 64; ++i)
         if (i >= last_valid) s[i] = -INFINITY;
-    }
-    // group maxima (16 keys) and row maximum of s''
-    float gm[4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float v[16];
+      for (int g = 0; g < 4; ++g) {
+        float v[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = s[16 * g + e];
-      gm[g] = max16(v);
+        for (int e = 0; e < 16; ++e) v[e] = s[16 * g + e];
+        gm[g] = max16(v);
+      }
     }
     const float mx = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
     const bool move = mx > m;  // exact running maximum
@@ -474,8 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&S.bar_k[i]), 1);
       mbar_init(smem_u32(&S.bar_v[i]), 1);
-      // MMA commits + scale-factor warps + softmax warps (they read the stage's table rows)
-      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 4 + 4 * wi.nq);
+      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 4);  // MMA commits + scale-factor warps
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&S.bar_s[t]), 1);
@@ -502,6 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&S.tmem_base), 512);
     tmem_relinquish();
   }
+  // fold operands: A rows [1, 1, 1, 0 ...] (BF16 1.0 = 0x3F80) then zeros; B zero halves
+  if (threadIdx.x < 16) {
+    const uint4 v1 = threadIdx.x < 8 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(S.fa)[threadIdx.x] = v1;
+  }
+  for (int i = threadIdx.x; i < 4 * 64; i += kThreads)
+    reinterpret_cast<uint4*>(S.fb[i >> 7][(i >> 6) & 1] + 1024)[i & 63] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

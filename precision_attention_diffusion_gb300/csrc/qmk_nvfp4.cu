@@ -5,7 +5,7 @@
 // scores. The term does not depend on the query row inside a block, so for every segment s and
 // head h it is the product of the block means and the dequantized centred keys (reading r12):
 //
-//     Tq[s][h][b][j] = (qm_b . deq(Kc_j)) * softmax_scale * log2(e)      (log2 units of S)
+//     Tq[s][h][b][j] = qm_b . deq(Kc_j)                                  (raw units of S)
 //
 // for the segment's query blocks b and its padded keys j (zero codes past the segment). The
 // attention kernel adds Tq to its scores. Layout: segment s at float offset c_off[s], then
@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
     const QmkItem* __restrict__ items, const SegInfo* __restrict__ segs,
     const int64_t* __restrict__ c_off, const float* __restrict__ qmean,
     const uint8_t* __restrict__ kcodes, const uint8_t* __restrict__ ksf, int64_t Tp,
-    int64_t nblk, int H, float cs, float* __restrict__ table, int* err) {
+    int64_t nblk, int H, float* __restrict__ table, int* err) {
   extern __shared__ uint8_t smem_raw[];
   QmkSmem& S = *reinterpret_cast<QmkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
   #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(dst + c32 + e) =
-                make_float4(__uint_as_float(r[e]) * cs, __uint_as_float(r[e + 1]) * cs,
-                            __uint_as_float(r[e + 2]) * cs, __uint_as_float(r[e + 3]) * cs);
+                make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                            __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
         }
       }
     }
@@ -229,7 +229,7 @@ int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, cudaStream_t stream) {
                      kQmkSmemBytes, stream>>>(
       p.d_qmk, p.d_segs, p.d_coff, reinterpret_cast<const float*>(ws + p.ws.q_mean),
       ws + p.ws.k_codes, ws + p.ws.k_sf, p.tpad, int64_t(p.blocks.size()), p.heads,
-      p.scale * 1.4426950408889634f, reinterpret_cast<float*>(ws + p.ws.qmk), p.d_err);
+      reinterpret_cast<float*>(ws + p.ws.qmk), p.d_err);
   return cuda_status(cudaGetLastError());
 }
 

@@ -179,6 +179,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// tcgen05.ld of 16 columns that also returns the maximum of the lane's 16 loaded values (f32).
+__device__ __forceinline__ float tmem_ld16_max(uint32_t taddr, uint32_t (&r)[16]) {
+  float mx;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, %16, [%17];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=f"(mx)
+      : "r"(taddr)
+      : "memory");
+  return mx;
+}
+
 // tcgen05.ld of 32 columns that also returns the maximum of the lane's 32 loaded values (f32),
 // a reduction the load unit performs (sm_103a); the maximum is valid after tcgen05.wait::ld.
 __device__ __forceinline__ float tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32]) {
@@ -250,6 +264,19 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
   d |= static_cast<uint64_t>(1024 >> 4) << 32;         // SBO: 8 rows * 128 bytes
   d |= static_cast<uint64_t>(1) << 46;                 // descriptor version for tcgen05
   d |= static_cast<uint64_t>(2) << 61;                 // SWIZZLE_128B
+  return d;
+}
+
+// Shared-memory descriptor, K-major operand without swizzle: core matrices of 8 rows x 16 bytes;
+// lbo = byte distance between core matrices along K, sbo = along M/N (0 repeats one group of 8
+// rows for every row group), layout code 0.
+__device__ __forceinline__ uint64_t sdesc_kmajor_noswz(uint32_t smem_addr, uint32_t lbo,
+                                                       uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
 

@@ -10,8 +10,8 @@
 //
 // What one CTA computes (readings r5 with tau = 0, r9, r11, r12): for the two 128-row query tiles
 // Q0, Q1 of one (segment, head), over 64-key sub-tiles u from the segment start,
-//   s''(i, j)  = (deq(Qc_i) . deq(Kc_j)) c + Tq_t(j),  Tq_t(j) = (qm_t . deq(Kc_j)) c (the
-//                table qmk_nvfp4.cu writes during quantization),
+//   s''(i, j)  = (deq(Qc_i) . deq(Kc_j) + Tq_t(j)) c,  Tq_t(j) = qm_t . deq(Kc_j) (the table
+//                qmk_nvfp4.cu writes during quantization, added to S by a BF16 MMA),
 //                with c = softmax_scale log2(e)            (log2 units)
 //   m_i        = running row maximum of s'' (exact: it moves whenever a sub-tile exceeds it)
 //   P'(i, j)   = 2^(s'' - m_i + log2 2688)                  (= 2688 exp(S' - m) of the pages)
@@ -28,15 +28,19 @@
 //               a 4-stage ring;
 //   warps 9/10  MMA issue for query tile 0/1 (tensor memory allocated by warp 9):
 //                 S_t(u)  = deq(Qc_t) deq(Kc(u))^T   2 MMAs M=128 N=64  K=64, A, B in smem
+//                 S_t(u) += 1 Tq_t(u)^T              1 kind::f16 MMA  M=128 N=64 K=16 (A =
+//                                                    rows [1, 1, 1, 0...], B = the table
+//                                                    entries as three BF16 pieces)
 //                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=128 K=64, A = P in TMEM
 //   warps 11-14 per sub-tile: K and V scale factors into tensor memory (the MMA reads the B-side
 //               scales of row n from column n / 32 of every lane quarter, so each of the four
-//               warps writes its own quarter);
+//               warps writes its own quarter), and the BF16 pieces of the table entries;
 //   warps 0-7   softmax of tile 0 (warps 0-3) and 1 (warps 4-7), one thread per query row (row ==
-//               tensor-memory lane); P codes and P scales go to tensor memory (A-side scales: row
-//               r in lane r, column r / 32), O is rescaled in tensor memory when a row's maximum
+//               tensor-memory lane); S and the maxima of its 16-key groups come from
+//               tcgen05.ld.red; P codes and P scales go to tensor memory (A-side scales: row r in
+//               lane r, column r / 32), O is rescaled in tensor memory when a row's maximum
 //               moves, and the same threads run the epilogue.
-// Tensor memory (512 columns): per query tile t a 64-column S, two P slots (8 columns of codes
+// Tensor memory (488 of 512 columns): per query tile t a 64-column S, two P slots (8 columns of codes
 // and 4 of scales each) and a 128-column O; then Q, K (two buffers) and V (two buffers) scale
 // blocks. Every barrier wait is bounded; on expiry the kernel records an error, drains its
 // in-flight copies and MMAs, frees its tensor memory and returns.

@@ -51,10 +51,10 @@ KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5}
 # an ncu capture of the full-size workload (profiles/attn_traffic_s30272_h56.md), keyed by the
 # workload and the SHA-256 of the kernel source at capture time (null once the kernel changed).
 NCU_TRAFFIC = {
-    ("fp8_s30272_h56", "477a3a0bd384a21293607f7b92bde901f4d9f3e5e755fddca8c4d1e8fb611690"):
-        2.12e9 + 425.24e6,
-    ("nvfp4_s30272_h56", "f6a361be72e9c338d50c9168ffec701aa8fbacfaac1ac073329a484f014e965e"):
-        2.39e9 + 425.11e6,
+    ("fp8_s30272_h56", "b3ec608431527b6576bff057ae9e00b5dfc55dccc13fc677003b0a9df411bbb5"):
+        1.93e9 + 425.50e6,
+    ("nvfp4_s30272_h56", "d9f3e7577e08e5f2aa13488b40f1f1da145b25a9d930d1546be188a0a3140ac0"):
+        2.38e9 + 425.02e6,
 }
 
 

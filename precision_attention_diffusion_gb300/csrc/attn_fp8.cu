@@ -8,22 +8,32 @@
 //
 // GB300 design (the SM120 kernel's 128x32 mma.sync tile is prior art, not the blueprint):
 //   * one CTA = one (segment, head) and two 128-row query tiles Q0, Q1 sharing every K/V tile;
-//   * warp 8 issues TMA loads: Q once, then 128-key K and V^T tiles into a 4-stage ring with
+//   * warp 16 issues TMA loads: Q once, then 128-key K and V^T tiles into a 4-stage ring with
 //     128-byte swizzle;
-//   * warp 9 allocates tensor memory; warps 9 and 10 issue the tcgen05.mma kind::f8f6f4 of query
-//     tiles 0 and 1 (two independent in-order streams) on 64-key sub-tiles u:
+//   * warp 17 allocates tensor memory; warps 17 and 18 issue the tcgen05.mma kind::f8f6f4 of query
+//     tiles 0 and 1 (two independent in-order streams) on 64-key sub-tiles u, one elect.sync per
+//     group of MMAs and its commit:
 //       S_t(u) = Q_t K(u)^T   (M=128, N=64;  A, B from shared memory)
 //       O_t += P_t(u) V(u)    (M=128, N=128; A = P_t from tensor memory)
 //   * tensor memory (all 512 columns): per query tile two 64-column S buffers and a 128-column O;
 //     P_t(u) (64 E4M3 per row = 16 columns) is written over the S buffer it was computed from, and
 //     S_t(u+2) is issued into that buffer right after PV_t(u), so S is always one sub-tile ahead
 //     of the softmax;
-//   * warps 0-3 / 4-7 run the online softmax of Q0 / Q1, one thread per query row (row == TMEM
-//     lane). The reference maximum m is the first sub-tile's maximum and moves to a later
-//     sub-tile's maximum M only when (M - m) c > 8 (reading r5 with tau = 8; the pages leave the
-//     rule open): alpha = 2^((m - M) c), O *= alpha (only when a row of the warp moved),
-//     P = E4M3(2^(S c - m c)) <= 256, l = l alpha + sum of the quantized P (reading r6),
-//     where S is the raw E4M3 dot product and c = dq dk softmax_scale log2(e);
+//   * warps 0-7 / 8-15 run the online softmax of Q0 / Q1, two threads per query row: with the
+//     16x32bx2 tensor-memory shapes, warp w of a tile covers the 16 rows (lanes) 32 (w & 3) +
+//     16 (w >> 2) + [0, 16), thread t and t ^ 16 of the warp holding keys [0, 32) and [32, 64)
+//     of the row's sub-tile (and channels [0, 64) and [64, 128) of its O); the load returns each
+//     half's maximum and one shuffle combines the halves. Four softmax warps per SM
+//     sub-partition hide each other's MUFU and tensor-memory latencies. The reference maximum m
+//     is the first sub-tile's maximum and moves to a later sub-tile's maximum M only when
+//     (M - m) c > 8 (reading r5 with tau = 8; the pages leave the rule open): alpha =
+//     2^((m - M) c), O *= alpha (only when a row of the warp moved), P = E4M3(2^(S c - m c)) <=
+//     256, l = l alpha + sum of the quantized P (reading r6; each thread sums its half, the
+//     halves are added at the end), where S is the raw E4M3 dot product and c = dq dk
+//     softmax_scale log2(e);
+//   * steady-state waits first park the warp in hardware (try_wait with a suspend-time hint) so
+//     that waiting warps take no issue slots from the warps they share a scheduler with; warp 19
+//     has no role (the 20-warp block keeps the register budget at 96 per thread);
 //   * epilogue: out = BF16_rn(O dv / l) for rows inside the segment only.
 // Every barrier wait is bounded; on expiry the kernel records an error, drains its in-flight
 // copies and MMAs, frees its tensor memory and returns.
@@ -37,9 +47,9 @@ namespace falp {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 352;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;   // warps 9 and 10 issue the MMAs of query tiles 0 and 1
+constexpr int kThreads = 640;   // 20 warps: 16 softmax, TMA, 2 MMA, one idle (see the header)
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;    // warps 17 and 18 issue the MMAs of query tiles 0 and 1
 constexpr int kSub = 64;                            // keys per sub-tile
 constexpr uint32_t kTileBytes = 128 * 128;          // one 128x128 E4M3 tile
 constexpr uint32_t kIdescS = idesc_f8f6f4(128, kSub, 0, 0);   // E4M3 x E4M3 -> F32, N=64
@@ -47,6 +57,7 @@ constexpr uint32_t kIdescPV = idesc_f8f6f4(128, 128, 0, 0);   // N = 128 channel
 constexpr uint32_t kProbeNs = 100000;         // one parked probe: at most ~100 us
 constexpr int kSpinProbes = 64;                 // plain probes before parking
 constexpr long long kDrainProbes = 20000;      // drains give up after ~2 s
+constexpr uint32_t kHintNs = 20000;           // first probe of a steady-state wait: park up to 20 us
 // Threshold (log2 units) by which a sub-tile's maximum must exceed the reference maximum before
 // the reference moves (and O, l are rescaled). P = 2^(S c - m c) <= 2^kTau stays inside E4M3.
 constexpr float kTau = 8.0f;
@@ -131,6 +142,15 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Smem& 
   return wait_phase_slow(bar, parity, S, a, role);
 }
 
+// Warp-uniform wait of the steady state: one probe that parks the warp in hardware until the phase
+// completes (or kHintNs passes), so that a waiting warp takes no issue slots from the warps it
+// shares a scheduler with; then the bounded wait.
+__device__ __forceinline__ bool wait_hinted(uint32_t bar, uint32_t parity, Smem& S,
+                                            const AttnArgs& a, int role) {
+  if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kHintNs))) return true;
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, S, a, role)) != 0;
+}
+
 // Wait used while draining after an abort: ignores the abort flag, bounded separately.
 __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity) {
   for (long long n = 0; n < kDrainProbes; ++n)
@@ -152,8 +172,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
   for (int j = 0; j < n_kv; ++j) {
     const int st = j % kStages;
     if (j >= kStages &&
-        !__all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_free[st]), ((j / kStages) - 1) & 1,
-                                            S, a, kRoleProducer)))
+        !wait_hinted(smem_u32(&S.bar_free[st]), ((j / kStages) - 1) & 1, S, a, kRoleProducer))
       break;
     const int row = sg.row0 + j * kTile;
     mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]), kTileBytes);
@@ -190,10 +209,7 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const Wor
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
     const uint64_t kb = dk + (((j % kStages) * kTileBytes + h * (kSub * 128)) >> 4);
     const uint32_t d = tmem + col_s(t, h);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f8f6f4_ss_elect(d, dq + 2 * kk, kb + 2 * kk, kIdescS, kk > 0);
-    mma_commit_elect(smem_u32(&S.bar_s[t][h]));
+    mma_f8f6f4_ss_k128_commit_elect(d, dq, kb, kIdescS, smem_u32(&S.bar_s[t][h]));
   };
   // O_t += P_t(u) V(u): keys [64h, 64h + 64) are bytes [64h, 64h + 64) of each V^T row; P from
   // the first 16 columns of S buffer h
@@ -201,13 +217,11 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const Wor
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
     const uint64_t vb = dvv + (((j % kStages) * kTileBytes + h * kSub) >> 4);
     const uint32_t pa = tmem + col_s(t, h);
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-      mma_f8f6f4_ts_elect(d_o, pa + 8 * kk, vb + 2 * kk, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
-    mma_commit_elect(smem_u32(&S.bar_o[t][h]));
+    mma_f8f6f4_ts_k64_commit_elect(d_o, pa, vb, kIdescPV, u > 0 ? 1u : 0u,
+                                   smem_u32(&S.bar_o[t][h]));
   };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, wait_phase(smem_u32(bar), parity, S, a, kRoleMma));
+    return wait_hinted(smem_u32(bar), parity, S, a, kRoleMma);
   };
   do {
     if (!wait(&S.bar_q, 0)) break;
@@ -251,76 +265,73 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
   const int h = wi.head;
   const float c = a.descale[h] * a.descale[a.H + h] * a.scale_log2;
   const float dv = a.descale[2 * a.H + h];
-  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  // warp wq (0..7) of the tile: lane quarter wq & 3, half wq >> 2; the row is shared by threads
+  // lane and lane ^ 16, which hold keys [0, 32) and [32, 64) of every sub-tile
+  const int rbase = 32 * (wq & 3) + 16 * (wq >> 2);
+  const int kh = lane >> 4;
+  const uint32_t lane_off = uint32_t(rbase) << 16;
   const uint32_t o_addr = tmem + col_o(t) + lane_off;
   const int last_valid = sg.len - (n_sub - 1) * kSub;  // keys of the last sub-tile, 1..64
-  float m = -INFINITY, l = 0.f;                         // reference maximum (raw units), sum
+  float m = -INFINITY, l = 0.f;                         // reference maximum, this half's sum
   bool ok = true;
   for (int u = 0; u < n_sub; ++u) {
     const int b = u & 1;
     const uint32_t s_addr = tmem + col_s(t, b) + lane_off;
-    ok = __all_sync(0xffffffffu,
-                    wait_phase(smem_u32(&S.bar_s[t][b]), (u >> 1) & 1, S, a, kRoleSoftmax));
+    ok = wait_hinted(smem_u32(&S.bar_s[t][b]), (u >> 1) & 1, S, a, kRoleSoftmax);
     if (!ok) break;
     tc_fence_after();
-    // the loads also return each half's maximum (the tensor-memory load unit reduces)
-    uint32_t r[2][32];
-    const float mx0 = tmem_ld32_max(s_addr, r[0]);
-    const float mx1 = tmem_ld32_max(s_addr + 32, r[1]);
+    uint32_t r[32];
+    const float mxh = tmem_ld32x2_max<32>(s_addr, r);
     tmem_wait_ld();
-    float s[64];
+    float s[32];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i >> 5][i & 31]);
-    float mx = fmaxf(mx0, mx1);
+    for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+    float mx = mxh;
     if (u == n_sub - 1 && last_valid < kSub) {  // keys past the segment: mask, then reduce
+      mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i >= last_valid) s[i] = -INFINITY;
-      mx = row_max64(s);
+      for (int i = 0; i < 32; ++i) {
+        if (32 * kh + i >= last_valid) s[i] = -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
     }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const bool move = (m == -INFINITY) || ((mx - m) * c > kTau);
     const float m_new = move ? mx : m;
     const float alpha = move ? ex2_approx((m - m_new) * c) : 1.f;  // m = -inf gives 0
     const float nmc = -m_new * c;
-    uint32_t pk[16];
-    float rs = 0.f;
+    uint32_t pk[8];
+    uint32_t hs[8];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {  // 32 keys per group
-      uint32_t hs[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {  // 4 keys
-        const int k0 = 32 * g + 4 * i;
-        float x0, x1, x2, x3;
-        fma2(x0, x1, s[k0], s[k0 + 1], c, nmc);
-        fma2(x2, x3, s[k0 + 2], s[k0 + 3], c, nmc);
-        const uint16_t c01 = cvt_e4m3x2(ex2_approx(x0), ex2_approx(x1));
-        const uint16_t c23 = cvt_e4m3x2(ex2_approx(x2), ex2_approx(x3));
-        pk[8 * g + i] = uint32_t(c01) | (uint32_t(c23) << 16);
-        // the quantized values, back in f16 (exact), summed pairwise (reading r6: l sums the
-        // quantized P)
-        hs[i] = hadd2_u32(cvt_e4m3x2_to_f16x2(c01), cvt_e4m3x2_to_f16x2(c23));
-      }
-      const uint32_t h8 = hadd2_u32(hadd2_u32(hadd2_u32(hs[0], hs[1]), hadd2_u32(hs[2], hs[3])),
-                                    hadd2_u32(hadd2_u32(hs[4], hs[5]), hadd2_u32(hs[6], hs[7])));
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h8));
-      rs += f.x + f.y;
+    for (int i = 0; i < 8; ++i) {  // 4 keys
+      float x0, x1, x2, x3;
+      fma2(x0, x1, s[4 * i], s[4 * i + 1], c, nmc);
+      fma2(x2, x3, s[4 * i + 2], s[4 * i + 3], c, nmc);
+      const uint16_t c01 = cvt_e4m3x2(ex2_approx(x0), ex2_approx(x1));
+      const uint16_t c23 = cvt_e4m3x2(ex2_approx(x2), ex2_approx(x3));
+      pk[i] = uint32_t(c01) | (uint32_t(c23) << 16);
+      // the quantized values, back in f16 (exact), summed pairwise (reading r6)
+      hs[i] = hadd2_u32(cvt_e4m3x2_to_f16x2(c01), cvt_e4m3x2_to_f16x2(c23));
     }
-    l = l * alpha + rs;
-    tmem_st16(s_addr, pk);  // P over the first 16 columns of the S buffer just read
+    const uint32_t h8 = hadd2_u32(hadd2_u32(hadd2_u32(hs[0], hs[1]), hadd2_u32(hs[2], hs[3])),
+                                  hadd2_u32(hadd2_u32(hs[4], hs[5]), hadd2_u32(hs[6], hs[7])));
+    const float2 fs = __half22float2(*reinterpret_cast<const __half2*>(&h8));
+    l = l * alpha + (fs.x + fs.y);
+    tmem_st8x2<8>(s_addr, pk);  // P over the first 16 columns of the S buffer just read
     if (u > 0 && __any_sync(0xffffffffu, move)) {
-      // rescale O between PV_t(u-1) and PV_t(u)
+      // rescale O between PV_t(u-1) and PV_t(u): this thread's 64 channels
       ok = __all_sync(0xffffffffu, wait_phase(smem_u32(&S.bar_o[t][b ^ 1]), ((u - 1) >> 1) & 1,
                                               S, a, kRoleSoftmax));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         uint32_t o[32];
-        tmem_ld32(o_addr + 32 * i, o);
+        tmem_ld32x2<64>(o_addr + 32 * i, o);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-        tmem_st32(o_addr + 32 * i, o);
+        tmem_st32x2<64>(o_addr + 32 * i, o);
       }
     }
     tmem_wait_st();
@@ -337,17 +348,19 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
                                           ((n_sub - 1) >> 1) & 1, S, a, kRoleEpilogue));
   if (!ok) return;
   tc_fence_after();
+  l += __shfl_xor_sync(0xffffffffu, l, 16);
   const float f = dv / l;
-  const int qrow = (wi.qt0 + t) * kTile + wq * 32 + lane;
+  const int qrow = (wi.qt0 + t) * kTile + rbase + (lane & 15);
   const bool valid = qrow < sg.len;
   // LSE in the units of S = q.k scale: m c (log2 units) + log2(l), times ln 2
-  if (a.lse && valid)
+  if (a.lse && valid && kh == 0)
     a.lse[int64_t(h) * a.lse_sh + sg.tok0 + qrow] = (m * c + log2f(l)) * 0.6931471805599453f;
-  __nv_bfloat16* dst = a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(h) * a.osh;
+  // this thread's channels: [0, 64) (kh = 0) or [64, 128) (kh = 1)
+  __nv_bfloat16* dst = a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(h) * a.osh + 64 * kh;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
     uint32_t o[32];
-    tmem_ld32(o_addr + 32 * i, o);
+    tmem_ld32x2<64>(o_addr + 32 * i, o);
     tmem_wait_ld();
     uint32_t w[16];
 #pragma unroll
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       for (int x = 0; x < 2; ++x) {
         mbar_init(smem_u32(&S.bar_s[t][x]), 1);
-        mbar_init(smem_u32(&S.bar_p[t][x]), 128);
+        mbar_init(smem_u32(&S.bar_p[t][x]), 256);
         mbar_init(smem_u32(&S.bar_o[t][x]), 1);
       }
       mbar_init(smem_u32(&S.bar_drain[t]), 1);
@@ -410,12 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     producer(&tm_q, &tm_k, &tm_v, S, a, wi, sg);
-  } else if (warp >= kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     const int t = warp - kMmaWarp;
     if (t < wi.nq) mma_issuer(S, a, wi, sg, tmem, t);
-  } else {
-    const int t = warp >> 2;
-    if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 3, lane);
+  } else if (warp < 16) {
+    const int t = warp >> 3;
+    if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 7, lane);
   }
   tc_fence_before();
   __syncthreads();

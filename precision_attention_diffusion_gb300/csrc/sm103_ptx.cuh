@@ -249,6 +249,60 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
       : "memory");
 }
 
+// 16x32bx2 shapes (two threads per tensor-memory lane): thread t of the warp accesses lane
+// (taddr lane) + (t & 15); threads 0-15 use columns [col, col + n), threads 16-31 columns
+// [col + kSplit, col + kSplit + n). Established by a GB300 probe for ld, ld.red and st.
+#define FALP_OUT32(r)                                                                           \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), \
+      "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),  \
+      "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), \
+      "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), \
+      "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define FALP_IN32(r)                                                                            \
+  "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),         \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),          \
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),        \
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),        \
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+#define FALP_LIST32 \
+  "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}"
+
+// 32 columns per thread with, as the second result, this thread's maximum of the 32 values.
+template <int kSplit>
+__device__ __forceinline__ float tmem_ld32x2_max(uint32_t taddr, uint32_t (&r)[32]) {
+  float mx;
+  asm volatile("tcgen05.ld.red.sync.aligned.16x32bx2.x32.max.f32 " FALP_LIST32 ", %32, [%33], %34;"
+               : FALP_OUT32(r), "=f"(mx)
+               : "r"(taddr), "n"(kSplit)
+               : "memory");
+  return mx;
+}
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x32.b32 " FALP_LIST32 ", [%32], %33;"
+               : FALP_OUT32(r)
+               : "r"(taddr), "n"(kSplit)
+               : "memory");
+}
+template <int kSplit>
+__device__ __forceinline__ void tmem_st32x2(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};"
+      ::"r"(taddr), "n"(kSplit), FALP_IN32(r)
+      : "memory");
+}
+template <int kSplit>
+__device__ __forceinline__ void tmem_st8x2(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9};"
+               ::"r"(taddr), "n"(kSplit), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]),
+               "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+#undef FALP_OUT32
+#undef FALP_IN32
+#undef FALP_LIST32
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05.mma descriptors
 // ------------------------------------------------------------------------------------------------
@@ -345,6 +399,46 @@ __device__ __forceinline__ void mma_f8f6f4_ts_elect(uint32_t d_tmem, uint32_t a_
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One elected lane issues a whole K = 128 contraction of E4M3 operands in shared memory (four
+// K = 32 MMAs; each K step moves both K-major descriptors by 32 bytes = 2 in the start-address
+// field), the first overwriting D, then the commit of the four to `bar`. One elect.sync per group
+// keeps the issuing warp's instruction count (and its cost to the warps it shares a scheduler
+// with) low.
+__device__ __forceinline__ void mma_f8f6f4_ss_k128_commit_elect(uint32_t d_tmem, uint64_t adesc,
+                                                                uint64_t bdesc, uint32_t idesc,
+                                                                uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %3, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %3, p1;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(bar)
+      : "memory");
+}
+
+// Same for a K = 64 contraction with A (E4M3) in tensor memory: two K = 32 MMAs (A moves by 8
+// columns = 32 bytes per row, B by 32 bytes), the first accumulating only if `accumulate`.
+__device__ __forceinline__ void mma_f8f6f4_ts_k64_commit_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                               uint64_t bdesc, uint32_t idesc,
+                                                               uint32_t accumulate, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 b1;\n\t.reg .b32 a1;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\tadd.s64 b1, %2, 2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %3, p1;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(bar)
       : "memory");
 }
 

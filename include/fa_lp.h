@@ -188,6 +188,42 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
                     int64_t out_stride_tok, int64_t out_stride_head, void* stream);
 
 /*
+ * fa_lp_attention_host -- the one-call form from and to host memory: copies Q, K and V to the
+ * device, quantizes, runs the attention and copies the output back. The heads are processed in
+ * chunks, and the copy-in of chunk c+1, the quantize + attention of chunk c and the copy-out of
+ * chunk c-1 overlap on three streams. Every step of the path is independent per head (the FP8
+ * scales are per (tensor, head), the NVFP4 means and scales per head), so the result equals
+ * fa_lp_attention on the same data bit for bit. The chunked schedule is this library's own
+ * design; the operation is the one of fa_lp_attention (FlashInfer docs,
+ * minimax_h3_sm120_varlen_attention_nvfp4, Parameters and description).
+ *   q, k, v         : host pointers, BF16 [tokens, heads, 128] with element strides (tok, head),
+ *                     channels contiguous, 16-byte aligned, strides multiples of 8 (as the device
+ *                     form). Page-locked memory (cudaHostAlloc / cudaHostRegister) lets the
+ *                     copies overlap the compute; pageable memory is accepted, the copies then
+ *                     serialise with it.
+ *   out             : host pointer, BF16 [tokens, heads, 128] with element strides; every row
+ *                     (all tokens lie in a segment) is written. Caller-owned.
+ *   heads_per_chunk : 1..heads, or 0 for the library's choice (4 to 8 chunks whose CTAs fill the
+ *                     GPU's waves best).
+ *   stream          : the quantize and attention kernels run on it; the copies run on two
+ *                     streams of the plan, ordered after the work already on `stream`, and
+ *                     `stream` is ordered after the last copy-out: once `stream` completes, `out`
+ *                     holds the result. Returns after enqueueing.
+ * Device memory: two chunk slots of Q, K, V and output (8 x tokens x heads_per_chunk x 256
+ * bytes), allocated on the first call (or a call with another chunk size) and kept by the plan,
+ * plus the workspace of plans of heads_per_chunk heads (cached like any plan). Device-side wait
+ * expiries are reported by fa_lp_get_last_error on this plan. A plan must not run this call
+ * from two host threads at once.
+ * Errors: INVALID_ARG (null or misaligned view, heads_per_chunk out of range, wrong device),
+ * UNSUPPORTED, OOM, CUDA.
+ */
+FA_LP_API int fa_lp_attention_host(fa_lp_plan* plan, const void* q, int64_t q_stride_tok,
+                                   int64_t q_stride_head, const void* k, int64_t k_stride_tok,
+                                   int64_t k_stride_head, const void* v, int64_t v_stride_tok,
+                                   int64_t v_stride_head, void* out, int64_t out_stride_tok,
+                                   int64_t out_stride_head, int heads_per_chunk, void* stream);
+
+/*
  * Inspection of the quantized operands (for bit-exact tests). `which` selects one array of the
  * workspace; the descriptor gives its device address and layout. Valid until the next call that
  * may grow the workspace.

@@ -135,6 +135,79 @@ bool bad_view(const void* ptr, int64_t st, int64_t sh) {
   return false;
 }
 
+// ---- host-buffer pipeline ------------------------------------------------------------------------
+// Copy heads [h0, h0 + n) of a BF16 [T, H, 128] view (element strides st, sh) into or out of a
+// dense [T, n, 128] device buffer: one 2D copy when the heads are adjacent, else one per head.
+cudaError_t copy_heads(void* dst, int64_t dst_st, int64_t dst_sh, const void* src, int64_t src_st,
+                       int64_t src_sh, int64_t T, int n, cudaMemcpyKind kind, cudaStream_t s) {
+  const size_t row = size_t(FA_LP_HEAD_DIM) * 2;
+  if (dst_sh == FA_LP_HEAD_DIM && src_sh == FA_LP_HEAD_DIM)
+    return cudaMemcpy2DAsync(dst, size_t(dst_st) * 2, src, size_t(src_st) * 2, row * n, size_t(T),
+                             kind, s);
+  for (int h = 0; h < n; ++h) {
+    const cudaError_t e = cudaMemcpy2DAsync(
+        static_cast<uint8_t*>(dst) + size_t(h) * dst_sh * 2, size_t(dst_st) * 2,
+        static_cast<const uint8_t*>(src) + size_t(h) * src_sh * 2, size_t(src_st) * 2, row,
+        size_t(T), kind, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Heads per chunk when the caller leaves it open: 4 to 8 chunks, the split whose chunks fill the
+// GPU's waves of CTAs best (ties: more chunks, so that the first copy-in and the last copy-out,
+// which nothing overlaps, are shorter).
+int default_heads_per_chunk(const fa_lp_plan& p) {
+  const int H = p.heads;
+  if (H < 4) return 1;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess ||
+      sms <= 0) {
+    cudaGetLastError();
+    sms = 152;
+  }
+  const double cph = double(p.work.size()) / H;  // CTAs per head
+  int best = (H + 3) / 4;
+  double best_eff = -1.0;
+  for (int nh = 1; nh <= H; ++nh) {
+    const int nc = (H + nh - 1) / nh;
+    if (nc < 4 || nc > 8) continue;
+    double ctas = 0.0, slots = 0.0;
+    for (int h0 = 0; h0 < H; h0 += nh) {
+      const double c = cph * std::min(nh, H - h0);
+      ctas += c;
+      slots += std::ceil(c / sms) * sms;
+    }
+    const double eff = slots > 0 ? ctas / slots : 0.0;
+    if (eff > best_eff + 1e-9 || (std::fabs(eff - best_eff) <= 1e-9 && nh < best)) {
+      best_eff = eff;
+      best = nh;
+    }
+  }
+  return best;
+}
+
+// Free the pipeline's device buffer, streams and events (device already current); hands the
+// sub-plans to the caller, which releases them outside the plan-cache lock.
+int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[2]) {
+  falp::HostPipe& hp = p->host;
+  int st = FA_LP_OK;
+  if (hp.s_in && cudaStreamSynchronize(hp.s_in) != cudaSuccess) st = FA_LP_ERR_CUDA;
+  if (hp.s_out && cudaStreamSynchronize(hp.s_out) != cudaSuccess) st = FA_LP_ERR_CUDA;
+  if (hp.buf && cudaFree(hp.buf) != cudaSuccess) st = FA_LP_ERR_CUDA;
+  for (cudaEvent_t* e : {&hp.start, &hp.end, &hp.in_done[0], &hp.in_done[1], &hp.in_free[0],
+                         &hp.in_free[1], &hp.out_ready[0], &hp.out_ready[1], &hp.out_free[0],
+                         &hp.out_free[1]})
+    if (*e) cudaEventDestroy(*e);
+  if (hp.s_in) cudaStreamDestroy(hp.s_in);
+  if (hp.s_out) cudaStreamDestroy(hp.s_out);
+  subs[0] = hp.sub[0];
+  subs[1] = hp.sub[1];
+  hp = falp::HostPipe();
+  if (st != FA_LP_OK) cudaGetLastError();
+  return st;
+}
+
 void build_plan(fa_lp_plan* p) {
   const int ns = p->nseg;
   p->row_off.assign(ns + 1, 0);
@@ -343,21 +416,29 @@ int fa_lp_plan_create(int64_t tokens, int heads, const int32_t* cu, int num_segm
 
 int fa_lp_plan_destroy(fa_lp_plan* p) {
   if (!p) return FA_LP_OK;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (--p->refcount > 0) return FA_LP_OK;
-  g_plans.erase(key_of(*p));
+  fa_lp_plan* subs[2] = {nullptr, nullptr};
   int st = FA_LP_OK;
-  if (p->dmeta) {
-    int cur = -1;
-    cudaGetDevice(&cur);
-    if (cur != p->device) cudaSetDevice(p->device);
-    if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dmeta) != cudaSuccess) {
-      cudaGetLastError();
-      st = FA_LP_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (--p->refcount > 0) return FA_LP_OK;
+    g_plans.erase(key_of(*p));
+    if (p->dmeta || p->host.buf || p->host.s_in) {
+      int cur = -1;
+      cudaGetDevice(&cur);
+      if (cur != p->device) cudaSetDevice(p->device);
+      st = host_pipe_release(p, subs);
+      if (p->dmeta &&
+          (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dmeta) != cudaSuccess)) {
+        cudaGetLastError();
+        st = FA_LP_ERR_CUDA;
+      }
+      if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     }
-    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    delete p;
   }
-  delete p;
+  // the sub-plans of the host pipeline are plans of the cache like any other (never p itself)
+  for (fa_lp_plan* sp : subs)
+    if (sp && sp != p) fa_lp_plan_destroy(sp);
   return st;
 }
 
@@ -454,6 +535,125 @@ int fa_lp_attention(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, cons
   return fa_lp_forward_varlen(p, cu_seqlens_dev, out, ost, osh, stream);
 }
 
+int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
+                         int64_t kst, int64_t ksh, const void* v, int64_t vst, int64_t vsh,
+                         void* out, int64_t ost, int64_t osh, int heads_per_chunk,
+                         void* stream_) {
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  if (heads_per_chunk < 0 || heads_per_chunk > p->heads) return FA_LP_ERR_INVALID_ARG;
+  if (p->tokens > 0 && (bad_view(q, qst, qsh) || bad_view(k, kst, ksh) || bad_view(v, vst, vsh) ||
+                        bad_view(out, ost, osh)))
+    return FA_LP_ERR_INVALID_ARG;
+  int st = check_current_device(p);
+  if (st != FA_LP_OK) return st;
+  if (p->tokens == 0) return FA_LP_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const int H = p->heads;
+  const int nh = heads_per_chunk ? heads_per_chunk : default_heads_per_chunk(*p);
+  const int64_t T = p->tokens;
+  falp::HostPipe& hp = p->host;
+  if (hp.nh != nh) {  // (re)build the pipeline for this chunk size
+    fa_lp_plan* old[2] = {nullptr, nullptr};
+    st = host_pipe_release(p, old);
+    for (fa_lp_plan* sp : old)
+      if (sp) fa_lp_plan_destroy(sp);
+    if (st != FA_LP_OK) return st;
+    const size_t bytes = size_t(8) * size_t(T) * size_t(nh) * FA_LP_HEAD_DIM * 2;
+    if (cudaMalloc(&hp.buf, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      hp.buf = nullptr;
+      return FA_LP_ERR_OOM;
+    }
+    bool ok = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* e : {&hp.start, &hp.end, &hp.in_done[0], &hp.in_done[1], &hp.in_free[0],
+                           &hp.in_free[1], &hp.out_ready[0], &hp.out_ready[1], &hp.out_free[0],
+                           &hp.out_free[1]})
+      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    // chunks of fewer heads than the plan run on plans of their own (a chunk of all the heads
+    // runs on this plan: a plan never holds itself)
+    for (int i = 0; i < 2 && ok; ++i) {
+      const int n = i == 0 ? nh : H % nh;
+      if (n == 0 || n == H) continue;
+      ok = fa_lp_plan_create(T, n, p->cu.data(), p->nseg, p->scale, p->mode, p->device,
+                             &hp.sub[i]) == FA_LP_OK;
+      ok = ok && hp.sub[i] != p;
+    }
+    hp.nh = nh;
+    if (!ok) {
+      cudaGetLastError();
+      host_pipe_release(p, old);
+      for (fa_lp_plan* sp : old)
+        if (sp) fa_lp_plan_destroy(sp);
+      return FA_LP_ERR_CUDA;
+    }
+  }
+  for (fa_lp_plan* sp : hp.sub)
+    if (sp) sp->spin_limit = p->spin_limit;
+  const size_t tb = size_t(T) * size_t(nh) * FA_LP_HEAD_DIM * 2;  // one tensor of one slot
+  uint8_t* base = static_cast<uint8_t*>(hp.buf);
+  auto dev = [&](int slot, int which) { return base + (size_t(slot) * 4 + which) * tb; };
+  auto ok_ = [](cudaError_t e) { return e == cudaSuccess; };
+  // the copies start after the work already on `stream` (which may still use the slots)
+  if (!ok_(cudaEventRecord(hp.start, stream)) || !ok_(cudaStreamWaitEvent(hp.s_in, hp.start, 0)) ||
+      !ok_(cudaStreamWaitEvent(hp.s_out, hp.start, 0))) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  const int nchunks = (H + nh - 1) / nh;
+  for (int c = 0; c < nchunks; ++c) {
+    const int h0 = c * nh, n = std::min(nh, H - h0), slot = c & 1;
+    fa_lp_plan* sp = (n == H) ? p : (n == nh) ? hp.sub[0] : hp.sub[1];
+    const int64_t dst = int64_t(n) * FA_LP_HEAD_DIM, dsh = FA_LP_HEAD_DIM;  // dense [T, n, 128]
+    const uint8_t* hq = static_cast<const uint8_t*>(q) + size_t(h0) * qsh * 2;
+    const uint8_t* hk = static_cast<const uint8_t*>(k) + size_t(h0) * ksh * 2;
+    const uint8_t* hv = static_cast<const uint8_t*>(v) + size_t(h0) * vsh * 2;
+    uint8_t* ho = static_cast<uint8_t*>(out) + size_t(h0) * osh * 2;
+    // copy-in of chunk c once the quantize of chunk c - 2 has consumed the slot
+    bool good = (c < 2 || ok_(cudaStreamWaitEvent(hp.s_in, hp.in_free[slot], 0))) &&
+                ok_(copy_heads(dev(slot, 0), dst, dsh, hq, qst, qsh, T, n,
+                               cudaMemcpyHostToDevice, hp.s_in)) &&
+                ok_(copy_heads(dev(slot, 1), dst, dsh, hk, kst, ksh, T, n,
+                               cudaMemcpyHostToDevice, hp.s_in)) &&
+                ok_(copy_heads(dev(slot, 2), dst, dsh, hv, vst, vsh, T, n,
+                               cudaMemcpyHostToDevice, hp.s_in)) &&
+                ok_(cudaEventRecord(hp.in_done[slot], hp.s_in)) &&
+                ok_(cudaStreamWaitEvent(stream, hp.in_done[slot], 0));
+    if (!good) {
+      cudaGetLastError();
+      return FA_LP_ERR_CUDA;
+    }
+    // quantize and attention of chunk c on the caller's stream
+    st = fa_lp_quantize(sp, dev(slot, 0), dst, dsh, dev(slot, 1), dst, dsh, dev(slot, 2), dst, dsh,
+                        stream);
+    if (st != FA_LP_OK) return st;
+    good = ok_(cudaEventRecord(hp.in_free[slot], stream)) &&
+           (c < 2 || ok_(cudaStreamWaitEvent(stream, hp.out_free[slot], 0)));
+    if (!good) {
+      cudaGetLastError();
+      return FA_LP_ERR_CUDA;
+    }
+    st = fa_lp_forward_varlen(sp, nullptr, dev(slot, 3), dst, dsh, stream);
+    if (st != FA_LP_OK) return st;
+    // copy-out of chunk c
+    good = ok_(cudaEventRecord(hp.out_ready[slot], stream)) &&
+           ok_(cudaStreamWaitEvent(hp.s_out, hp.out_ready[slot], 0)) &&
+           ok_(copy_heads(ho, ost, osh, dev(slot, 3), dst, dsh, T, n, cudaMemcpyDeviceToHost,
+                          hp.s_out)) &&
+           ok_(cudaEventRecord(hp.out_free[slot], hp.s_out));
+    if (!good) {
+      cudaGetLastError();
+      return FA_LP_ERR_CUDA;
+    }
+  }
+  // `stream` completes only after the last copy-out
+  if (!ok_(cudaEventRecord(hp.end, hp.s_out)) || !ok_(cudaStreamWaitEvent(stream, hp.end, 0))) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  return FA_LP_OK;
+}
+
 int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
   if (!p || !d) return FA_LP_ERR_INVALID_ARG;
   void* base = nullptr;
@@ -519,18 +719,28 @@ int fa_lp_copy_quantized(const fa_lp_plan* p, int which, void* dst, size_t dst_b
 int fa_lp_get_last_error(fa_lp_plan* p, int* device_status) {
   if (!p || !device_status) return FA_LP_ERR_INVALID_ARG;
   *device_status = 0;
-  if (!p->dmeta) return FA_LP_OK;
-  int cur = -1;
-  cudaGetDevice(&cur);
-  if (cur != p->device) cudaSetDevice(p->device);
   int v = 0;
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpy(&v, p->d_err, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
-  if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FA_LP_ERR_CUDA;
+  if (p->dmeta) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, p->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return FA_LP_ERR_CUDA;
+    }
+  }
+  // launches of the host-buffer entry point record their status in its sub-plans (plans of
+  // fewer heads, so this recursion ends)
+  for (fa_lp_plan* sp : p->host.sub) {
+    if (!sp || sp == p) continue;
+    int sv = 0;
+    const int st = fa_lp_get_last_error(sp, &sv);
+    if (st == FA_LP_ERR_CUDA) return st;
+    if (v == 0) v = sv;
   }
   *device_status = v;
   return v ? FA_LP_ERR_DEVICE_TIMEOUT : FA_LP_OK;

@@ -60,6 +60,16 @@ struct WsLayout {
   size_t total = 0;
 };
 
+// State of the host-buffer entry point (fa_lp_attention_host): head-chunk pipeline.
+struct HostPipe {
+  int nh = 0;                                 // heads per chunk of the buffers below
+  fa_lp_plan* sub[2] = {nullptr, nullptr};    // plans of nh heads and of a last, shorter chunk
+  void* buf = nullptr;                        // 2 slots x {q, k, v, out} x tokens x nh x 128 BF16
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in_done[2] = {}, in_free[2] = {}, out_ready[2] = {}, out_free[2] = {};
+};
+
 }  // namespace falp
 
 struct fa_lp_plan {
@@ -91,6 +101,7 @@ struct fa_lp_plan {
   int* d_err = nullptr;  // [0]: sticky device status, [1]: abort word (launch generation)
   bool quantized = false;
   int refcount = 1;
+  falp::HostPipe host;  // created by the first fa_lp_attention_host call
 };
 
 namespace falp {

@@ -36,6 +36,7 @@ EXPORTS = (
     "fa_lp_plan_row_offsets", "fa_lp_get_quantized", "fa_lp_copy_quantized",
     "fa_lp_get_last_error", "fa_lp_plan_set_wait_limit", "fa_lp_release_workspace",
     "fa_lp_encode", "fa_lp_fp8_descale_noalloc", "fa_lp_forward_varlen_lse",
+    "fa_lp_attention_host",
 )
 
 _lib = None
@@ -84,6 +85,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.fa_lp_forward_varlen.argtypes = [P, P, P, i64, i64, P]
         L.fa_lp_forward_varlen_lse.argtypes = [P, P, P, i64, i64, P, i64, P]
         L.fa_lp_attention.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, P, i64, i64, P]
+        L.fa_lp_attention_host.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, i64, i64,
+                                           i32, P]
         L.fa_lp_plan_row_offsets.argtypes = [P, ctypes.POINTER(i64)]
         L.fa_lp_get_quantized.argtypes = [P, i32, ctypes.POINTER(_ArrayDesc)]
         L.fa_lp_copy_quantized.argtypes = [P, i32, P, sz, P]
@@ -118,12 +121,12 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _view(x: torch.Tensor, name: str):
+def _view(x: torch.Tensor, name: str, host: bool = False):
     if x.dtype != torch.bfloat16 or x.dim() != 3 or x.shape[2] != 128 or x.stride(2) != 1:
         raise ValueError(f"{name} must be a bfloat16 [tokens, heads, 128] view with unit channel "
                          f"stride (got {tuple(x.shape)} {x.dtype} strides {x.stride()})")
-    if not x.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.is_cuda == host:
+        raise ValueError(f"{name} must be a {'host (CPU)' if host else 'CUDA'} tensor")
     return ctypes.c_void_p(x.data_ptr()), int(x.stride(0)), int(x.stride(1))
 
 
@@ -222,6 +225,19 @@ class Plan:
         cu = ctypes.c_void_p(cu_seqlens_dev.data_ptr()) if cu_seqlens_dev is not None else None
         _check(load().fa_lp_attention(self._h, qa, qs, qh, ka, ks, kh, va, vs, vh, cu, oa, os_, oh,
                                       _stream(stream)), "fa_lp_attention")
+        return out
+
+    def attention_host(self, q, k, v, out, heads_per_chunk: int = 0, stream=None):
+        """out = attention(q, k, v) with q, k, v and out in host memory (CPU tensors; page-locked
+        ones let the copies overlap the compute). Heads go through the device in chunks whose
+        copy-in, compute and copy-out overlap; `out` is complete once `stream` is."""
+        qa, qs, qh = _view(q, "q", host=True)
+        ka, ks, kh = _view(k, "k", host=True)
+        va, vs, vh = _view(v, "v", host=True)
+        oa, os_, oh = _view(out, "out", host=True)
+        _check(load().fa_lp_attention_host(self._h, qa, qs, qh, ka, ks, kh, va, vs, vh, oa, os_,
+                                           oh, int(heads_per_chunk), _stream(stream)),
+               "fa_lp_attention_host")
         return out
 
     # -- inspection -------------------------------------------------------------------------------

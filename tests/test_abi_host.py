@@ -114,6 +114,17 @@ def test_calls_validate_before_touching_the_device(lib):
         assert lib.fa_lp_plan_set_wait_limit(h, 0) == 1
         assert lib.fa_lp_plan_set_wait_limit(h, 5) == 0
         assert lib.fa_lp_encode(3, None, 0, None, None) == 1
+        # host-buffer entry: NULL views and chunk sizes outside 0..heads are rejected first
+        hb = ctypes.create_string_buffer(64 * 128 * 2 + 16)
+        hp = ctypes.c_void_p((ctypes.addressof(hb) + 15) // 16 * 16)
+        assert lib.fa_lp_attention_host(h, None, 128, 128, hp, 128, 128, hp, 128, 128, hp, 128,
+                                        128, 0, None) == 1
+        assert lib.fa_lp_attention_host(h, hp, 128, 128, hp, 128, 128, hp, 128, 128, hp, 128,
+                                        128, 2, None) == 1
+        assert lib.fa_lp_attention_host(h, hp, 128, 128, hp, 128, 128, hp, 128, 128, hp, 128,
+                                        128, -1, None) == 1
+        assert lib.fa_lp_attention_host(h, hp, 127, 128, hp, 128, 128, hp, 128, 128, hp, 128,
+                                        128, 1, None) == 1
     finally:
         lib.fa_lp_plan_destroy(h)
 

@@ -8,7 +8,9 @@
 // Arithmetic (readings r7-r10): means are FP64 sums in canonical order -- 128-token chunks from
 // the segment start summed left to right, then the chunk sums left to right -- and
 // mean = fl32(sum / n); centred x = fl32(x - mean); per group of 16: s = E4M3_rn(fl32(amax / 6)),
-// code = E2M1_rn_sat(fl32(x / deq(s))), codes 0 when s == 0. Divisions are IEEE (__fdiv_rn).
+// code = E2M1_rn_sat(fl32(x / deq(s))), codes 0 when s == 0. The scale's division by 6 is IEEE
+// (__fdiv_rn); x / deq(s) is the correctly rounded quotient by Markstein's correction (see
+// div_rn), the same value as IEEE division.
 //
 // Layouts written (padded token axis as for FP8: segment s on rows [row0_s, row0_s + L_s)):
 //   Q, K codes : u8 [H][Tpad][64]    two E2M1 codes per byte, even channel in the low nibble
@@ -28,29 +30,40 @@
 namespace falp {
 namespace {
 
-__device__ __forceinline__ float bf16_at(const uint16_t* x, int64_t t, int h, int c, int64_t st,
-                                         int64_t sh) {
-  return __uint_as_float(uint32_t(x[t * st + int64_t(h) * sh + c]) << 16);
-}
-
 __device__ __forceinline__ float e4m3_value(uint8_t code) {
   const uint32_t h2 = cvt_e4m3x2_to_f16x2(uint16_t(code));
   return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
 }
 
-// One 16-element group held 4 per lane by 4 consecutive lanes: shared amax, UE4M3 scale, and
-// the 4 codes of this lane packed into 16 bits (element 0 in the low nibble).
-__device__ __forceinline__ uint32_t group16(const float (&x)[4], uint8_t* sf_out) {
-  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+// x / d rounded to nearest even, for a normal d and its correctly rounded reciprocal y = RN(1/d),
+// by Markstein's correction (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q = RN(x y) lies within an ulp of
+// x / d, the residual r = x - q d is exact in one FMA, and RN(q + r y) = RN(x / d). A zero x keeps
+// its sign (x / d would). Checked on GB300 against IEEE division for every E4M3 divisor and every
+// dividend with a quotient in [2^-3, 16), both signs (1.5e10 cases), and 4.3e9 random ones.
+__device__ __forceinline__ float div_rn(float x, float d, float y) {
+  const float q = __fmul_rn(x, y);
+  const float r = fmaf(-q, d, x);
+  const float q1 = fmaf(r, y, q);
+  return x == 0.f ? x : q1;
+}
+
+// One 16-element group held by one thread: UE4M3 scale and the 16 E2M1 codes, element 2i in the
+// low nibble of byte i.
+__device__ __forceinline__ uint2 group16(const float (&x)[16], uint8_t* sf_out) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
   const uint8_t sf = uint8_t(cvt_e4m3x2(__fdiv_rn(a, 6.f), 0.f) & 0xFF);
   *sf_out = sf;
-  if (sf == 0) return 0u;
+  if (sf == 0) return make_uint2(0u, 0u);
   const float ds = e4m3_value(sf);
-  const uint32_t lo = cvt_e2m1x2(__fdiv_rn(x[0], ds), __fdiv_rn(x[1], ds));
-  const uint32_t hi = cvt_e2m1x2(__fdiv_rn(x[2], ds), __fdiv_rn(x[3], ds));
-  return lo | (hi << 8);
+  const float y = __frcp_rn(ds);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i >> 2] |= cvt_e2m1x2(div_rn(x[2 * i], ds, y), div_rn(x[2 * i + 1], ds, y)) << (8 * (i & 3));
+  return make_uint2(w[0], w[1]);
 }
 
 // Pass 1: per (128-row block, head) column sums, equal to the FP64 sums of the rows in order. For
@@ -145,8 +158,9 @@ __global__ void __launch_bounds__(128) nvfp4_kmean_kernel(const SegInfo* __restr
   kmean[(int64_t(s) * H + h) * kD + c] = m;
 }
 
-// Pass 3: Q and K codes and scales. One CTA per (128-row block, head, tensor); a warp per row at
-// a time, each lane 4 channels (a 16-channel group = 4 lanes).
+// Pass 3: Q and K codes and scales. One thread per (row, 16-channel group): 8 threads per row; a
+// 256-thread CTA covers 32 rows per step and its 128-row block in 4 steps, every load of a thread
+// issued before its arithmetic.
 __global__ void __launch_bounds__(256) nvfp4_pack_qk_kernel(
     const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
     int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t Tp,
@@ -154,77 +168,93 @@ __global__ void __launch_bounds__(256) nvfp4_pack_qk_kernel(
     uint8_t* __restrict__ qc, uint8_t* __restrict__ kc, uint8_t* __restrict__ qs,
     uint8_t* __restrict__ ks, float* __restrict__ qkm) {
   const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = threadIdx.x & 7, rr = threadIdx.x >> 3, c0 = 16 * g;
   const BlockInfo bi = blocks[b];
   const uint16_t* x = z == 0 ? q : k;
   const int64_t st = z == 0 ? qst : kst, sh = z == 0 ? qsh : ksh;
   const float* mean = z == 0 ? qmean + (int64_t(h) * nblk + b) * kD
                              : kmean + (int64_t(bi.seg) * H + h) * kD;
+  const float* kmu = kmean + (int64_t(bi.seg) * H + h) * kD;  // for q . km (Q only)
   uint8_t* codes = (z == 0 ? qc : kc) + (int64_t(h) * Tp + int64_t(b) * kTile) * 64;
   uint8_t* scales = (z == 0 ? qs : ks) + (int64_t(h) * Tp + int64_t(b) * kTile) * 8;
-  const int c0 = lane * 4;
-  float mu[4], kmu[4];
+  uint4 w[4][2];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    mu[e] = mean[c0 + e];
-    kmu[e] = kmean[(int64_t(bi.seg) * H + h) * kD + c0 + e];  // for q . km (Q only)
-  }
-  for (int r = warp; r < kTile; r += 8) {
-    uint32_t packed = 0u;
-    uint8_t sf = 0;
-    float qk = 0.f;
+  for (int i = 0; i < 4; ++i) {
+    const int r = 32 * i + rr;
+    w[i][0] = w[i][1] = make_uint4(0u, 0u, 0u, 0u);
     if (r < bi.nvalid) {
-      const uint2 w = *reinterpret_cast<const uint2*>(x + int64_t(bi.tok0 + r) * st +
-                                                      int64_t(h) * sh + c0);
-      if (z == 0) {
-        qk = __uint_as_float(w.x << 16) * kmu[0];
-        qk = fmaf(__uint_as_float(w.x & 0xFFFF0000u), kmu[1], qk);
-        qk = fmaf(__uint_as_float(w.y << 16), kmu[2], qk);
-        qk = fmaf(__uint_as_float(w.y & 0xFFFF0000u), kmu[3], qk);
-      }
-      float xc[4];
-      xc[0] = __fsub_rn(__uint_as_float(w.x << 16), mu[0]);
-      xc[1] = __fsub_rn(__uint_as_float(w.x & 0xFFFF0000u), mu[1]);
-      xc[2] = __fsub_rn(__uint_as_float(w.y << 16), mu[2]);
-      xc[3] = __fsub_rn(__uint_as_float(w.y & 0xFFFF0000u), mu[3]);
+      const uint4* src =
+          reinterpret_cast<const uint4*>(x + int64_t(bi.tok0 + r) * st + int64_t(h) * sh + c0);
+      w[i][0] = __ldg(src);
+      w[i][1] = __ldg(src + 1);
+    }
+  }
+  float mu[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) mu[e] = mean[c0 + e];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 32 * i + rr;
+    const uint32_t u[8] = {w[i][0].x, w[i][0].y, w[i][0].z, w[i][0].w,
+                           w[i][1].x, w[i][1].y, w[i][1].z, w[i][1].w};
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[2 * e] = __uint_as_float(u[e] << 16);
+      v[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+    }
+    uint2 packed = make_uint2(0u, 0u);
+    uint8_t sf = 0;
+    if (r < bi.nvalid) {
+      float xc[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) xc[e] = __fsub_rn(v[e], mu[e]);
       packed = group16(xc, &sf);
     }
-    reinterpret_cast<uint16_t*>(codes + int64_t(r) * 64)[lane] = uint16_t(packed);
-    if ((lane & 3) == 0) scales[int64_t(r) * 8 + (lane >> 2)] = sf;
-    if (z == 0) {
+    *reinterpret_cast<uint2*>(codes + int64_t(r) * 64 + 8 * g) = packed;
+    scales[int64_t(r) * 8 + g] = sf;
+    if (z == 0) {  // the BF16 query row times its segment's K mean (rows past the block: 0)
+      float qk = 0.f;
+      if (r < bi.nvalid) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, o);
-      if (lane == 0) qkm[int64_t(h) * Tp + int64_t(b) * kTile + r] = qk;
+        for (int e = 0; e < 16; ++e) qk = fmaf(v[e], kmu[c0 + e], qk);
+      }
+      qk += __shfl_xor_sync(0xffffffffu, qk, 1);
+      qk += __shfl_xor_sync(0xffffffffu, qk, 2);
+      qk += __shfl_xor_sync(0xffffffffu, qk, 4);
+      if (g == 0) qkm[int64_t(h) * Tp + int64_t(b) * kTile + r] = qk;
     }
   }
 }
 
 // Pass 4: V^T codes and scales. One CTA per (128-key block, head): the BF16 tile goes through
-// shared memory; then per (channel, 16-key group) a 4-lane team quantizes 16 keys.
+// shared memory with 16-byte loads; then one thread per (channel, 16-key group).
 __global__ void __launch_bounds__(256) nvfp4_pack_vt_kernel(
     const uint16_t* __restrict__ v, int64_t vst, int64_t vsh, const BlockInfo* __restrict__ blocks,
     int H, int64_t Tp, uint8_t* __restrict__ vt, uint8_t* __restrict__ vs) {
-  __shared__ float tile[kTile][kD + 1];
+  __shared__ __align__(16) uint16_t tile[kTile][kD + 8];  // +8: rows start on distinct banks
   const int b = blockIdx.x, h = blockIdx.y;
   const BlockInfo bi = blocks[b];
-  for (int i = threadIdx.x; i < kTile * kD; i += 256) {
-    const int r = i >> 7, c = i & 127;
-    tile[r][c] = r < bi.nvalid ? bf16_at(v, bi.tok0 + r, h, c, vst, vsh) : 0.f;
+  for (int i = threadIdx.x; i < kTile * 16; i += 256) {
+    const int r = i >> 4, c8 = (i & 15) * 8;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (r < bi.nvalid)
+      w = __ldg(reinterpret_cast<const uint4*>(v + int64_t(bi.tok0 + r) * vst + int64_t(h) * vsh +
+                                               c8));
+    *reinterpret_cast<uint4*>(&tile[r][c8]) = w;
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  // 128 channels x 8 groups = 1024 teams of 4 lanes; 64 teams per pass of 256 threads
-  for (int team = threadIdx.x >> 2; team < kD * 8; team += 64) {
-    const int c = team >> 3, g = team & 7;
-    const int k0 = g * 16 + (lane & 3) * 4;
-    float x[4];
+  // 128 channels x 8 groups; a warp takes 32 consecutive channels of one group
+  for (int task = threadIdx.x; task < kD * 8; task += 256) {
+    const int c = task & (kD - 1), g = task >> 7;
+    float x[16];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = tile[k0 + e][c];
+    for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(uint32_t(tile[16 * g + e][c]) << 16);
     uint8_t sf;
-    const uint32_t packed = group16(x, &sf);
-    uint8_t* row = vt + (int64_t(h) * kD + c) * (Tp / 2) + int64_t(b) * (kTile / 2);
-    reinterpret_cast<uint16_t*>(row)[g * 4 + (lane & 3)] = uint16_t(packed);
-    if ((lane & 3) == 0) vs[((int64_t(h) * (Tp / kTile) + b) * kD + c) * 8 + g] = sf;
+    const uint2 packed = group16(x, &sf);
+    *reinterpret_cast<uint2*>(vt + (int64_t(h) * kD + c) * (Tp / 2) + int64_t(b) * (kTile / 2) +
+                              8 * g) = packed;
+    vs[((int64_t(h) * (Tp / kTile) + b) * kD + c) * 8 + g] = sf;
   }
 }
 

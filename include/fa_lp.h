@@ -78,6 +78,8 @@ FA_LP_API const char* fa_lp_status_string(int status);
  *   heads           : H (1..1024).
  *   cu_seqlens_host : host pointer, num_segments + 1 int32 entries. Copied; not retained.
  *   num_segments    : >= 1. Empty segments (cu[s] == cu[s+1]) are allowed and produce no work.
+ *                     A batch of B sequences of length S is the segmentation [0, S, 2S, ..., BS]
+ *                     over the [B*S, H, 128] token axis (each sequence attends to itself only).
  *   softmax_scale   : > 0 and finite; <= 0 or NaN selects 1/sqrt(128).
  *   mode            : FA_LP_MODE_FP8 or FA_LP_MODE_NVFP4.
  *   device          : CUDA device ordinal the plan will run on (not touched here).

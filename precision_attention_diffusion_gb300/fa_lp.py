@@ -294,6 +294,40 @@ def attention(q, k, v, cu_seqlens, out=None, *, cu_seqlens_host=None, softmax_sc
     return plan.attention(q, k, v, cu_seqlens, out=out, stream=stream)
 
 
+def merge_batch(x: torch.Tensor, name: str) -> torch.Tensor:
+    """View a [batch, seq, heads, 128] tensor as the packed [batch * seq, heads, 128] token axis,
+    without copying: the batch stride must equal seq times the token stride (true for contiguous
+    tensors and for slices of a fused [batch, seq, 3, heads, 128] QKV buffer)."""
+    if x.dim() != 4:
+        raise ValueError(f"{name} must be [batch, seq, heads, 128] (got {tuple(x.shape)})")
+    B, S = x.shape[0], x.shape[1]
+    if B > 1 and S > 0 and x.stride(0) != S * x.stride(1):
+        raise ValueError(f"{name}: batch stride {x.stride(0)} is not seq x token stride "
+                         f"({S} x {x.stride(1)}); the batch cannot be packed without a copy")
+    return x.as_strided((B * S, x.shape[2], x.shape[3]), (x.stride(1), x.stride(2), x.stride(3)))
+
+
+def attention_batched(q, k, v, out=None, *, softmax_scale=None, mode: int = MODE_FP8,
+                      stream=None):
+    """Batch > 1 through varlen packing: q, k, v [batch, seq, heads, 128] become one packed call
+    with cu_seqlens = [0, seq, 2 seq, ..., batch seq] (each sequence attends to itself only).
+    Scales follow the packed call (per (tensor, head) over every token of the batch). Returns
+    out [batch, seq, heads, 128]."""
+    B, S, H = q.shape[0], q.shape[1], q.shape[2]
+    for name, x in (("k", k), ("v", v)):
+        if tuple(x.shape) != tuple(q.shape):
+            raise ValueError(f"{name} shape {tuple(x.shape)} differs from q {tuple(q.shape)}")
+    qp, kp, vp = merge_batch(q, "q"), merge_batch(k, "k"), merge_batch(v, "v")
+    if out is None:
+        out = torch.empty((B, S, H, q.shape[3]), dtype=torch.bfloat16, device=q.device)
+    op = merge_batch(out, "out")
+    cu_host = [i * S for i in range(B + 1)]
+    cu_dev = torch.tensor(cu_host, dtype=torch.int32, device=q.device)
+    attention(qp, kp, vp, cu_dev, out=op, cu_seqlens_host=cu_host, softmax_scale=softmax_scale,
+              mode=mode, stream=stream)
+    return out
+
+
 _plans = {}
 
 

@@ -149,3 +149,23 @@ def test_nvfp4_workspace_holds_the_qmk_table(lib):
     assert two <= one - 0.49 * table
     # an empty segment adds no table (only its K-means row: H x 128 floats, aligned)
     assert ws_of([0, 0, 30272], 56) <= one + 56 * 128 * 4 + 2048
+
+
+def test_batched_front_end_packs_without_copies():
+    """[batch, seq, heads, 128] views become the packed token axis only when no copy is needed."""
+    import torch
+    from precision_attention_diffusion_gb300 import fa_lp
+    x = torch.zeros(3, 5, 2, 128, dtype=torch.bfloat16)
+    p = fa_lp.merge_batch(x, "x")
+    assert tuple(p.shape) == (15, 2, 128) and p.data_ptr() == x.data_ptr()
+    assert p.stride() == (256, 128, 1)
+    fused = torch.zeros(3, 5, 3, 2, 128, dtype=torch.bfloat16)
+    q = fa_lp.merge_batch(fused[:, :, 0], "q")
+    assert q.stride() == (768, 128, 1) and tuple(q.shape) == (15, 2, 128)
+    # token 7 of the packed view is sequence 1, token 2 of the batch
+    fused[1, 2, 0, 1, 5] = 3.0
+    assert float(q[7, 1, 5]) == 3.0
+    with pytest.raises(ValueError):
+        fa_lp.merge_batch(x.transpose(0, 1), "x")  # seq-major storage: batch cannot be packed
+    with pytest.raises(ValueError):
+        fa_lp.merge_batch(x[0], "x")

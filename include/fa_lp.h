@@ -205,15 +205,16 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
  *                     serialise with it.
  *   out             : host pointer, BF16 [tokens, heads, 128] with element strides; every row
  *                     (all tokens lie in a segment) is written. Caller-owned.
- *   heads_per_chunk : 1..heads, or 0 for the library's choice (4 to 8 chunks whose CTAs fill the
- *                     GPU's waves best).
+ *   heads_per_chunk : 1..heads for chunks of that many heads (the last may be shorter), or 0 for
+ *                     the library's choice: the size giving 4 to 8 chunks whose CTAs fill the
+ *                     GPU's waves best (1-head chunks when heads < 4).
  *   stream          : the quantize and attention kernels run on it; the copies run on two
  *                     streams of the plan, ordered after the work already on `stream`, and
  *                     `stream` is ordered after the last copy-out: once `stream` completes, `out`
  *                     holds the result. Returns after enqueueing.
- * Device memory: two chunk slots of Q, K, V and output (8 x tokens x heads_per_chunk x 256
- * bytes), allocated on the first call (or a call with another chunk size) and kept by the plan,
- * plus the workspace of plans of heads_per_chunk heads (cached like any plan). Device-side wait
+ * Device memory: two chunk slots of Q, K, V and output (8 x tokens x (largest chunk) x 256
+ * bytes), allocated on the first call (or a call with another heads_per_chunk) and kept by the
+ * plan, plus plans of the chunk sizes (cached like any plan). Device-side wait
  * expiries are reported by fa_lp_get_last_error on this plan. A plan must not run this call
  * from two host threads at once.
  * Errors: INVALID_ARG (null or misaligned view, heads_per_chunk out of range, wrong device),

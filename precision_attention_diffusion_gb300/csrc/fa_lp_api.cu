@@ -154,42 +154,49 @@ cudaError_t copy_heads(void* dst, int64_t dst_st, int64_t dst_sh, const void* sr
   return cudaSuccess;
 }
 
-// Heads per chunk when the caller leaves it open: 4 to 8 chunks, the split whose chunks fill the
-// GPU's waves of CTAs best (ties: more chunks, so that the first copy-in and the last copy-out,
-// which nothing overlaps, are shorter).
-int default_heads_per_chunk(const fa_lp_plan& p) {
+// Chunks of heads for the host-buffer pipeline: equal chunks (the last may be shorter) of
+// heads_per_chunk heads, or, when the caller leaves it open, of the size that gives 4 to 8 chunks
+// whose CTAs fill the GPU's waves best (ties: more chunks, so that the first copy-in and the last
+// copy-out, which nothing overlaps, are shorter).
+std::vector<int> host_schedule(const fa_lp_plan& p, int heads_per_chunk) {
   const int H = p.heads;
-  if (H < 4) return 1;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess ||
-      sms <= 0) {
-    cudaGetLastError();
-    sms = 152;
-  }
-  const double cph = double(p.work.size()) / H;  // CTAs per head
-  int best = (H + 3) / 4;
-  double best_eff = -1.0;
-  for (int nh = 1; nh <= H; ++nh) {
-    const int nc = (H + nh - 1) / nh;
-    if (nc < 4 || nc > 8) continue;
-    double ctas = 0.0, slots = 0.0;
-    for (int h0 = 0; h0 < H; h0 += nh) {
-      const double c = cph * std::min(nh, H - h0);
-      ctas += c;
-      slots += std::ceil(c / sms) * sms;
+  int nh = heads_per_chunk;
+  if (nh <= 0) {
+    nh = H < 4 ? 1 : (H + 3) / 4;
+    if (H >= 4) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess ||
+          sms <= 0) {
+        cudaGetLastError();
+        sms = 152;
+      }
+      const double cph = double(p.work.size()) / H;  // CTAs per head
+      double best_eff = -1.0;
+      for (int n = 1; n <= H; ++n) {
+        const int nc = (H + n - 1) / n;
+        if (nc < 4 || nc > 8) continue;
+        double ctas = 0.0, slots = 0.0;
+        for (int h0 = 0; h0 < H; h0 += n) {
+          const double c = cph * std::min(n, H - h0);
+          ctas += c;
+          slots += std::ceil(c / sms) * sms;
+        }
+        const double eff = slots > 0 ? ctas / slots : 0.0;
+        if (eff > best_eff + 1e-9 || (std::fabs(eff - best_eff) <= 1e-9 && n < nh)) {
+          best_eff = eff;
+          nh = n;
+        }
+      }
     }
-    const double eff = slots > 0 ? ctas / slots : 0.0;
-    if (eff > best_eff + 1e-9 || (std::fabs(eff - best_eff) <= 1e-9 && nh < best)) {
-      best_eff = eff;
-      best = nh;
-    }
   }
-  return best;
+  std::vector<int> out;
+  for (int h0 = 0; h0 < H; h0 += nh) out.push_back(std::min(nh, H - h0));
+  return out;
 }
 
 // Free the pipeline's device buffer, streams and events (device already current); hands the
 // sub-plans to the caller, which releases them outside the plan-cache lock.
-int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[2]) {
+int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[4]) {
   falp::HostPipe& hp = p->host;
   int st = FA_LP_OK;
   if (hp.s_in && cudaStreamSynchronize(hp.s_in) != cudaSuccess) st = FA_LP_ERR_CUDA;
@@ -201,8 +208,7 @@ int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[2]) {
     if (*e) cudaEventDestroy(*e);
   if (hp.s_in) cudaStreamDestroy(hp.s_in);
   if (hp.s_out) cudaStreamDestroy(hp.s_out);
-  subs[0] = hp.sub[0];
-  subs[1] = hp.sub[1];
+  for (int i = 0; i < 4; ++i) subs[i] = hp.sub[i];
   hp = falp::HostPipe();
   if (st != FA_LP_OK) cudaGetLastError();
   return st;
@@ -416,7 +422,7 @@ int fa_lp_plan_create(int64_t tokens, int heads, const int32_t* cu, int num_segm
 
 int fa_lp_plan_destroy(fa_lp_plan* p) {
   if (!p) return FA_LP_OK;
-  fa_lp_plan* subs[2] = {nullptr, nullptr};
+  fa_lp_plan* subs[4] = {nullptr, nullptr, nullptr, nullptr};
   int st = FA_LP_OK;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -549,19 +555,21 @@ int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
   if (p->tokens == 0) return FA_LP_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const int H = p->heads;
-  const int nh = heads_per_chunk ? heads_per_chunk : default_heads_per_chunk(*p);
   const int64_t T = p->tokens;
   falp::HostPipe& hp = p->host;
-  if (hp.nh != nh) {  // (re)build the pipeline for this chunk size
-    fa_lp_plan* old[2] = {nullptr, nullptr};
+  if (hp.key != heads_per_chunk) {  // (re)build the pipeline for this chunking
+    fa_lp_plan* old[4] = {nullptr, nullptr, nullptr, nullptr};
     st = host_pipe_release(p, old);
     for (fa_lp_plan* sp : old)
       if (sp) fa_lp_plan_destroy(sp);
     if (st != FA_LP_OK) return st;
-    const size_t bytes = size_t(8) * size_t(T) * size_t(nh) * FA_LP_HEAD_DIM * 2;
+    hp.sizes = host_schedule(*p, heads_per_chunk);
+    hp.maxn = *std::max_element(hp.sizes.begin(), hp.sizes.end());
+    const size_t bytes = size_t(8) * size_t(T) * size_t(hp.maxn) * FA_LP_HEAD_DIM * 2;
     if (cudaMalloc(&hp.buf, bytes) != cudaSuccess) {
       cudaGetLastError();
       hp.buf = nullptr;
+      hp.sizes.clear();
       return FA_LP_ERR_OOM;
     }
     bool ok = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) == cudaSuccess &&
@@ -572,14 +580,16 @@ int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
       ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     // chunks of fewer heads than the plan run on plans of their own (a chunk of all the heads
     // runs on this plan: a plan never holds itself)
-    for (int i = 0; i < 2 && ok; ++i) {
-      const int n = i == 0 ? nh : H % nh;
-      if (n == 0 || n == H) continue;
+    int nsub = 0;
+    for (int n : hp.sizes) {
+      if (!ok || n == H || std::find(hp.sub_n, hp.sub_n + nsub, n) != hp.sub_n + nsub) continue;
+      if (nsub == 4) { ok = false; break; }
       ok = fa_lp_plan_create(T, n, p->cu.data(), p->nseg, p->scale, p->mode, p->device,
-                             &hp.sub[i]) == FA_LP_OK;
-      ok = ok && hp.sub[i] != p;
+                             &hp.sub[nsub]) == FA_LP_OK;
+      ok = ok && hp.sub[nsub] != p;
+      hp.sub_n[nsub++] = n;
     }
-    hp.nh = nh;
+    hp.key = heads_per_chunk;
     if (!ok) {
       cudaGetLastError();
       host_pipe_release(p, old);
@@ -590,20 +600,27 @@ int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
   }
   for (fa_lp_plan* sp : hp.sub)
     if (sp) sp->spin_limit = p->spin_limit;
-  const size_t tb = size_t(T) * size_t(nh) * FA_LP_HEAD_DIM * 2;  // one tensor of one slot
+  const size_t tb = size_t(T) * size_t(hp.maxn) * FA_LP_HEAD_DIM * 2;  // one tensor of one slot
   uint8_t* base = static_cast<uint8_t*>(hp.buf);
   auto dev = [&](int slot, int which) { return base + (size_t(slot) * 4 + which) * tb; };
   auto ok_ = [](cudaError_t e) { return e == cudaSuccess; };
+  auto plan_of = [&](int n) -> fa_lp_plan* {
+    if (n == H) return p;
+    for (int i = 0; i < 4; ++i)
+      if (hp.sub_n[i] == n) return hp.sub[i];
+    return nullptr;
+  };
   // the copies start after the work already on `stream` (which may still use the slots)
   if (!ok_(cudaEventRecord(hp.start, stream)) || !ok_(cudaStreamWaitEvent(hp.s_in, hp.start, 0)) ||
       !ok_(cudaStreamWaitEvent(hp.s_out, hp.start, 0))) {
     cudaGetLastError();
     return FA_LP_ERR_CUDA;
   }
-  const int nchunks = (H + nh - 1) / nh;
-  for (int c = 0; c < nchunks; ++c) {
-    const int h0 = c * nh, n = std::min(nh, H - h0), slot = c & 1;
-    fa_lp_plan* sp = (n == H) ? p : (n == nh) ? hp.sub[0] : hp.sub[1];
+  const int nchunks = int(hp.sizes.size());
+  for (int c = 0, h0 = 0; c < nchunks; h0 += hp.sizes[c], ++c) {
+    const int n = hp.sizes[c], slot = c & 1;
+    fa_lp_plan* sp = plan_of(n);
+    if (!sp) return FA_LP_ERR_CUDA;
     const int64_t dst = int64_t(n) * FA_LP_HEAD_DIM, dsh = FA_LP_HEAD_DIM;  // dense [T, n, 128]
     const uint8_t* hq = static_cast<const uint8_t*>(q) + size_t(h0) * qsh * 2;
     const uint8_t* hk = static_cast<const uint8_t*>(k) + size_t(h0) * ksh * 2;

@@ -62,9 +62,13 @@ struct WsLayout {
 
 // State of the host-buffer entry point (fa_lp_attention_host): head-chunk pipeline.
 struct HostPipe {
-  int nh = 0;                                 // heads per chunk of the buffers below
-  fa_lp_plan* sub[2] = {nullptr, nullptr};    // plans of nh heads and of a last, shorter chunk
-  void* buf = nullptr;                        // 2 slots x {q, k, v, out} x tokens x nh x 128 BF16
+  int key = -1;                               // heads_per_chunk the pipeline was built for
+  std::vector<int> sizes;                     // heads of each chunk, in order
+  int maxn = 0;                               // largest chunk
+  fa_lp_plan* sub[4] = {nullptr, nullptr, nullptr, nullptr};  // plans of the chunk sizes
+  int sub_n[4] = {0, 0, 0, 0};                // (fewer heads than the plan; a chunk of all
+                                              // the heads runs on the plan itself)
+  void* buf = nullptr;                        // 2 slots x {q, k, v, out} x tokens x maxn x 128 BF16
   cudaStream_t s_in = nullptr, s_out = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
   cudaEvent_t in_done[2] = {}, in_free[2] = {}, out_ready[2] = {}, out_free[2] = {};

@@ -96,3 +96,16 @@ def test_host_entry_reports_device_wait_expiry(fa):
     torch.cuda.synchronize()
     assert plan.last_error() == 0
     assert torch.equal(out.view(torch.int16), device_reference(fa, plan, buf).view(torch.int16))
+
+
+def test_host_entry_default_schedule_many_heads(fa):
+    """The library's default chunking with enough heads for several chunks and a two-segment
+    segmentation."""
+    T, H = 2048, 24
+    buf = fused_host(T, H, seed=55)
+    plan = fa.Plan([0, 1000, T], H, mode=0)
+    ref = device_reference(fa, plan, buf)
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16).pin_memory()
+    plan.attention_host(buf[:, 0], buf[:, 1], buf[:, 2], out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

@@ -1,6 +1,6 @@
 """FP8 E4M3 path on the GPU through the C ABI, against the oracle.
 
-Bar (the benchmark spec): quantized codes and descales bit-exact; output within relative RMS 1e-2 of the
+Bar: quantized codes and descales bit-exact; output within relative RMS 1e-2 of the
 FP8-emulating oracle (C2, replaying the kernel's 64-key tiles and reference-max rule) and within
 0.06 of FP64 exact attention (C1) on Gaussian inputs. Per row, the error is also bounded
 (relative RMS of any one row <= 5e-2 of C2) so that a single wrong row cannot hide in the mean.

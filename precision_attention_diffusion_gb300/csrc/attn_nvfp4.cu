@@ -420,13 +420,14 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
     tmem_st8(tmem + col_p(t, x) + lane_off, pk);
     tmem_st1(tmem + col_psf(t, x) + uint32_t(wq) + lane_off, sfw);
     if (u > 0 && __any_sync(0xffffffffu, move)) {
-      // rescale O between PV_t(u-1) and PV_t(u)
+      // rescale O between PV_t(u-1) and PV_t(u), two 32-column loads in flight
       if (!(ok = wait_all(&S.bar_o[t][x ^ 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax))) break;
       tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t o[32];
+      for (int i = 0; i < 4; i += 2) {
+        uint32_t o[32], o2[32];
         tmem_ld32(o_addr + 32 * i, o);
+        tmem_ld32(o_addr + 32 * i + 32, o2);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -434,8 +435,12 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
           fma2(a0, a1, __uint_as_float(o[e]), __uint_as_float(o[e + 1]), alpha, 0.f);
           o[e] = __float_as_uint(a0);
           o[e + 1] = __float_as_uint(a1);
+          fma2(a0, a1, __uint_as_float(o2[e]), __uint_as_float(o2[e + 1]), alpha, 0.f);
+          o2[e] = __float_as_uint(a0);
+          o2[e + 1] = __float_as_uint(a1);
         }
         tmem_st32(o_addr + 32 * i, o);
+        tmem_st32(o_addr + 32 * i + 32, o2);
       }
     }
     tmem_wait_st();

@@ -358,14 +358,11 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_sr[t]));  // S_t(u+1) may now overwrite S
-    // s'' = S c (c > 0, so the group maxima scale the same way, exactly)
+    // raw S; s'' = S c enters only as the exp2 argument S c + gb (one FMA). c > 0, so the group
+    // maxima of s'' are the raw maxima times c, exactly.
     float s[64];
 #pragma unroll
-    for (int i = 0; i < 64; i += 2)
-      fma2(s[i], s[i + 1], __uint_as_float(r[i >> 4][i & 15]),
-           __uint_as_float(r[i >> 4][(i + 1) & 15]), cs, 0.f);
-#pragma unroll
-    for (int g = 0; g < 4; ++g) gm[g] *= cs;
+    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i >> 4][i & 15]);
     if (u == n_sub - 1 && last_valid < kSub) {  // keys past the segment: mask, then reduce
 #pragma unroll
       for (int i = 0; i < 64; ++i)
@@ -378,6 +375,8 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
         gm[g] = max16(v);
       }
     }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) gm[g] *= cs;
     const float mx = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
     const bool move = mx > m;  // exact running maximum
     const float m_new = move ? mx : m;
@@ -397,7 +396,7 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float x0, x1;
-        fma2(x0, x1, s[16 * g + 2 * i], s[16 * g + 2 * i + 1], 1.f, gb);
+        fma2(x0, x1, s[16 * g + 2 * i], s[16 * g + 2 * i + 1], cs, gb);
         uint32_t h2;
         b[i] = cvt_e2m1x2_and_f16x2(ex2_approx(x0), ex2_approx(x1), h2);
         // the quantized values in f16 (exact; a group sums to at most 96 in steps of 0.5)

@@ -53,8 +53,8 @@ KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5}
 NCU_TRAFFIC = {
     ("fp8_s30272_h56", "b3ec608431527b6576bff057ae9e00b5dfc55dccc13fc677003b0a9df411bbb5"):
         1.93e9 + 425.50e6,
-    ("nvfp4_s30272_h56", "2edec3a932eb0431577e13cc0f0d7c3daa4bbc5a2487702c3bec99347bc71469"):
-        2.40e9 + 425.41e6,
+    ("nvfp4_s30272_h56", "34f2851e9ee735c99a78e346d09332e8769f076124d32b4ab9b0e77deac59cd3"):
+        2.41e9 + 425.52e6,
 }
 
 

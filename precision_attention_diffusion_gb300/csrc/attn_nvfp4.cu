@@ -18,7 +18,9 @@
 //   per 16 keys: sf = UE4M3(max P' / 6), code = E2M1(P' / deq(sf)), both evaluated in the
 //                exponent: max P' / 6 = 2^(max s'' - m + log2 448), P' / deq(sf) =
 //                2^(s'' - m + log2 2688 - log2 deq(sf)) (one exp2 per key, no division)
-//   l_i        = l_i 2^(m_old - m_new) + sum deq(P),   O_i likewise with deq(P) deq(V)
+//   l_i        = l_i 2^(m_old - m_new) + sum deq(P),   O_i likewise with deq(P) deq(V); l is
+//                accumulated by the PV MMA itself: every V^T stage carries 16 rows of E2M1 1.0
+//                (scale 1.0) after its 128 channels, so O has 144 columns and column 128 is l
 //   out        = BF16(O / l) for rows inside the segment.
 //
 // Roles (480 threads):
@@ -31,18 +33,20 @@
 //                 S_t(u) += 1 Tq_t(u)^T              1 kind::f16 MMA  M=128 N=64 K=16 (A =
 //                                                    rows [1, 1, 1, 0...], B = the table
 //                                                    entries as three BF16 pieces)
-//                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=128 K=64, A = P in TMEM
+//                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=144 K=64, A = P in TMEM
+//                                                    (N 128-143: the 1.0 rows, giving l)
 //   warps 11-14 per sub-tile: K and V scale factors into tensor memory (the MMA reads the B-side
 //               scales of row n from column n / 32 of every lane quarter, so each of the four
-//               warps writes its own quarter), and the BF16 pieces of the table entries;
+//               warps writes its own quarter; the 1.0 rows' scale column is written once),
+//               and the BF16 pieces of the table entries;
 //   warps 0-7   softmax of tile 0 (warps 0-3) and 1 (warps 4-7), one thread per query row (row ==
 //               tensor-memory lane); S and the maxima of its 16-key groups come from
 //               tcgen05.ld.red; P codes and P scales go to tensor memory (A-side scales: row r in
 //               lane r, column r / 32), O is rescaled in tensor memory when a row's maximum
 //               moves, and the same threads run the epilogue.
-// Tensor memory (488 of 512 columns): per query tile t a 64-column S, two P slots (8 columns of codes
-// and 4 of scales each) and a 128-column O; then Q, K (two buffers) and V (two buffers) scale
-// blocks. Every barrier wait is bounded; on expiry the kernel records an error, drains its
+// Tensor memory (512 columns): per query tile t a 144-column O, one P slot (8 columns of codes, 4
+// of scales: PV(u-1) has read it long before P(u) is ready), a 64-column S; Q, K (two buffers)
+// and V (two buffers) scale blocks in the gaps. Every barrier wait is bounded; on expiry the kernel records an error, drains its
 // in-flight copies and MMAs, frees its tensor memory and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -63,26 +67,31 @@ constexpr int kSub = 64;         // keys per sub-tile
 constexpr uint32_t kCodeTile = 128 * 64;  // 128 rows of 128 E2M1 codes
 constexpr uint32_t kSfTile = 128 * 8;     // 128 rows of 8 UE4M3 scales
 constexpr uint32_t kIdescS = idesc_mxf4nvf4(128, kSub);
-constexpr uint32_t kIdescPV = idesc_mxf4nvf4(128, 128);
+constexpr uint32_t kVTile = 144 * 64;    // V^T stage: 128 channel rows + 16 rows of E2M1 1.0
+constexpr uint32_t kIdescPV = idesc_mxf4nvf4(128, 144);  // channels + 16 row-sum columns
 // kind::f16: D f32, A and B BF16, K-major, M=128, N=64
 constexpr uint32_t kIdescFold = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(kSub) >> 3) << 17) |
                                 ((128u >> 4) << 24);
 constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
 constexpr float kLog2_6 = 2.5849625007211562f;
 
-// tensor-memory columns
-__device__ __forceinline__ uint32_t col_s(int t) { return 224u * uint32_t(t); }
-__device__ __forceinline__ uint32_t col_p(int t, int x) { return 224u * uint32_t(t) + 64u + 16u * uint32_t(x); }
-__device__ __forceinline__ uint32_t col_psf(int t, int x) { return col_p(t, x) + 8u; }
-__device__ __forceinline__ uint32_t col_o(int t) { return 224u * uint32_t(t) + 96u; }
-__device__ __forceinline__ uint32_t col_qsf(int t) { return 448u + 8u * uint32_t(t); }
-__device__ __forceinline__ uint32_t col_ksf(int b) { return 464u + 8u * uint32_t(b); }
-__device__ __forceinline__ uint32_t col_vsf(int b) { return 480u + 4u * uint32_t(b); }
+// tensor-memory columns (512): per query tile t at 256 t -- O 144 (channels, then 16 columns that
+// accumulate the row sum l through the 1.0 rows of V^T), the P codes (8) and P scales (4) of one
+// sub-tile, S 64 -- and, in the gaps, the Q scales, the K and V scale blocks (double buffered; a V
+// block has a fifth column for the 1.0 rows). Starts: O and S 32-aligned, P codes 16-aligned,
+// scale blocks 8-aligned (4 for the B side).
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u * uint32_t(t); }
+__device__ __forceinline__ uint32_t col_p(int t) { return 256u * uint32_t(t) + 144u; }
+__device__ __forceinline__ uint32_t col_psf(int t) { return 256u * uint32_t(t) + 152u; }
+__device__ __forceinline__ uint32_t col_s(int t) { return 256u * uint32_t(t) + 192u; }
+__device__ __forceinline__ uint32_t col_vsf(int b) { return b ? 416u : 160u; }
+__device__ __forceinline__ uint32_t col_qsf(int t) { return 168u + 8u * uint32_t(t); }
+__device__ __forceinline__ uint32_t col_ksf(int b) { return b ? 424u : 184u; }
 
 struct Smem {
   uint8_t q[2][kCodeTile];
   uint8_t k[kStages][kCodeTile];
-  uint8_t v[kStages][kCodeTile];   // V^T: 128 channel rows of 128 keys
+  uint8_t v[kStages][kVTile];      // V^T: 128 channel rows of 128 keys, 16 rows of 1.0
   // qm K^T fold into S (one kind::f16 MMA per sub-tile): A = 128 identical rows [1, 1, 1, 0...]
   // (one core matrix repeated, then a zero core matrix), B = per key the table entry as three
   // BF16 pieces (64 keys x 16 bytes, then 1 KB of zeros for K 8..15)
@@ -107,6 +116,7 @@ struct Smem {
   int abort_flag;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 struct Nvfp4Args {
   const SegInfo* segs;
@@ -221,9 +231,9 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
   // keys [64h, 64h + 64) of a 128-key tile are bytes [32h, 32h + 32) of each V^T row
   auto issue_pv = [&](int u) {
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
-    const uint64_t vb = dv + (((j % kStages) * kCodeTile) >> 4) + 2 * h;
-    mma_mxf4_ts_elect(tmem + col_o(t), tmem + col_p(t, int(h)), vb, kIdescPV,
-                      tmem + col_psf(t, int(h)), tmem + col_vsf(int(h)), u > 0 ? 1u : 0u);
+    const uint64_t vb = dv + (((j % kStages) * kVTile) >> 4) + 2 * h;
+    mma_mxf4_ts_elect(tmem + col_o(t), tmem + col_p(t), vb, kIdescPV,
+                      tmem + col_psf(t), tmem + col_vsf(int(h)), u > 0 ? 1u : 0u);
     mma_commit_elect(smem_u32(&S.bar_o[t][h]));
     mma_commit_elect(smem_u32(&S.bar_sffree[h]));
     if (h == 1 || u + 1 == n_sub) mma_commit_elect(smem_u32(&S.bar_free[j % kStages]));
@@ -279,6 +289,9 @@ __device__ __forceinline__ void scale_factor_warps(Smem& S, const Nvfp4Args& a, 
       tmem_st1(tmem + col_qsf(t) + 4u + uint32_t(quarter) + lane_off, w.y);
     }
   }
+  // rows 128-143 of V^T (the 1.0 rows): scale 1.0 in column 4 of both V scale blocks
+  tmem_st1(tmem + col_vsf(0) + 4u + lane_off, lane < 16 ? 0x38383838u : 0u);
+  tmem_st1(tmem + col_vsf(1) + 4u + lane_off, lane < 16 ? 0x38383838u : 0u);
   for (int u = 0; u < n_sub; ++u) {
     const int j = u >> 1, h = u & 1, st = j % kStages, b = u & 1;
     if (h == 0) {
@@ -343,7 +356,7 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
   const uint32_t s_addr = tmem + col_s(t) + lane_off;
   const uint32_t o_addr = tmem + col_o(t) + lane_off;
   const int last_valid = sg.len - (n_sub - 1) * kSub;  // keys of the last sub-tile, 1..64
-  float m = -INFINITY, l = 0.f;                         // running maximum (log2 units), sum
+  float m = -INFINITY;                                  // running maximum (log2 units)
   bool ok = true;
   for (int u = 0; u < n_sub; ++u) {
     const int x = u & 1;
@@ -384,7 +397,6 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
     const float bias = kLog2_2688 - m_new;                  // s'' + bias = log2 P'
     uint32_t pk[8];
     uint32_t sfw = 0u;
-    float rs = 0.f;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {  // 16 keys per scale group
       // second level: UE4M3 scale of the group = E4M3(max P' / 6), max P' / 6 = 2^(gm + bias) / 6;
@@ -392,32 +404,26 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
       const uint32_t sf = cvt_e4m3x2(ex2_approx(gm[g] + (bias - kLog2_6)), 0.f) & 0xFFu;
       const float ds = e4m3_to_f32(sf);
       const float gb = sf ? bias - lg2_approx(ds) : -INFINITY;
-      uint32_t b[8], hs = 0u;
+      uint32_t b[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float x0, x1;
         fma2(x0, x1, s[16 * g + 2 * i], s[16 * g + 2 * i + 1], cs, gb);
-        uint32_t h2;
-        b[i] = cvt_e2m1x2_and_f16x2(ex2_approx(x0), ex2_approx(x1), h2);
-        // the quantized values in f16 (exact; a group sums to at most 96 in steps of 0.5)
-        hs = hadd2_u32(hs, h2);
+        b[i] = uint32_t(cvt_e2m1x2(ex2_approx(x0), ex2_approx(x1)));
       }
       pk[2 * g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040),
                               0x5410);
       pk[2 * g + 1] = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
                                   __byte_perm(b[6], b[7], 0x0040), 0x5410);
-      const float2 hf = f16x2_to_f32x2(hs);
-      rs = fmaf(hf.x + hf.y, ds, rs);  // l sums the dequantized P (reading r6)
       sfw |= sf << (8 * g);
     }
-    l = l * alpha + rs;
-    // P slot x was last read by PV_t(u-2)
-    if (u >= 2) {
-      if (!(ok = wait_all(&S.bar_o[t][x], ((u - 2) >> 1) & 1, S, a, kRoleSoftmax))) break;
+    // the P slot was last read by PV_t(u-1)
+    if (u >= 1) {
+      if (!(ok = wait_all(&S.bar_o[t][x ^ 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax))) break;
       tc_fence_after();
     }
-    tmem_st8(tmem + col_p(t, x) + lane_off, pk);
-    tmem_st1(tmem + col_psf(t, x) + uint32_t(wq) + lane_off, sfw);
+    tmem_st8(tmem + col_p(t) + lane_off, pk);
+    tmem_st1(tmem + col_psf(t) + uint32_t(wq) + lane_off, sfw);
     if (u > 0 && __any_sync(0xffffffffu, move)) {
       // rescale O between PV_t(u-1) and PV_t(u), two 32-column loads in flight
       if (!(ok = wait_all(&S.bar_o[t][x ^ 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax))) break;
@@ -441,6 +447,12 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
         tmem_st32(o_addr + 32 * i, o);
         tmem_st32(o_addr + 32 * i + 32, o2);
       }
+      uint32_t o3[16];  // the row-sum columns
+      tmem_ld16_max(o_addr + 128, o3);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) o3[e] = __float_as_uint(__uint_as_float(o3[e]) * alpha);
+      tmem_st16(o_addr + 128, o3);
     }
     tmem_wait_st();
     tc_fence_before();
@@ -455,6 +467,8 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
   if (!wait_all(&S.bar_o[t][(n_sub - 1) & 1], ((n_sub - 1) >> 1) & 1, S, a, kRoleEpilogue))
     return;
   tc_fence_after();
+  const float l = __uint_as_float(tmem_ld1(o_addr + 128));  // sum of the dequantized P
+  tmem_wait_ld();
   const float f = __frcp_rn(l);
   const int qrow = (wi.qt0 + t) * kTile + wq * 32 + lane;
   const bool valid = qrow < sg.len;
@@ -537,6 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   for (int i = threadIdx.x; i < 4 * 64; i += kThreads)
     reinterpret_cast<uint4*>(S.fb[i >> 7][(i >> 6) & 1] + 1024)[i & 63] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < kStages * 64; i += kThreads)  // E2M1 1.0 = 0x2, two per byte
+    reinterpret_cast<uint4*>(S.v[i >> 6] + kCodeTile)[i & 63] =
+        make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();

@@ -7,6 +7,8 @@ module only builds it with g++ and marshals numpy arrays through ctypes.
 
 Sources followed (page title and section):
   * SGLang PR #40175 "add fp8_fa_sm120 FP8 backend for SM120 GPUs", Modifications.
+  * SGLang PR #40116 "Add SM120 Sage compute for SubBlock sparse attention", Modifications and
+    Accuracy Tests (block-sparse lists).
   * FlashInfer docs, ``flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4``,
     description and Parameters.
 """
@@ -64,6 +66,12 @@ def lib() -> ctypes.CDLL:
                                          f64, P, i64, P, P, i32]
             L.orc_attn_fp8.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, i32, i32, f64, P,
                                        i64, P, P, P, i32]
+            L.orc_attn_exact_sparse.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32,
+                                                P, i32, f64, P, P, P, i64, P, P, i32]
+            L.orc_attn_exact_sparse.restype = i32
+            L.orc_attn_fp8_sparse.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, P, P, i32,
+                                              f64, P, i64, P, P, P, i32]
+            L.orc_attn_fp8_sparse.restype = i32
             L.orc_nvfp4_kmean.argtypes = [P, i64, i64, i64, i32, P, i32, P, i32]
             L.orc_nvfp4_qblock_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_qblock_offsets.restype = i64
             L.orc_nvfp4_vgroup_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_vgroup_offsets.restype = i64
@@ -173,6 +181,56 @@ def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, tau=0
                        _p(cu), len(cu) - 1, float(scale), int(n_kv), int(p_shift), float(tau),
                        _p(rows),
                        rows.shape[0], _p(o64), _p(o16), _p(ls), _threads(nthreads))
+    return (o64, o16, ls) if lse else (o64, o16)
+
+
+# ------------------------------------------------------------------------------------------------
+# block-sparse (64-row query blocks x 64-key key blocks, reading r16)
+# ------------------------------------------------------------------------------------------------
+def _lists(blk_off, blk_idx):
+    off = np.ascontiguousarray(blk_off, np.int32)
+    idx = np.ascontiguousarray(blk_idx, np.int32)
+    if idx.size == 0:
+        idx = np.zeros(1, np.int32)
+    return off, idx
+
+
+def attn_exact_sparse(q, k, v, cu, blk_off, blk_idx, rows, scale, nthreads=0, lse=False):
+    """C1 under block lists -> out [n,128] float64 (and lse [n] with lse=True). Raises
+    ValueError when a list breaks the contract (index outside the segment, not ascending)."""
+    (qa, qst, qsh), (ka, kst, ksh), (va, vst, vsh) = _bf16_view(q), _bf16_view(k), _bf16_view(v)
+    cu = np.ascontiguousarray(cu, np.int32)
+    off, idx = _lists(blk_off, blk_idx)
+    rows = np.ascontiguousarray(rows, np.int64).reshape(-1, 2)
+    out = np.empty((rows.shape[0], D), np.float64)
+    ls = np.empty(rows.shape[0], np.float64)
+    st = lib().orc_attn_exact_sparse(_p(qa), qst, qsh, _p(ka), kst, ksh, _p(va), vst, vsh,
+                                     q.shape[0], q.shape[1], _p(cu), len(cu) - 1, float(scale),
+                                     _p(off), _p(idx), _p(rows), rows.shape[0], _p(out), _p(ls),
+                                     _threads(nthreads))
+    if st != 0:
+        raise ValueError("block list outside its segment or not strictly ascending")
+    return (out, ls) if lse else out
+
+
+def attn_fp8_sparse(cq, ck, cv, dq, dk, dv, cu, blk_off, blk_idx, rows, scale, p_shift=0,
+                    tau=0.0, nthreads=0, lse=False):
+    """C2 under block lists: the listed 64-key blocks, in list order, are the online softmax's
+    key tiles -> (out fp64 [n,128], out bf16 bits[, lse])."""
+    cq, ck, cv = (np.ascontiguousarray(a, np.uint8) for a in (cq, ck, cv))
+    dq, dk, dv = (np.ascontiguousarray(a, np.float32) for a in (dq, dk, dv))
+    cu = np.ascontiguousarray(cu, np.int32)
+    off, idx = _lists(blk_off, blk_idx)
+    rows = np.ascontiguousarray(rows, np.int64).reshape(-1, 2)
+    o64 = np.empty((rows.shape[0], D), np.float64)
+    o16 = np.empty((rows.shape[0], D), np.uint16)
+    ls = np.empty(rows.shape[0], np.float64)
+    st = lib().orc_attn_fp8_sparse(_p(cq), _p(ck), _p(cv), _p(dq), _p(dk), _p(dv), cq.shape[0],
+                                   cq.shape[1], _p(cu), len(cu) - 1, float(scale), _p(off),
+                                   _p(idx), int(p_shift), float(tau), _p(rows), rows.shape[0],
+                                   _p(o64), _p(o16), _p(ls), _threads(nthreads))
+    if st != 0:
+        raise ValueError("block list outside its segment or not strictly ascending")
     return (o64, o16, ls) if lse else (o64, o16)
 
 

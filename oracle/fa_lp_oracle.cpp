@@ -8,6 +8,9 @@
 //  * SGLang PR #40175 "add fp8_fa_sm120 FP8 backend for SM120 GPUs", section Modifications
 //    (kernel.py: E4M3 QK and PV with FP32 accumulation, online softmax, probabilities packed to
 //    E4M3; fused_prep.py: per-head amax then pack of strided BF16 Q/K/V).
+//  * SGLang PR #40116 "Add SM120 Sage compute for SubBlock sparse attention", Modifications
+//    (Q64 x K64 blocks, partial blocks, variable per-row block counts, mixed sparse and dense
+//    rows) and Accuracy Tests (ragged lengths, variable block counts, empty rows).
 //  * FlashInfer docs, flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4, the
 //    description paragraph (SageAttention3 FP4 recipe: K centred by the segment's per-channel
 //    mean, Q by its 128-row block mean with qm K^T added back, E2M1 codes with one UE4M3 scale per
@@ -36,6 +39,11 @@
 //  r12 the qm K^T term uses the dequantized centred K.
 //  r15 LSE of a row = m + log(l) in the natural units of S = q.k scale: the log of the normalizer
 //      of the (quantized) softmax the output divides by (exact attention: log sum exp(s)).
+//  r16 block-sparse attention (SGLang PR #40116, Modifications and Accuracy Tests): a query row
+//      in the g-th 64-row block of its segment attends to the keys of the 64-key blocks listed
+//      for (head, g), blocks counted from the segment start, the last one partial; lists are
+//      strictly ascending; a row with an empty list outputs 0 and has LSE -inf. The FP8 replay
+//      takes the listed blocks, in list order, as the online softmax's key tiles.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared -pthread (no fast-math), so that fp32
 // products and quotients are single IEEE round-to-nearest operations on any host.
@@ -208,6 +216,110 @@ void nvfp4_group(const float* x, int n, uint8_t* codes, uint8_t* sf_out) {
   }
 }
 
+// Key ranges [j0, j1) of one query row, in the order the online softmax visits them.
+using Ranges = std::vector<std::pair<int64_t, int64_t>>;
+
+// Exact FP64 attention of query row (t, h) over the keys of `keys`; no key gives 0 and LSE -inf.
+void exact_row(const uint16_t* q, int64_t qst, int64_t qsh, const uint16_t* k, int64_t kst,
+               int64_t ksh, const uint16_t* v, int64_t vst, int64_t vsh, int64_t t, int h,
+               const Ranges& keys, double scale, double* out, double* lse) {
+  std::vector<double> qi(kD), sc;
+  for (int c = 0; c < kD; ++c) qi[c] = load_bf16(q, t, h, c, qst, qsh);
+  double m = -std::numeric_limits<double>::infinity();
+  for (const auto& kr : keys)
+    for (int64_t j = kr.first; j < kr.second; ++j) {
+      double acc = 0.0;
+      for (int c = 0; c < kD; ++c) acc += qi[c] * static_cast<double>(load_bf16(k, j, h, c, kst, ksh));
+      sc.push_back(acc * scale);
+      m = std::max(m, sc.back());
+    }
+  double l = 0.0;
+  std::vector<double> o(kD, 0.0);
+  size_t i = 0;
+  for (const auto& kr : keys)
+    for (int64_t j = kr.first; j < kr.second; ++j, ++i) {
+      const double p = std::exp(sc[i] - m);
+      l += p;
+      for (int c = 0; c < kD; ++c) o[c] += p * load_bf16(v, j, h, c, vst, vsh);
+    }
+  for (int c = 0; c < kD; ++c) out[c] = l > 0.0 ? o[c] / l : 0.0;
+  if (lse) lse[0] = l > 0.0 ? m + std::log(l) : -std::numeric_limits<double>::infinity();
+}
+
+// FP8-emulating attention of query row (t, h) (C2 below) over the key tiles `tiles`, in order.
+void fp8_row(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv, const float* dq,
+             const float* dk, const float* dv, int H, int64_t t, int h, const Ranges& tiles,
+             double scale, int p_shift, double tau, double* out64, uint16_t* out16, double* lse) {
+  const double inf = std::numeric_limits<double>::infinity();
+  const double pscale = std::ldexp(1.0, p_shift);
+  const double tau_nat = tau * std::log(2.0);  // threshold in the natural-log units of S
+  const double sfac = static_cast<double>(dq[h]) * static_cast<double>(dk[h]) * scale;
+  double qi[kD];
+  for (int c = 0; c < kD; ++c) qi[c] = e4m3_decode(cq[(t * H + h) * kD + c]);
+  double m = -inf, l = 0.0;
+  std::vector<double> o(kD, 0.0), sc;
+  for (const auto& tile : tiles) {
+    const int64_t j0 = tile.first, j1 = tile.second;
+    sc.assign(j1 - j0, 0.0);
+    double mt = -inf;
+    for (int64_t j = j0; j < j1; ++j) {
+      double acc = 0.0;  // exact: products are multiples of 2^-18, |sum| < 2^25
+      for (int c = 0; c < kD; ++c) acc += qi[c] * e4m3_decode(ck[(j * H + h) * kD + c]);
+      sc[j - j0] = acc * sfac;
+      mt = std::max(mt, sc[j - j0]);
+    }
+    const double m_new = (m == -inf || mt > m + tau_nat) ? mt : m;
+    const double alpha = (m == -inf) ? 0.0 : std::exp(m - m_new);
+    l *= alpha;
+    for (int c = 0; c < kD; ++c) o[c] *= alpha;
+    for (int64_t j = j0; j < j1; ++j) {
+      const float pt = static_cast<float>(std::exp(sc[j - j0] - m_new) * pscale);
+      const double pq = e4m3_decode(e4m3_encode(pt)) / pscale;
+      if (pq == 0.0) continue;
+      l += pq;
+      for (int c = 0; c < kD; ++c) o[c] += pq * e4m3_decode(cv[(j * H + h) * kD + c]);
+    }
+    m = m_new;
+  }
+  for (int c = 0; c < kD; ++c) {
+    const double y = l > 0.0 ? o[c] * static_cast<double>(dv[h]) / l : 0.0;
+    out64[c] = y;
+    if (out16) out16[c] = f64_to_bf16(y);
+  }
+  // r15: the log of the quantized softmax normalizer, in the natural units of S
+  if (lse) lse[0] = l > 0.0 ? m + std::log(l) : -inf;
+}
+
+// r16: 64-row query blocks and 64-key key blocks, counted from each segment's first token.
+constexpr int kSparseBlock = 64;
+
+// First query block of every segment (qb0[s]) and the total G over the packed batch.
+int64_t sparse_qblock_offsets(const int32_t* cu, int nseg, std::vector<int64_t>& qb0) {
+  qb0.assign(nseg + 1, 0);
+  for (int s = 0; s < nseg; ++s)
+    qb0[s + 1] = qb0[s] + (cu[s + 1] - cu[s] + kSparseBlock - 1) / kSparseBlock;
+  return qb0[nseg];
+}
+
+// Key tiles of row (t, h) under the block lists; false if the list breaks the contract
+// (an index outside the segment's key blocks, or not strictly ascending).
+bool sparse_tiles(const int32_t* cu, int nseg, const std::vector<int64_t>& qb0, int64_t G,
+                  const int32_t* blk_off, const int32_t* blk_idx, int64_t t, int h, Ranges& out) {
+  const int s = segment_of(cu, nseg, t);
+  const int64_t a = cu[s], b = cu[s + 1];
+  const int64_t nkb = (b - a + kSparseBlock - 1) / kSparseBlock;
+  const int64_t g = qb0[s] + (t - a) / kSparseBlock;
+  out.clear();
+  int64_t prev = -1;
+  for (int64_t i = blk_off[h * G + g]; i < blk_off[h * G + g + 1]; ++i) {
+    const int64_t kb = blk_idx[i];
+    if (kb < 0 || kb >= nkb || kb <= prev) return false;
+    prev = kb;
+    out.push_back({a + kSparseBlock * kb, std::min(b, a + kSparseBlock * (kb + 1))});
+  }
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -268,25 +380,9 @@ void orc_attn_exact(const uint16_t* q, int64_t qst, int64_t qsh,
     const int64_t t = rows[2 * r];
     const int h = static_cast<int>(rows[2 * r + 1]);
     const int s = segment_of(cu, nseg, t);
-    const int64_t a = cu[s], b = cu[s + 1];
-    std::vector<double> qi(kD), sc(b - a);
-    for (int c = 0; c < kD; ++c) qi[c] = load_bf16(q, t, h, c, qst, qsh);
-    double m = -std::numeric_limits<double>::infinity();
-    for (int64_t j = a; j < b; ++j) {
-      double acc = 0.0;
-      for (int c = 0; c < kD; ++c) acc += qi[c] * static_cast<double>(load_bf16(k, j, h, c, kst, ksh));
-      sc[j - a] = acc * scale;
-      m = std::max(m, sc[j - a]);
-    }
-    double l = 0.0;
-    std::vector<double> o(kD, 0.0);
-    for (int64_t j = a; j < b; ++j) {
-      const double p = std::exp(sc[j - a] - m);
-      l += p;
-      for (int c = 0; c < kD; ++c) o[c] += p * load_bf16(v, j, h, c, vst, vsh);
-    }
-    for (int c = 0; c < kD; ++c) out[r * kD + c] = o[c] / l;
-    if (lse) lse[r] = m + std::log(l);  // log sum_j exp(s_j), s = q.k scale
+    const Ranges keys{{cu[s], cu[s + 1]}};
+    exact_row(q, qst, qsh, k, kst, ksh, v, vst, vsh, t, h, keys, scale, out + r * kD,
+              lse ? lse + r : nullptr);
   });
 }
 
@@ -304,50 +400,69 @@ void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
                   int p_shift, double tau, const int64_t* rows, int64_t nrows, double* out64,
                   uint16_t* out16, double* lse, int nthreads) {
   (void)T;
-  const double inf = std::numeric_limits<double>::infinity();
-  const double pscale = std::ldexp(1.0, p_shift);
-  const double tau_nat = tau * std::log(2.0);  // threshold in the natural-log units of S
   parallel_for(nrows, nthreads, [&](int64_t r) {
     const int64_t t = rows[2 * r];
     const int h = static_cast<int>(rows[2 * r + 1]);
     const int s = segment_of(cu, nseg, t);
-    const int64_t a = cu[s], b = cu[s + 1];
-    const double sfac = static_cast<double>(dq[h]) * static_cast<double>(dk[h]) * scale;
-    double qi[kD];
-    for (int c = 0; c < kD; ++c) qi[c] = e4m3_decode(cq[(t * H + h) * kD + c]);
-    double m = -inf, l = 0.0;
-    std::vector<double> o(kD, 0.0), sc;
-    for (int64_t j0 = a; j0 < b; j0 += n_kv) {
-      const int64_t j1 = std::min(b, j0 + n_kv);
-      sc.assign(j1 - j0, 0.0);
-      double mt = -inf;
-      for (int64_t j = j0; j < j1; ++j) {
-        double acc = 0.0;  // exact: products are multiples of 2^-18, |sum| < 2^25
-        for (int c = 0; c < kD; ++c) acc += qi[c] * e4m3_decode(ck[(j * H + h) * kD + c]);
-        sc[j - j0] = acc * sfac;
-        mt = std::max(mt, sc[j - j0]);
-      }
-      const double m_new = (m == -inf || mt > m + tau_nat) ? mt : m;
-      const double alpha = (m == -inf) ? 0.0 : std::exp(m - m_new);
-      l *= alpha;
-      for (int c = 0; c < kD; ++c) o[c] *= alpha;
-      for (int64_t j = j0; j < j1; ++j) {
-        const float pt = static_cast<float>(std::exp(sc[j - j0] - m_new) * pscale);
-        const double pq = e4m3_decode(e4m3_encode(pt)) / pscale;
-        if (pq == 0.0) continue;
-        l += pq;
-        for (int c = 0; c < kD; ++c) o[c] += pq * e4m3_decode(cv[(j * H + h) * kD + c]);
-      }
-      m = m_new;
-    }
-    for (int c = 0; c < kD; ++c) {
-      const double y = o[c] * static_cast<double>(dv[h]) / l;
-      out64[r * kD + c] = y;
-      if (out16) out16[r * kD + c] = f64_to_bf16(y);
-    }
-    // r15: the log of the quantized softmax normalizer, in the natural units of S
-    if (lse) lse[r] = m + std::log(l);
+    Ranges tiles;
+    for (int64_t j0 = cu[s]; j0 < cu[s + 1]; j0 += n_kv)
+      tiles.push_back({j0, std::min<int64_t>(cu[s + 1], j0 + n_kv)});
+    fp8_row(cq, ck, cv, dq, dk, dv, H, t, h, tiles, scale, p_shift, tau, out64 + r * kD,
+            out16 ? out16 + r * kD : nullptr, lse ? lse + r : nullptr);
   });
+}
+
+// ---------------------------------------------------------------------------------------------
+// C1 and C2 under block-sparse lists (r16). blk_off: int32 [H * G + 1], the list of (head h,
+// query block g) is blk_idx[blk_off[h G + g], blk_off[h G + g + 1]); G = sum over segments of
+// ceil(L_s / 64). Return 0, or -1 when a row's list breaks the contract (its output is then 0).
+// ---------------------------------------------------------------------------------------------
+int orc_attn_exact_sparse(const uint16_t* q, int64_t qst, int64_t qsh,
+                          const uint16_t* k, int64_t kst, int64_t ksh,
+                          const uint16_t* v, int64_t vst, int64_t vsh, int64_t T, int H,
+                          const int32_t* cu, int nseg, double scale, const int32_t* blk_off,
+                          const int32_t* blk_idx, const int64_t* rows, int64_t nrows,
+                          double* out, double* lse, int nthreads) {
+  (void)T; (void)H;
+  std::vector<int64_t> qb0;
+  const int64_t G = sparse_qblock_offsets(cu, nseg, qb0);
+  std::vector<int> bad(nrows, 0);
+  parallel_for(nrows, nthreads, [&](int64_t r) {
+    const int64_t t = rows[2 * r];
+    const int h = static_cast<int>(rows[2 * r + 1]);
+    Ranges keys;
+    if (!sparse_tiles(cu, nseg, qb0, G, blk_off, blk_idx, t, h, keys)) {
+      bad[r] = 1;
+      keys.clear();
+    }
+    exact_row(q, qst, qsh, k, kst, ksh, v, vst, vsh, t, h, keys, scale, out + r * kD,
+              lse ? lse + r : nullptr);
+  });
+  return std::count(bad.begin(), bad.end(), 1) ? -1 : 0;
+}
+
+int orc_attn_fp8_sparse(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
+                        const float* dq, const float* dk, const float* dv, int64_t T, int H,
+                        const int32_t* cu, int nseg, double scale, const int32_t* blk_off,
+                        const int32_t* blk_idx, int p_shift, double tau, const int64_t* rows,
+                        int64_t nrows, double* out64, uint16_t* out16, double* lse,
+                        int nthreads) {
+  (void)T;
+  std::vector<int64_t> qb0;
+  const int64_t G = sparse_qblock_offsets(cu, nseg, qb0);
+  std::vector<int> bad(nrows, 0);
+  parallel_for(nrows, nthreads, [&](int64_t r) {
+    const int64_t t = rows[2 * r];
+    const int h = static_cast<int>(rows[2 * r + 1]);
+    Ranges tiles;
+    if (!sparse_tiles(cu, nseg, qb0, G, blk_off, blk_idx, t, h, tiles)) {
+      bad[r] = 1;
+      tiles.clear();
+    }
+    fp8_row(cq, ck, cv, dq, dk, dv, H, t, h, tiles, scale, p_shift, tau, out64 + r * kD,
+            out16 ? out16 + r * kD : nullptr, lse ? lse + r : nullptr);
+  });
+  return std::count(bad.begin(), bad.end(), 1) ? -1 : 0;
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -26,7 +26,13 @@ WORKLOADS = {
     # NVFP4 at the H3 shape, and a small case of the same kernel (profiling)
     "nvfp4_s30272_h56": dict(cu=[0, 30272], heads=56),
     "nvfp4_s4096_h56": dict(cu=[0, 4096], heads=56),
+    # block-sparse FP8 at the H3 shape: 64-row query blocks x 64-key blocks, about a quarter of
+    # the key blocks listed per query block (the pages' sparsity 0.75), and a small case
+    "sparse_fp8_s30272_h56": dict(cu=[0, 30272], heads=56, density=0.25),
+    "sparse_fp8_s4096_h56": dict(cu=[0, 4096], heads=56, density=0.25),
 }
+
+SPARSE_BLOCK = 64  # rows of a query block and keys of a key block of the block-sparse lists
 
 
 def gaussian_bf16(shape, seed: int, std: float = 1.0) -> torch.Tensor:
@@ -66,3 +72,46 @@ def sample_rows(cu, heads: int, n_heads: int, n_rows: int, seed: int):
         return []
     ts = torch.randint(0, tokens, (n_rows,), generator=g).tolist()
     return [(t, h) for h in hs for t in sorted(ts)]
+
+
+def block_sparse_lists(cu, heads: int, density: float, seed: int, dense_every: int = 0,
+                       empty_every: int = 0):
+    """A seeded block-sparse pattern in the form the block-sparse forward takes.
+
+    Query blocks are the 64-row blocks of every segment (counted from the segment's first token,
+    the last one partial), numbered g = 0 .. G-1 over the segments in order; key blocks are the
+    64-key blocks of the same segment. For every (head h, query block g) the list holds distinct
+    key-block indices in ascending order: its length is density x (key blocks of the segment) x
+    u, u uniform in [0.5, 1.5), rounded, at least 1; its blocks are drawn uniformly without
+    replacement. Every `dense_every`-th list (counted over h G + g) names every key block and
+    every `empty_every`-th none (mixed sparse/dense rows and empty rows). Returns (offsets int32
+    [H G + 1], indices int32 [nnz]); the list of (h, g) is indices[offsets[h G + g] :
+    offsets[h G + g + 1]]."""
+    import numpy as np
+
+    rng = np.random.default_rng(int(seed))
+    lens = [int(b) - int(a) for a, b in zip(cu[:-1], cu[1:])]
+    nblk = [(L + SPARSE_BLOCK - 1) // SPARSE_BLOCK for L in lens]
+    G = sum(nblk)
+    lists = [[None] * G for _ in range(heads)]
+    g0 = 0
+    for n in nblk:  # a segment of n blocks: n query blocks, each choosing among n key blocks
+        if n == 0:
+            continue
+        k = np.clip(np.rint(density * n * (0.5 + rng.random((heads, n)))), 1, n).astype(np.int64)
+        ranks = np.argsort(np.argsort(rng.random((heads, n, n)), axis=2), axis=2)
+        for h in range(heads):
+            for i in range(n):
+                j = h * G + g0 + i
+                if empty_every and j % empty_every == empty_every - 1:
+                    lists[h][g0 + i] = np.zeros(0, np.int64)
+                elif dense_every and j % dense_every == dense_every - 1:
+                    lists[h][g0 + i] = np.arange(n)
+                else:
+                    lists[h][g0 + i] = np.nonzero(ranks[h, i] < k[h, i])[0]
+        g0 += n
+    flat = [lists[h][g] for h in range(heads) for g in range(G)]
+    offsets = np.zeros(heads * G + 1, np.int64)
+    offsets[1:] = np.cumsum([len(x) for x in flat])
+    idx = np.concatenate(flat) if flat else np.zeros(0, np.int64)
+    return offsets.astype(np.int32), idx.astype(np.int32)

@@ -38,6 +38,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "E4M3 varlen attn TFLOPS at S=30272,H=56,D=128; % of FP8 tensor peak"
 METRIC_NVFP4 = "NVFP4 varlen attn TFLOPS at S=30272,H=56,D=128; % of FP4 tensor peak"
+METRIC_SPARSE = ("Block-sparse E4M3 attn TFLOPS (listed 64x64 blocks) at S=30272,H=56,D=128, "
+                 "density 0.25; % of FP8 tensor peak")
 UNIT = "TFLOPS"
 D = 128
 # dense FP8 and FP4 over dense BF16 tensor rate of the part (nominal 4.5, 13.5 / 2.25 PFLOP/s)
@@ -45,7 +47,8 @@ FP8_OVER_BF16 = 2.0
 FP4_OVER_BF16 = 6.0
 # kernels per step: FP8 amax, pack Q/K, pack V^T, attention; NVFP4 block sums, K means, pack
 # Q/K, pack V^T, attention
-KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5}
+KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5, "sparse": 5}
+METRICS = {"fp8": METRIC, "nvfp4": METRIC_NVFP4, "sparse": METRIC_SPARSE}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes) of one attention launch from
 # an ncu capture of the full-size workload (profiles/attn_traffic_s30272_h56.md), keyed by the
@@ -78,7 +81,43 @@ def workload(name):
 
 
 def mode_of(name):
-    return "nvfp4" if name.startswith("nvfp4") else "fp8"
+    if name.startswith("nvfp4"):
+        return "nvfp4"
+    return "sparse" if name.startswith("sparse") else "fp8"
+
+
+def sparse_lists(name, cu, H, seed=0):
+    """The block lists of a block-sparse workload (every 16th list dense)."""
+    from precision_attention_diffusion_gb300 import inputs
+    return inputs.block_sparse_lists(cu, H, density=inputs.WORKLOADS[name]["density"], seed=seed,
+                                     dense_every=16)
+
+
+def sparse_flops(cu, H, off, idx):
+    """4 D x (query rows x listed keys) summed over every (head, 64-row block)."""
+    import numpy as np
+    rows_g, keys_s, seg_g = [], [], []
+    for s, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        L = b - a
+        n = -(-L // 64)
+        rows_g += [min(64, L - 64 * i) for i in range(n)]
+        seg_g += [s] * n
+        keys_s.append(L)
+    rows_g = np.asarray(rows_g, np.float64)
+    G = len(rows_g)
+    total = 0.0
+    off = np.asarray(off, np.int64)
+    idx = np.asarray(idx, np.int64)
+    lens = np.asarray(keys_s)
+    for j in range(H * G):
+        g = j % G
+        lst = idx[off[j]:off[j + 1]]
+        if len(lst) == 0:
+            continue
+        L = lens[seg_g[g]]
+        keys = 64.0 * len(lst) - (64 * (lst[-1] + 1) - L if 64 * (lst[-1] + 1) > L else 0)
+        total += rows_g[g] * keys
+    return 4.0 * D * total
 
 
 def attn_flops(cu, H):
@@ -158,10 +197,11 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------
 # CPU oracle on a bounded sample of the workload (the cpu_baseline object and the reference arm)
 # ------------------------------------------------------------------------------------------------
-def oracle_sample(cu, H, seconds, seed=0, mode="fp8"):
+def oracle_sample(cu, H, seconds, seed=0, mode="fp8", sparse_name=None):
     """Time the oracle (as it stands, all host threads) on head 0 of the workload: quantize
-    that head's full Q/K/V, then emulating attention (FP8 or NVFP4) of R query rows of the
-    longest segment. Extrapolates to the whole workload: per head, quantize once + L rows."""
+    that head's full Q/K/V, then emulating attention (FP8, NVFP4 or block-sparse FP8) of R query
+    rows of the longest segment. Extrapolates to the whole workload: per head, quantize once + L
+    rows (a block-sparse row visits its listed keys: random rows sample the mean)."""
     import numpy as np
     import torch
 
@@ -179,6 +219,11 @@ def oracle_sample(cu, H, seconds, seed=0, mode="fp8"):
         z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
     else:
         qz = [oracle.fp8_quantize(bits(x)) for x in (q, k, v)]
+    if mode == "sparse":  # head 0's lists of the workload's pattern (one head: offsets [G + 1])
+        off_all, idx_all = sparse_lists(sparse_name, cu, H)
+        G = (len(off_all) - 1) // H
+        off0 = off_all[:G + 1].copy()
+        idx0 = idx_all[:off0[-1]].copy()
     t_quant = time.perf_counter() - t0
     ncores = os.cpu_count() or 1
     g = np.random.default_rng(seed)
@@ -188,6 +233,9 @@ def oracle_sample(cu, H, seconds, seed=0, mode="fp8"):
         t1 = time.perf_counter()
         if mode == "nvfp4":
             oracle.attn_nvfp4(z, cu, rows, 1.0 / math.sqrt(D), n_kv=64)
+        elif mode == "sparse":
+            oracle.attn_fp8_sparse(qz[0][0], qz[1][0], qz[2][0], qz[0][1], qz[1][1], qz[2][1], cu,
+                                   off0, idx0, rows, 1.0 / math.sqrt(D), tau=8.0)
         else:
             oracle.attn_fp8(qz[0][0], qz[1][0], qz[2][0], qz[0][1], qz[1][1], qz[2][1], cu, rows,
                             1.0 / math.sqrt(D))
@@ -205,8 +253,12 @@ def oracle_sample(cu, H, seconds, seed=0, mode="fp8"):
     # full-workload estimate: each head quantizes once and runs every query row of every segment
     per_row = t_attn / R
     # per-row cost grows with its segment's length: scale by L_s / L_longest
-    est_s = H * (t_quant + per_row * sum(x * x for x in lens) / L)
-    value = attn_flops(cu, H) / est_s / 1e12
+    if mode == "sparse":
+        est_s = H * (t_quant + per_row * T)
+        value = sparse_flops(cu, H, off_all, idx_all) / est_s / 1e12
+    else:
+        est_s = H * (t_quant + per_row * sum(x * x for x in lens) / L)
+        value = attn_flops(cu, H) / est_s / 1e12
     return dict(value=value, unit=UNIT, cores=ncores, kind="oracle",
                 sample=(f"head 0 of {H}: {mode.upper()} quantize of its full Q/K/V ({T} tokens, "
                         f"{t_quant:.2f} s) + {mode.upper()}-emulating attention of {R} random query "
@@ -245,15 +297,15 @@ def run_reference(args):
     per_step = max(args.cpu_seconds / 3.0, 3.0)
     mode = mode_of(args.workload)
     for _ in range(args.warmup):
-        oracle_sample(cu, H, per_step / 2, mode=mode)
+        oracle_sample(cu, H, per_step / 2, mode=mode, sparse_name=args.workload)
     vals, secs = [], []
     for i in range(args.steps):
-        r = oracle_sample(cu, H, per_step, seed=i, mode=mode)
+        r = oracle_sample(cu, H, per_step, seed=i, mode=mode, sparse_name=args.workload)
         vals.append(r["value"])
         secs.append(r["est_full_workload_s"])
     v = statistics.median(vals)
     line = {
-        "impl": "reference", "metric": METRIC_NVFP4 if mode == "nvfp4" else METRIC, "value": v,
+        "impl": "reference", "metric": METRICS[mode], "value": v,
         "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.median(secs) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
@@ -276,6 +328,10 @@ def config_of(name, cu, H):
          "l2": "inputs (1.3 GB) and codes larger than L2: no flush"}
     if mode_of(name) == "nvfp4":
         c["k_offset"] = "per-(head, channel) K offset N(0, 4), constant over tokens"
+    if mode_of(name) == "sparse":
+        c["block_lists"] = ("64-row query blocks x 64-key blocks; per list density 0.25 x "
+                            "U[0.5, 1.5) of the key blocks, uniform without replacement, "
+                            "every 16th list dense (seed 0)")
     return c
 
 
@@ -299,6 +355,12 @@ def run_ours(args):
     mode = mode_of(args.workload)
     T = cu[-1]
     flops = attn_flops(cu, H)
+    if mode == "sparse":
+        import numpy as np
+        off_h, idx_h = sparse_lists(args.workload, cu, H, seed=rank)
+        flops = sparse_flops(cu, H, off_h, idx_h)
+        d_off = torch.from_numpy(off_h).cuda()
+        d_idx = torch.from_numpy(idx_h).cuda()
     g = torch.Generator(device="cuda").manual_seed(1234 + rank)
     buf = torch.randn((T, 3, H, D), generator=g, device="cuda", dtype=torch.float32)
     if mode == "nvfp4":
@@ -311,9 +373,15 @@ def run_ours(args):
     plan = fa_lp.Plan(cu, H, mode=fa_lp.MODE_NVFP4 if mode == "nvfp4" else fa_lp.MODE_FP8)
     stream = torch.cuda.current_stream()
 
+    def forward():
+        if mode == "sparse":
+            plan.forward_sparse(d_off, d_idx, out, stream)
+        else:
+            plan.forward(out, cu_dev, stream)
+
     def step():
         plan.quantize(q, k, v, stream)
-        plan.forward(out, cu_dev, stream)
+        forward()
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -348,7 +416,7 @@ def run_ours(args):
         plan.quantize(q, k, v, stream)
         evq[i][1].record(stream)
         evf[i][0].record(stream)
-        plan.forward(out, cu_dev, stream)
+        forward()
         evf[i][1].record(stream)
     ev[1].record(stream)
     torch.cuda.synchronize()
@@ -368,7 +436,44 @@ def run_ours(args):
     # output back; the library overlaps the copies of one chunk of heads with the compute of the
     # next
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and mode == "sparse":
+        # block-sparse: every step copies Q/K/V and the block lists from page-locked host memory,
+        # quantizes, runs the block-sparse forward and copies the output back, on one stream
+        hbuf = buf.cpu().pin_memory()
+        hout = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
+        hoff = torch.from_numpy(off_h).pin_memory()
+        hidx = torch.from_numpy(idx_h).pin_memory()
+        dbuf = torch.empty_like(buf)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                dbuf.copy_(hbuf, non_blocking=True)
+                d_off.copy_(hoff, non_blocking=True)
+                d_idx.copy_(hidx, non_blocking=True)
+                plan.quantize(dbuf[:, 0], dbuf[:, 1], dbuf[:, 2], stream)
+                plan.forward_sparse(d_off, d_idx, out, stream)
+                hout.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / K)
+        if plan.last_error():
+            raise RuntimeError("device error in the end-to-end region")
+        in_bytes = (hbuf.numel() * hbuf.element_size() + hoff.numel() * 4 + hidx.numel() * 4)
+        e2e = {"value": ws * flops / (e_ms / 1e3) / 1e12, "unit": UNIT,
+               "ms_per_step": e_ms, "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "call": "fa_lp_quantize + fa_lp_forward_sparse with host-to-device copies of "
+                       "Q/K/V and the block lists and the copy-out, serial on one stream"}
+    elif not args.no_e2e:
         hbuf = buf.cpu().pin_memory()
         hout = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
         hq, hk, hv = hbuf[:, 0], hbuf[:, 1], hbuf[:, 2]
@@ -398,7 +503,7 @@ def run_ours(args):
 
     pk = peaks()
     achieved = flops / (fwd_ms / 1e3) / 1e12
-    kname = "attn_nvfp4" if mode == "nvfp4" else "attn_fp8"
+    kname = {"nvfp4": "attn_nvfp4", "fp8": "attn_fp8", "sparse": "attn_fp8_sparse"}[mode]
     sha = file_sha(os.path.join(ROOT, "precision_attention_diffusion_gb300", "csrc", kname + ".cu"))
     traffic = NCU_TRAFFIC.get((args.workload, sha))
     pkey = "fp4" if mode == "nvfp4" else "fp8"
@@ -421,8 +526,12 @@ def run_ours(args):
         # quantize passes: HBM-bound; algorithmic bytes = 2 reads of Q/K/V + 1 write of the codes
         q_bytes = 2 * 3 * T * H * D * 2 + 3 * T * H * D
         dtype = "fp8_e4m3 (fp32 accumulate, bf16 in/out)"
+    if mode == "sparse":
+        roof["algorithmic_flops_per_launch"] = flops
+        roof["launch_note"] = ("forward_ms covers the list merge (one small kernel) and the "
+                               "attention kernel")
     line = {
-        "metric": METRIC_NVFP4 if mode == "nvfp4" else METRIC, "value": value, "unit": UNIT,
+        "metric": METRICS[mode], "value": value, "unit": UNIT,
         "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype,
@@ -434,7 +543,8 @@ def run_ours(args):
         "gpu_launches": KERNELS_PER_STEP[mode] * K,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds, mode=mode)
+        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds, mode=mode,
+                                             sparse_name=args.workload)
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

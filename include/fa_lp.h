@@ -181,6 +181,45 @@ FA_LP_API int fa_lp_forward_varlen_lse(fa_lp_plan* plan, const int32_t* cu_seqle
                                        int64_t out_stride_tok, int64_t out_stride_head, float* lse,
                                        int64_t lse_stride_head, void* stream);
 
+/*
+ * fa_lp_forward_sparse -- block-sparse attention on the plan's quantized operands (FP8 plans).
+ * Passage: SGLang PR #40116 "Add SM120 Sage compute for SubBlock sparse attention",
+ * Modifications (64-row query blocks x 64-key blocks, a key block being 4 pooling cells of 16
+ * keys; partial blocks; variable per-row block counts, mixed sparse and dense query rows) and
+ * Accuracy Tests (ragged lengths, variable block counts, empty rows). Reading taken here: a
+ * query row in the g-th 64-row block of its segment attends to the keys of the 64-key blocks
+ * listed for (head, g) -- block kb covers keys [64 kb, min(64 kb + 64, L_s)) of the segment --
+ * with the arithmetic of fa_lp_forward_varlen (E4M3 Q K^T and P V, FP32 accumulation, online
+ * softmax with the lazy reference maximum over the listed blocks in list order, l from the
+ * quantized P); a row whose list is empty is written as 0 (LSE -inf). The pages' SM120 mode
+ * takes Q K^T in INT8; here both products are E4M3, on the same quantized operands as the dense
+ * forward (call fa_lp_quantize first).
+ *   block_offsets : device int32 [heads * G + 1], non-decreasing, block_offsets[0] >= 0; the list
+ *                   of (head h, query block g) is block_indices[block_offsets[h G + g] ..
+ *                   block_offsets[h G + g + 1]). G = fa_lp_sparse_query_blocks(plan) = sum over
+ *                   segments of ceil(L_s / 64); query blocks are numbered over the segments in
+ *                   order (empty segments have none).
+ *   block_indices : device int32 [num_indices]; every list strictly ascending, entries in
+ *                   [0, ceil(L_s / 64)) of the query block's segment.
+ *   num_indices   : length of block_indices; no read goes past it.
+ *   out, strides, lse, lse_stride_head : as fa_lp_forward_varlen_lse (lse may be NULL).
+ * The lists are read on the device: a list that breaks the contract has its offending entries
+ * dropped (its rows' output is then unspecified, but no access leaves the arrays) and
+ * fa_lp_get_last_error reports status 0x200 and returns FA_LP_ERR_INVALID_ARG.
+ * Device memory: the plan keeps a scratch buffer of 4 * num_indices + 12 * heads * (Tpad / 128)
+ * bytes (merged lists and tile tables), grown stream-ordered on `stream` when a call needs more.
+ * Errors: STATE (no quantize on this plan yet), UNSUPPORTED (NVFP4 plan, or a segment longer
+ * than 12.5 M tokens), INVALID_ARG, OOM, CUDA.
+ */
+FA_LP_API int fa_lp_forward_sparse(fa_lp_plan* plan, const int32_t* cu_seqlens_dev,
+                                   const int32_t* block_offsets, const int32_t* block_indices,
+                                   int64_t num_indices, void* out, int64_t out_stride_tok,
+                                   int64_t out_stride_head, float* lse, int64_t lse_stride_head,
+                                   void* stream);
+
+/* Number G of 64-row query blocks of the plan (the block lists of fa_lp_forward_sparse). */
+FA_LP_API int fa_lp_sparse_query_blocks(const fa_lp_plan* plan, int64_t* num_query_blocks);
+
 /* fa_lp_attention -- fa_lp_quantize followed by fa_lp_forward_varlen on the same stream: the
  * one-call form out = attention(q, k, v, cu_seqlens) of the FlashInfer op's signature. */
 FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_tok,
@@ -266,8 +305,10 @@ FA_LP_API int fa_lp_copy_quantized(const fa_lp_plan* plan, int which, void* dst,
 
 /*
  * fa_lp_get_last_error -- device-side status of the plan's kernels: 0 when every bounded
- * device wait completed, otherwise a code with the waiting role in its low byte. Reading it
- * synchronizes the device and clears it. Returns FA_LP_ERR_DEVICE_TIMEOUT when non-zero.
+ * device wait completed and every block list was valid; 0x1RR when a wait expired (RR = the
+ * waiting role), returning FA_LP_ERR_DEVICE_TIMEOUT; 0x200 when fa_lp_forward_sparse met a block
+ * list that breaks its contract, returning FA_LP_ERR_INVALID_ARG. The first error is kept.
+ * Reading it synchronizes the device and clears it.
  */
 FA_LP_API int fa_lp_get_last_error(fa_lp_plan* plan, int* device_status);
 

@@ -89,12 +89,14 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   const size_t n_wrk = p->work.size() * sizeof(WorkItem);
   const size_t n_qmk = p->qmk_items.size() * sizeof(QmkItem);
   const size_t n_cof = p->c_off.size() * sizeof(int64_t);
+  const size_t n_qb0 = p->sp_qb0.size() * sizeof(int32_t);
   const size_t o_seg = 0;
   const size_t o_blk = align_up(o_seg + n_seg, 256);
   const size_t o_wrk = align_up(o_blk + n_blk, 256);
   const size_t o_qmk = align_up(o_wrk + n_wrk, 256);
   const size_t o_cof = align_up(o_qmk + n_qmk, 256);
-  const size_t o_err = align_up(o_cof + n_cof, 256);
+  const size_t o_qb0 = align_up(o_cof + n_cof, 256);
+  const size_t o_err = align_up(o_qb0 + n_qb0, 256);
   const size_t total = o_err + 256;
   void* d = nullptr;
   if (cudaMalloc(&d, total) != cudaSuccess) {
@@ -107,6 +109,7 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   if (n_wrk) std::memcpy(host.data() + o_wrk, p->work.data(), n_wrk);
   if (n_qmk) std::memcpy(host.data() + o_qmk, p->qmk_items.data(), n_qmk);
   if (n_cof) std::memcpy(host.data() + o_cof, p->c_off.data(), n_cof);
+  if (n_qb0) std::memcpy(host.data() + o_qb0, p->sp_qb0.data(), n_qb0);
   if (cudaMemcpyAsync(d, host.data(), total, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaFree(d);
@@ -120,6 +123,7 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   p->d_work = reinterpret_cast<WorkItem*>(b + o_wrk);
   p->d_qmk = reinterpret_cast<QmkItem*>(b + o_qmk);
   p->d_coff = reinterpret_cast<int64_t*>(b + o_cof);
+  p->d_sp_qb0 = reinterpret_cast<int32_t*>(b + o_qb0);
   p->d_err = reinterpret_cast<int*>(b + o_err);
   if (log_enabled())
     std::fprintf(stderr, "[fa_lp] plan %p: device tables %zu bytes on device %d\n", (void*)p,
@@ -232,6 +236,14 @@ void build_plan(fa_lp_plan* p) {
   }
   p->row_off[ns] = row;
   p->tpad = row;
+  // block-sparse lists: 64-row query blocks and 64-key blocks per segment
+  p->sp_qb0.assign(ns, 0);
+  for (int s = 0; s < ns; ++s) {
+    const int64_t nkb = (int64_t(p->cu[s + 1]) - p->cu[s] + 63) / 64;
+    p->sp_qb0[s] = int32_t(p->sp_G);
+    p->sp_G += nkb;
+    p->sp_nw_max = std::max<int>(p->sp_nw_max, int((nkb + 31) / 32));
+  }
 
   // Work list: longest segment first (LPT); within a segment, blocks of kHeadGroup heads, and in
   // a block the query-tile pairs of its heads interleaved. The CTAs resident at one time then
@@ -428,11 +440,16 @@ int fa_lp_plan_destroy(fa_lp_plan* p) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (--p->refcount > 0) return FA_LP_OK;
     g_plans.erase(key_of(*p));
-    if (p->dmeta || p->host.buf || p->host.s_in) {
+    if (p->dmeta || p->host.buf || p->host.s_in || p->sp_buf) {
       int cur = -1;
       cudaGetDevice(&cur);
       if (cur != p->device) cudaSetDevice(p->device);
       st = host_pipe_release(p, subs);
+      if (p->sp_buf &&
+          (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->sp_buf) != cudaSuccess)) {
+        cudaGetLastError();
+        st = FA_LP_ERR_CUDA;
+      }
       if (p->dmeta &&
           (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dmeta) != cudaSuccess)) {
         cudaGetLastError();
@@ -530,6 +547,66 @@ int fa_lp_forward_varlen_lse(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void*
 int fa_lp_forward_varlen(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out, int64_t ost,
                          int64_t osh, void* stream_) {
   return fa_lp_forward_varlen_lse(p, cu_seqlens_dev, out, ost, osh, nullptr, 0, stream_);
+}
+
+int fa_lp_sparse_query_blocks(const fa_lp_plan* p, int64_t* num_query_blocks) {
+  if (!p || !num_query_blocks) return FA_LP_ERR_INVALID_ARG;
+  *num_query_blocks = p->sp_G;
+  return FA_LP_OK;
+}
+
+int fa_lp_forward_sparse(fa_lp_plan* p, const int32_t* cu_seqlens_dev,
+                         const int32_t* block_offsets, const int32_t* block_indices,
+                         int64_t num_indices, void* out, int64_t ost, int64_t osh, float* lse,
+                         int64_t lse_stride_head, void* stream_) {
+  (void)cu_seqlens_dev;
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  if (p->mode != FA_LP_MODE_FP8) return FA_LP_ERR_UNSUPPORTED;
+  if (!p->quantized) return FA_LP_ERR_STATE;
+  if (p->tokens > 0 && bad_view(out, ost, osh)) return FA_LP_ERR_INVALID_ARG;
+  if (num_indices < 0 || (p->tokens > 0 && !block_offsets) || (num_indices > 0 && !block_indices))
+    return FA_LP_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(block_offsets) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(block_indices) % 4 != 0)
+    return FA_LP_ERR_INVALID_ARG;
+  if (lse && p->tokens > 0 &&
+      (lse_stride_head < p->tokens || reinterpret_cast<uintptr_t>(lse) % 4 != 0))
+    return FA_LP_ERR_INVALID_ARG;
+  // the list merge keeps two key-block bitmaps of the longest segment in 48 KB of shared memory
+  if (size_t(p->sp_nw_max) * 8 > 48 * 1024) return FA_LP_ERR_UNSUPPORTED;
+  int st = check_current_device(p);
+  if (st != FA_LP_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const DevWs& w = g_ws[p->device];
+    if (!w.ptr || w.bytes < p->ws.total) return FA_LP_ERR_STATE;
+    base = w.ptr;
+    // per-plan scratch: merged lists (as many entries as the lists) + tile tables; grow-only,
+    // stream-ordered
+    const size_t nb = p->blocks.size(), H = size_t(p->heads);
+    const size_t tables = align_up(size_t(std::max<int64_t>(num_indices, 1)) * 4, 256);
+    const size_t need = tables + H * nb * (8 + 4);
+    if (p->sp_bytes < need) {
+      if (p->sp_buf && cudaFreeAsync(p->sp_buf, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_LP_ERR_CUDA;
+      }
+      p->sp_buf = nullptr;
+      p->sp_bytes = 0;
+      if (cudaMallocAsync(&p->sp_buf, need, stream) != cudaSuccess) {
+        cudaGetLastError();
+        p->sp_buf = nullptr;
+        return FA_LP_ERR_OOM;
+      }
+      p->sp_bytes = need;
+    }
+    p->sp_tables = align_up(size_t(std::max<int64_t>(num_indices, 1)) * 4, 256);
+  }
+  if (p->work.empty()) return FA_LP_OK;
+  return falp::launch_fp8_sparse(*p, static_cast<uint8_t*>(base), block_offsets, block_indices,
+                                 num_indices, out, ost, osh, lse, lse_stride_head, stream);
 }
 
 int fa_lp_attention(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
@@ -760,7 +837,8 @@ int fa_lp_get_last_error(fa_lp_plan* p, int* device_status) {
     if (v == 0) v = sv;
   }
   *device_status = v;
-  return v ? FA_LP_ERR_DEVICE_TIMEOUT : FA_LP_OK;
+  if (v == 0) return FA_LP_OK;
+  return (v & 0xF00) == 0x200 ? FA_LP_ERR_INVALID_ARG : FA_LP_ERR_DEVICE_TIMEOUT;
 }
 
 int fa_lp_release_workspace(int device, void* stream) {

@@ -94,6 +94,12 @@ struct fa_lp_plan {
   std::vector<falp::QmkItem> qmk_items;          // NVFP4 qm K^T table tiles
   std::vector<int64_t> c_off;                    // NVFP4: float offset of each segment's table
   falp::WsLayout ws;
+  // block-sparse forward (FP8 plans): 64-row query blocks
+  int64_t sp_G = 0;                   // query blocks over the packed batch
+  std::vector<int32_t> sp_qb0;        // first query block of every segment
+  int sp_nw_max = 0;                  // 32-bit words of the largest segment's key-block bitmap
+  void* sp_buf = nullptr;             // merged lists (u32 [num_indices]) + tile tables
+  size_t sp_bytes = 0, sp_tables = 0; // its size; byte offset of the tables (i64 + i32 [H][nb])
   int64_t spin_limit = 20000;  // parked probes of <= 100 us each: about 2 s per wait
   // device metadata (created on first use on the plan's device)
   void* dmeta = nullptr;
@@ -102,6 +108,7 @@ struct fa_lp_plan {
   falp::WorkItem* d_work = nullptr;
   falp::QmkItem* d_qmk = nullptr;
   int64_t* d_coff = nullptr;
+  int32_t* d_sp_qb0 = nullptr;
   int* d_err = nullptr;  // [0]: sticky device status, [1]: abort word (launch generation)
   bool quantized = false;
   int refcount = 1;
@@ -129,6 +136,9 @@ int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64
                           int64_t vst, int64_t vsh, cudaStream_t stream);
 int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
                            float* lse, int64_t lse_sh, cudaStream_t stream);
+int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* block_offsets,
+                      const int32_t* block_indices, int64_t num_indices, void* out, int64_t ost,
+                      int64_t osh, float* lse, int64_t lse_sh, cudaStream_t stream);
 int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, cudaStream_t stream);
 int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
 

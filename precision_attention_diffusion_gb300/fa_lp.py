@@ -36,7 +36,7 @@ EXPORTS = (
     "fa_lp_plan_row_offsets", "fa_lp_get_quantized", "fa_lp_copy_quantized",
     "fa_lp_get_last_error", "fa_lp_plan_set_wait_limit", "fa_lp_release_workspace",
     "fa_lp_encode", "fa_lp_fp8_descale_noalloc", "fa_lp_forward_varlen_lse",
-    "fa_lp_attention_host",
+    "fa_lp_attention_host", "fa_lp_forward_sparse", "fa_lp_sparse_query_blocks",
 )
 
 _lib = None
@@ -84,6 +84,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.fa_lp_quantize.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P]
         L.fa_lp_forward_varlen.argtypes = [P, P, P, i64, i64, P]
         L.fa_lp_forward_varlen_lse.argtypes = [P, P, P, i64, i64, P, i64, P]
+        L.fa_lp_forward_sparse.argtypes = [P, P, P, P, i64, P, i64, i64, P, i64, P]
+        L.fa_lp_sparse_query_blocks.argtypes = [P, ctypes.POINTER(i64)]
         L.fa_lp_attention.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, P, i64, i64, P]
         L.fa_lp_attention_host.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, i64, i64,
                                            i32, P]
@@ -184,7 +186,7 @@ class Plan:
     def last_error(self) -> int:
         v = ctypes.c_int()
         st = load().fa_lp_get_last_error(self._h, ctypes.byref(v))
-        if st not in (FA_LP_OK, FA_LP_ERR_DEVICE_TIMEOUT):
+        if v.value == 0:  # a non-zero device status comes with DEVICE_TIMEOUT or INVALID_ARG
             _check(st, "fa_lp_get_last_error")
         return v.value
 
@@ -213,6 +215,37 @@ class Plan:
                                                ctypes.c_void_p(lse.data_ptr()),
                                                int(lse.stride(0)), _stream(stream)),
                "fa_lp_forward_varlen_lse")
+        return out
+
+    def sparse_query_blocks(self) -> int:
+        """G: the 64-row query blocks of the plan (block lists are indexed h * G + g)."""
+        g = ctypes.c_int64()
+        _check(load().fa_lp_sparse_query_blocks(self._h, ctypes.byref(g)),
+               "fa_lp_sparse_query_blocks")
+        return g.value
+
+    def forward_sparse(self, block_offsets, block_indices, out, stream=None, lse=None):
+        """Block-sparse attention over the last quantize: `block_offsets` (int32 [heads G + 1])
+        and `block_indices` (int32) on the device, the list of (head h, query block g) being
+        block_indices[block_offsets[h G + g] : block_offsets[h G + g + 1]]."""
+        oa, os_, oh = _view(out, "out")
+        for name, x in (("block_offsets", block_offsets), ("block_indices", block_indices)):
+            if x.dtype != torch.int32 or not x.is_cuda or not x.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+        if block_offsets.numel() != self.heads * self.sparse_query_blocks() + 1:
+            raise ValueError("block_offsets must hold heads * G + 1 entries")
+        lp, ls = None, 0
+        if lse is not None:
+            if (lse.dtype != torch.float32 or lse.dim() != 2 or lse.stride(1) != 1
+                    or not lse.is_cuda or lse.shape[0] != self.heads
+                    or lse.shape[1] < self.tokens):
+                raise ValueError("lse must be a CUDA float32 [heads, >= tokens] tensor with unit "
+                                 "token stride")
+            lp, ls = ctypes.c_void_p(lse.data_ptr()), int(lse.stride(0))
+        _check(load().fa_lp_forward_sparse(self._h, None, ctypes.c_void_p(block_offsets.data_ptr()),
+                                           ctypes.c_void_p(block_indices.data_ptr()),
+                                           int(block_indices.numel()), oa, os_, oh, lp, ls,
+                                           _stream(stream)), "fa_lp_forward_sparse")
         return out
 
     def attention(self, q, k, v, cu_seqlens_dev=None, out=None, stream=None):

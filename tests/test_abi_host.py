@@ -169,3 +169,28 @@ def test_batched_front_end_packs_without_copies():
         fa_lp.merge_batch(x.transpose(0, 1), "x")  # seq-major storage: batch cannot be packed
     with pytest.raises(ValueError):
         fa_lp.merge_batch(x[0], "x")
+
+
+def test_sparse_query_blocks_and_argument_checks(lib):
+    """G = sum over segments of ceil(L_s / 64) (64-row query blocks, SGLang PR #40116,
+    Modifications); fa_lp_forward_sparse refuses NVFP4 plans and calls before quantize."""
+    cu = [0, 0, 17, 4113, 4113, 31800, 32768]
+    st, h = _create(lib, cu, heads=3)
+    assert st == 0
+    try:
+        g = ctypes.c_int64()
+        assert lib.fa_lp_sparse_query_blocks(h, ctypes.byref(g)) == 0
+        assert g.value == sum((b - a + 63) // 64 for a, b in zip(cu[:-1], cu[1:]))
+        assert lib.fa_lp_sparse_query_blocks(h, None) == 1
+        # before quantize: out of order
+        assert lib.fa_lp_forward_sparse(h, None, ctypes.c_void_p(16), ctypes.c_void_p(16), 4,
+                                        ctypes.c_void_p(16), 128, 128, None, 0, None) == 6
+    finally:
+        lib.fa_lp_plan_destroy(h)
+    st, h = _create(lib, [0, 256], heads=1, mode=1)
+    assert st == 0
+    try:
+        assert lib.fa_lp_forward_sparse(h, None, ctypes.c_void_p(16), ctypes.c_void_p(16), 4,
+                                        ctypes.c_void_p(16), 128, 128, None, 0, None) == 2
+    finally:
+        lib.fa_lp_plan_destroy(h)

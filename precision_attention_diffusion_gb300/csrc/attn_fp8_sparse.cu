@@ -17,8 +17,12 @@
 //     merges the two ascending lists of every tile into one ascending list of key blocks, each
 //     entry tagged with the halves (rows 0-63, 64-127) that listed it, and stores it in place of
 //     the two lists (the merged list is never longer than the two together);
-//   * one CTA = one (segment, head) and two query tiles, each with its own pipeline over its own
-//     merged list: TMA warp 16 / 19 streams the tile's K blocks (64 keys x 128 channels, 128-byte
+//   * a second prologue kernel orders the query tiles of every group (one segment, up to 8 heads,
+//     the CTAs that run together and share K/V in L2) by merged-list length, longest first, and
+//     the attention CTAs take them two at a time: the two tiles of a CTA have about the same
+//     length (a CTA lasts as long as its longer tile) and long tiles start first;
+//   * one CTA = two query tiles, each with its own pipeline over its own merged list: TMA warp
+//     16 / 19 streams the tile's K blocks (64 keys x 128 channels, 128-byte
 //     swizzle) and V^T blocks (128 channels x 64 keys, 64-byte swizzle) through a 5-stage ring;
 //     MMA warp 17 / 18 issues S = Q K^T (N = 64) and O += P V (K = 64), S one block ahead in the
 //     second tensor-memory buffer; softmax warps 0-7 / 8-15 as in the dense kernel (two threads
@@ -76,11 +80,13 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct SpArgs {
   const SegInfo* segs;
-  const WorkItem* work;
   const float* descale;    // [3][H]
   const uint32_t* uni;     // merged lists
   const int64_t* tbase;    // [H][nblocks] first entry of each tile's merged list
   const int32_t* tcnt;     // [H][nblocks] entries
+  const int32_t* order;    // tile ids (h nblocks + block) by group, longest list first
+  const SparseCta* ctas;   // slots of each CTA
+  const BlockInfo* blocks;
   int nblocks;
   __nv_bfloat16* out;
   int64_t ost, osh;
@@ -181,17 +187,68 @@ __global__ void __launch_bounds__(128) sparse_merge_kernel(
   }
 }
 
+// Prologue 2: within each group (one segment, heads [h0, h0 + nh)), the tile ids in descending
+// order of merged-list length (a counting sort on min(length, 4095); ties in any order).
+constexpr int kOrderBins = 4096;
+__global__ void __launch_bounds__(256) sparse_order_kernel(const SparseGroup* __restrict__ groups,
+                                                           const SegInfo* __restrict__ segs,
+                                                           const int32_t* __restrict__ tcnt,
+                                                           int nblocks, int32_t* __restrict__ order) {
+  __shared__ int bins[kOrderBins];
+  const SparseGroup gr = groups[blockIdx.x];
+  const SegInfo sg = segs[gr.seg];
+  const int nb = sg.nblk, nt = gr.nh * nb, b0 = sg.row0 / kTile;
+  for (int i = threadIdx.x; i < kOrderBins; i += 256) bins[i] = 0;
+  __syncthreads();
+  auto tile = [&](int j) { return (gr.h0 + j / nb) * nblocks + b0 + j % nb; };
+  auto key = [&](int id) { return kOrderBins - 1 - min(tcnt[id], kOrderBins - 1); };
+  for (int j = threadIdx.x; j < nt; j += 256) atomicAdd(&bins[key(tile(j))], 1);
+  __syncthreads();
+  // exclusive scan of the bins: 256 threads x 16 consecutive bins
+  constexpr int kPer = kOrderBins / 256;
+  __shared__ int part[256];
+  int loc[kPer], sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    loc[i] = sum;
+    sum += bins[threadIdx.x * kPer + i];
+  }
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int i = 0; i < 256; ++i) {
+      const int x = part[i];
+      part[i] = acc;
+      acc += x;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) bins[threadIdx.x * kPer + i] = part[threadIdx.x] + loc[i];
+  __syncthreads();
+  for (int j = threadIdx.x; j < nt; j += 256) {
+    const int id = tile(j);
+    order[gr.slot0 + atomicAdd(&bins[key(id)], 1)] = id;
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
-// Attention roles.
+// Attention roles. A query tile of a CTA: its segment, head and tile index in the segment.
+struct TileRef {
+  SegInfo sg;
+  int head, qt;
+};
+
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                          const CUtensorMap* tm_v, Smem& S, const SpArgs& a,
-                                         const WorkItem& wi, const SegInfo& sg, int t,
-                                         const uint32_t* ent, int n) {
+                                         const TileRef& tr, int t, const uint32_t* ent, int n) {
   if (n == 0) return;
-  const int rq = sg.row0 + (wi.qt0 + t) * kTile;
+  const SegInfo& sg = tr.sg;
+  const int rq = sg.row0 + tr.qt * kTile;
   mbar_arrive_expect_tx_elect(smem_u32(&S.bar_q[t]), kQBytes);
-  tma_load_3d_elect(smem_u32(S.q[t]), tm_q, smem_u32(&S.bar_q[t]), 0, rq, wi.head);
+  tma_load_3d_elect(smem_u32(S.q[t]), tm_q, smem_u32(&S.bar_q[t]), 0, rq, tr.head);
   int issued = 0;
   for (int j = 0; j < n; ++j) {
     const int st = j % kSt;
@@ -200,9 +257,9 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
       break;
     const int row = sg.row0 + kBlk * int(__ldg(ent + j) & kKbMask);
     mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[t][st]), kKBytes);
-    tma_load_3d_elect(smem_u32(S.k[t][st]), tm_k, smem_u32(&S.bar_k[t][st]), 0, row, wi.head);
+    tma_load_3d_elect(smem_u32(S.k[t][st]), tm_k, smem_u32(&S.bar_k[t][st]), 0, row, tr.head);
     mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[t][st]), kVBytes);
-    tma_load_3d_elect(smem_u32(S.v[t][st]), tm_v, smem_u32(&S.bar_v[t][st]), row, 0, wi.head);
+    tma_load_3d_elect(smem_u32(S.v[t][st]), tm_v, smem_u32(&S.bar_v[t][st]), row, 0, tr.head);
     issued = j + 1;
   }
   drain_phase(smem_u32(&S.bar_q[t]), 0);
@@ -265,11 +322,11 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const SpArgs& a, uint32_t tm
   drain_phase(smem_u32(&S.bar_drain[t]), 0);
 }
 
-__device__ __forceinline__ void softmax_and_epilogue(Smem& S, const SpArgs& a, const WorkItem& wi,
-                                                     const SegInfo& sg, uint32_t tmem, int t,
-                                                     int wq, int lane, const uint32_t* ent,
-                                                     int n) {
-  const int h = wi.head;
+__device__ __forceinline__ void softmax_and_epilogue(Smem& S, const SpArgs& a, const TileRef& tr,
+                                                     uint32_t tmem, int t, int wq, int lane,
+                                                     const uint32_t* ent, int n) {
+  const SegInfo& sg = tr.sg;
+  const int h = tr.head;
   const float c = a.descale[h] * a.descale[a.H + h] * a.scale_log2;
   const float dv = a.descale[2 * a.H + h];
   const int rbase = 32 * (wq & 3) + 16 * (wq >> 2);  // rows of this warp: rbase + [0, 16)
@@ -371,7 +428,7 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const SpArgs& a, c
   l += __shfl_xor_sync(0xffffffffu, l, 16);
   const bool any = l > 0.f;  // false: this half listed no block
   const float f = any ? dv / l : 0.f;
-  const int qrow = (wi.qt0 + t) * kTile + rbase + (lane & 15);
+  const int qrow = tr.qt * kTile + rbase + (lane & 15);
   const bool valid = qrow < sg.len;
   if (a.lse && valid && kh == 0)
     a.lse[int64_t(h) * a.lse_sh + sg.tok0 + qrow] =
@@ -413,15 +470,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WorkItem wi = a.work[blockIdx.x];
-  const SegInfo sg = a.segs[wi.seg];
-  // this CTA's tiles: merged list and its length (0 for a tile the work item does not hold)
+  const SparseCta cta = a.ctas[blockIdx.x];
+  // this CTA's tiles: merged list and its length (0 for a second tile the CTA does not hold)
+  TileRef tr[2];
   const uint32_t* ent[2];
   int n[2];
   for (int t = 0; t < 2; ++t) {
-    const int64_t ti = int64_t(wi.head) * a.nblocks + sg.row0 / kTile + wi.qt0 + t;
-    ent[t] = a.uni + (t < wi.nq ? a.tbase[ti] : 0);
-    n[t] = t < wi.nq ? a.tcnt[ti] : 0;
+    const int id = t < cta.count ? a.order[cta.slot + t] : a.order[cta.slot];
+    const int hh = id / a.nblocks;
+    const BlockInfo bi = a.blocks[id - hh * a.nblocks];
+    tr[t].sg = a.segs[bi.seg];
+    tr[t].head = hh;
+    tr[t].qt = bi.blk;
+    ent[t] = a.uni + a.tbase[id];
+    n[t] = t < cta.count ? a.tcnt[id] : 0;
   }
 
   if (threadIdx.x == 0) {
@@ -458,13 +520,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp0 || warp == kTmaWarp1) {
     const int t = warp == kTmaWarp0 ? 0 : 1;
-    producer(&tm_q, &tm_k, &tm_v, S, a, wi, sg, t, ent[t], n[t]);
+    producer(&tm_q, &tm_k, &tm_v, S, a, tr[t], t, ent[t], n[t]);
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     const int t = warp - kMmaWarp;
     mma_issuer(S, a, tmem, t, n[t]);
   } else if (warp < 16) {
     const int t = warp >> 3;
-    if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 7, lane, ent[t], n[t]);
+    if (t < cta.count) softmax_and_epilogue(S, a, tr[t], tmem, t, warp & 7, lane, ent[t], n[t]);
   }
   tc_fence_before();
   __syncthreads();
@@ -490,11 +552,15 @@ int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* off, cons
   uint32_t* uni = static_cast<uint32_t*>(p.sp_buf);
   int64_t* tbase = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(p.sp_buf) + p.sp_tables);
   int32_t* tcnt = reinterpret_cast<int32_t*>(tbase + int64_t(p.heads) * nblocks);
+  int32_t* order = tcnt + int64_t(p.heads) * nblocks;
   const size_t merge_smem = size_t(2) * p.sp_nw_max * sizeof(uint32_t);
   dim3 gm(unsigned(nblocks), unsigned(p.heads));
   sparse_merge_kernel<<<gm, 128, merge_smem, stream>>>(off, idx, n_idx, p.d_blocks, p.d_segs,
                                                        p.d_sp_qb0, p.sp_G, nblocks, uni, tbase,
                                                        tcnt, p.d_err);
+  if (cudaGetLastError() != cudaSuccess) return FA_LP_ERR_CUDA;
+  sparse_order_kernel<<<unsigned(p.sp_groups.size()), 256, 0, stream>>>(p.d_sp_groups, p.d_segs,
+                                                                        tcnt, nblocks, order);
   if (cudaGetLastError() != cudaSuccess) return FA_LP_ERR_CUDA;
 
   const uint64_t H = uint64_t(p.heads), Tp = uint64_t(p.tpad);
@@ -510,7 +576,9 @@ int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* off, cons
   if (st != FA_LP_OK) return st;
   SpArgs a;
   a.segs = p.d_segs;
-  a.work = p.d_work;
+  a.order = order;
+  a.ctas = p.d_sp_ctas;
+  a.blocks = p.d_blocks;
   a.descale = reinterpret_cast<const float*>(ws + p.ws.descale);
   a.uni = uni;
   a.tbase = tbase;
@@ -527,7 +595,8 @@ int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* off, cons
   a.w.abort_word = p.d_err + 1;
   a.w.gen = next_launch_generation();
   a.w.spin_limit = p.spin_limit;
-  attn_fp8_sparse_kernel<<<unsigned(p.work.size()), kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
+  attn_fp8_sparse_kernel<<<unsigned(p.sp_ctas.size()), kThreads, kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                      a);
   return cuda_status(cudaGetLastError());
 }
 

@@ -90,13 +90,17 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   const size_t n_qmk = p->qmk_items.size() * sizeof(QmkItem);
   const size_t n_cof = p->c_off.size() * sizeof(int64_t);
   const size_t n_qb0 = p->sp_qb0.size() * sizeof(int32_t);
+  const size_t n_spg = p->sp_groups.size() * sizeof(falp::SparseGroup);
+  const size_t n_spc = p->sp_ctas.size() * sizeof(falp::SparseCta);
   const size_t o_seg = 0;
   const size_t o_blk = align_up(o_seg + n_seg, 256);
   const size_t o_wrk = align_up(o_blk + n_blk, 256);
   const size_t o_qmk = align_up(o_wrk + n_wrk, 256);
   const size_t o_cof = align_up(o_qmk + n_qmk, 256);
   const size_t o_qb0 = align_up(o_cof + n_cof, 256);
-  const size_t o_err = align_up(o_qb0 + n_qb0, 256);
+  const size_t o_spg = align_up(o_qb0 + n_qb0, 256);
+  const size_t o_spc = align_up(o_spg + n_spg, 256);
+  const size_t o_err = align_up(o_spc + n_spc, 256);
   const size_t total = o_err + 256;
   void* d = nullptr;
   if (cudaMalloc(&d, total) != cudaSuccess) {
@@ -110,6 +114,8 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   if (n_qmk) std::memcpy(host.data() + o_qmk, p->qmk_items.data(), n_qmk);
   if (n_cof) std::memcpy(host.data() + o_cof, p->c_off.data(), n_cof);
   if (n_qb0) std::memcpy(host.data() + o_qb0, p->sp_qb0.data(), n_qb0);
+  if (n_spg) std::memcpy(host.data() + o_spg, p->sp_groups.data(), n_spg);
+  if (n_spc) std::memcpy(host.data() + o_spc, p->sp_ctas.data(), n_spc);
   if (cudaMemcpyAsync(d, host.data(), total, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaFree(d);
@@ -124,6 +130,8 @@ int ensure_device_meta(fa_lp_plan* p, cudaStream_t stream) {
   p->d_qmk = reinterpret_cast<QmkItem*>(b + o_qmk);
   p->d_coff = reinterpret_cast<int64_t*>(b + o_cof);
   p->d_sp_qb0 = reinterpret_cast<int32_t*>(b + o_qb0);
+  p->d_sp_groups = reinterpret_cast<falp::SparseGroup*>(b + o_spg);
+  p->d_sp_ctas = reinterpret_cast<falp::SparseCta*>(b + o_spc);
   p->d_err = reinterpret_cast<int*>(b + o_err);
   if (log_enabled())
     std::fprintf(stderr, "[fa_lp] plan %p: device tables %zu bytes on device %d\n", (void*)p,
@@ -261,6 +269,21 @@ void build_plan(fa_lp_plan* p) {
       for (int t = 0; t < nb; t += 2)
         for (int h = h0; h < std::min(p->heads, h0 + kHeadGroup); ++h)
           p->work.push_back(WorkItem{s, h, t, std::min(2, nb - t)});
+  }
+  // Block-sparse forward: the same segment / head-group order; a group's tiles are paired on the
+  // device once their list lengths are known.
+  int32_t slot = 0;
+  for (int s : order) {
+    const int nb = p->segs[s].nblk;
+    if (nb == 0) continue;
+    for (int h0 = 0; h0 < p->heads; h0 += kHeadGroup) {
+      const int nh = std::min(kHeadGroup, p->heads - h0);
+      const int nt = nh * nb;
+      p->sp_groups.push_back(falp::SparseGroup{slot, h0, nh, s});
+      for (int i = 0; i < nt; i += 2)
+        p->sp_ctas.push_back(falp::SparseCta{slot + i, std::min(2, nt - i)});
+      slot += nt;
+    }
   }
 
   // Workspace layout.
@@ -587,7 +610,7 @@ int fa_lp_forward_sparse(fa_lp_plan* p, const int32_t* cu_seqlens_dev,
     // stream-ordered
     const size_t nb = p->blocks.size(), H = size_t(p->heads);
     const size_t tables = align_up(size_t(std::max<int64_t>(num_indices, 1)) * 4, 256);
-    const size_t need = tables + H * nb * (8 + 4);
+    const size_t need = tables + H * nb * (8 + 4 + 4);
     if (p->sp_bytes < need) {
       if (p->sp_buf && cudaFreeAsync(p->sp_buf, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -604,7 +627,7 @@ int fa_lp_forward_sparse(fa_lp_plan* p, const int32_t* cu_seqlens_dev,
     }
     p->sp_tables = align_up(size_t(std::max<int64_t>(num_indices, 1)) * 4, 256);
   }
-  if (p->work.empty()) return FA_LP_OK;
+  if (p->sp_ctas.empty()) return FA_LP_OK;
   return falp::launch_fp8_sparse(*p, static_cast<uint8_t*>(base), block_offsets, block_indices,
                                  num_indices, out, ost, osh, lse, lse_stride_head, stream);
 }

@@ -39,6 +39,19 @@ struct WorkItem {
   int32_t nq;       // 1 or 2 query tiles
 };
 
+// Block-sparse forward: a group of query tiles (one segment, up to 8 heads) whose CTAs run
+// together; the tiles of a group are ordered by their merged-list length on the device and taken
+// two per CTA.
+struct SparseGroup {
+  int32_t slot0;    // first slot of the group in the tile order
+  int32_t h0, nh;   // heads [h0, h0 + nh)
+  int32_t seg;
+};
+struct SparseCta {
+  int32_t slot;     // first of this CTA's slots
+  int32_t count;    // 1 or 2 tiles
+};
+
 // Tile of the NVFP4 qm K^T table: (segment, 128-block M tile, 256-key N tile).
 struct QmkItem {
   int32_t seg;
@@ -98,8 +111,11 @@ struct fa_lp_plan {
   int64_t sp_G = 0;                   // query blocks over the packed batch
   std::vector<int32_t> sp_qb0;        // first query block of every segment
   int sp_nw_max = 0;                  // 32-bit words of the largest segment's key-block bitmap
+  std::vector<falp::SparseGroup> sp_groups;
+  std::vector<falp::SparseCta> sp_ctas;
   void* sp_buf = nullptr;             // merged lists (u32 [num_indices]) + tile tables
-  size_t sp_bytes = 0, sp_tables = 0; // its size; byte offset of the tables (i64 + i32 [H][nb])
+  size_t sp_bytes = 0, sp_tables = 0; // its size; byte offset of the tables (i64 base, i32 count,
+                                      // i32 order, each [H][nb])
   int64_t spin_limit = 20000;  // parked probes of <= 100 us each: about 2 s per wait
   // device metadata (created on first use on the plan's device)
   void* dmeta = nullptr;
@@ -109,6 +125,8 @@ struct fa_lp_plan {
   falp::QmkItem* d_qmk = nullptr;
   int64_t* d_coff = nullptr;
   int32_t* d_sp_qb0 = nullptr;
+  falp::SparseGroup* d_sp_groups = nullptr;
+  falp::SparseCta* d_sp_ctas = nullptr;
   int* d_err = nullptr;  // [0]: sticky device status, [1]: abort word (launch generation)
   bool quantized = false;
   int refcount = 1;

@@ -58,6 +58,8 @@ NCU_TRAFFIC = {
         1.93e9 + 425.50e6,
     ("nvfp4_s30272_h56", "34f2851e9ee735c99a78e346d09332e8769f076124d32b4ab9b0e77deac59cd3"):
         2.41e9 + 425.52e6,
+    ("sparse_fp8_s30272_h56", "e5d1a5d2907619824f628c89021aee2ed9a2884711c7eaddbab2306473042073"):
+        1.835e9 + 705.42e6,
 }
 
 

@@ -125,6 +125,20 @@ def test_sparse_halves_of_a_tile_differ(fa):
     assert empty.sum() == 64
 
 
+@pytest.mark.parametrize("cu,H,density,dense_every,empty_every", [
+    ([0, 192], 1, 0.5, 0, 2),            # a tile holding one full 64-row block only
+    ([0, 64, 128, 129, 257], 2, 1.0, 0, 0),  # long lists (half to all blocks), short segments
+    ([0, 0, 17, 4113, 4113, 5200], 4, 0.2, 3, 4),  # the varlen layout's empty / short segments
+])
+def test_sparse_shapes(fa, cu, H, density, dense_every, empty_every):
+    q, k, v = inputs.qkv_separate(cu[-1], H, seed=10 + H)
+    off, idx = inputs.block_sparse_lists(cu, H, density=density, seed=H, dense_every=dense_every,
+                                         empty_every=empty_every)
+    plan, out, lse = run_sparse(fa, q, k, v, cu, H, off, idx, lse=True)
+    rows = all_rows(cu, H) if cu[-1] * H <= 3000 else inputs.sample_rows(cu, H, H, 512, seed=3)
+    check_sparse(fa, plan, out, q, k, v, cu, H, off, idx, rows, lse)
+
+
 def test_sparse_list_breaking_the_contract_is_reported(fa):
     """A descending list is caught by the device-side check: status 0x200, INVALID_ARG, no
     access outside the arrays; the next valid call is clean."""

@@ -442,13 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
                          float* lse, int64_t lse_sh, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kSmemBytes)) != cudaSuccess)
-      return FA_LP_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (set_smem_limit_once(reinterpret_cast<const void*>(attn_fp8_kernel), int(kSmemBytes), p.device,
+                          smem_set) != FA_LP_OK)
+    return FA_LP_ERR_CUDA;
   const uint64_t H = uint64_t(p.heads), Tp = uint64_t(p.tpad);
   CUtensorMap tq, tk, tv;
   int st = encode_tmap_3d_u8(&tq, ws + p.ws.q_codes, 128, Tp, H, 128, Tp * 128, 128, 128,

@@ -541,13 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* off, const int32_t* idx,
                       int64_t n_idx, void* out, int64_t ost, int64_t osh, float* lse,
                       int64_t lse_sh, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_fp8_sparse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kSmemBytes)) != cudaSuccess)
-      return FA_LP_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (set_smem_limit_once(reinterpret_cast<const void*>(attn_fp8_sparse_kernel), int(kSmemBytes), p.device,
+                          smem_set) != FA_LP_OK)
+    return FA_LP_ERR_CUDA;
   const int nblocks = int(p.blocks.size());
   uint32_t* uni = static_cast<uint32_t*>(p.sp_buf);
   int64_t* tbase = reinterpret_cast<int64_t*>(static_cast<uint8_t*>(p.sp_buf) + p.sp_tables);

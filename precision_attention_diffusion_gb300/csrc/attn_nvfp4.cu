@@ -583,13 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
                            float* lse, int64_t lse_sh, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kSmemBytes)) != cudaSuccess)
-      return FA_LP_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (set_smem_limit_once(reinterpret_cast<const void*>(attn_nvfp4_kernel), int(kSmemBytes), p.device,
+                          smem_set) != FA_LP_OK)
+    return FA_LP_ERR_CUDA;
   const uint64_t H = uint64_t(p.heads), Tp = uint64_t(p.tpad);
   CUtensorMap tq, tk, tv;
   // Q, K codes: [H][Tp][64 bytes]; V^T codes: [H][128][Tp / 2 bytes]; boxes of 128 rows x 64 B

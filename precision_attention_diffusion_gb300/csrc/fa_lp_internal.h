@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <vector>
@@ -164,5 +165,21 @@ int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStr
 int next_launch_generation();
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_LP_OK : FA_LP_ERR_CUDA; }
+
+// Raise a kernel's dynamic shared-memory limit on `device` once (the attribute belongs to the
+// device's context, so every device is set up on its own first launch). `done` holds one bit per
+// device; safe to call from several host threads (a repeated set is harmless).
+inline int set_smem_limit_once(const void* kernel, int bytes, int device,
+                               std::atomic<uint64_t>& done) {
+  const uint64_t bit = (device >= 0 && device < 64) ? (uint64_t(1) << device) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return FA_LP_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return FA_LP_OK;
+}
 
 }  // namespace falp

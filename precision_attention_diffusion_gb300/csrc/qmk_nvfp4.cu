@@ -261,13 +261,10 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
 
 int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, cudaStream_t stream) {
   if (p.qmk_items.empty()) return FA_LP_OK;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(nvfp4_qmk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kQmkSmemBytes)) != cudaSuccess)
-      return FA_LP_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (set_smem_limit_once(reinterpret_cast<const void*>(nvfp4_qmk_kernel), int(kQmkSmemBytes), p.device,
+                          smem_set) != FA_LP_OK)
+    return FA_LP_ERR_CUDA;
   nvfp4_qmk_kernel<<<dim3(unsigned(p.qmk_items.size()), unsigned(p.heads)), kQmkThreads,
                      kQmkSmemBytes, stream>>>(
       p.d_qmk, p.d_segs, p.d_coff, reinterpret_cast<const float*>(ws + p.ws.q_mean),

@@ -266,6 +266,30 @@ FA_LP_API int fa_lp_attention_host(fa_lp_plan* plan, const void* q, int64_t q_st
                                    int64_t out_stride_head, int heads_per_chunk, void* stream);
 
 /*
+ * fa_lp_attention_sparse_host -- fa_lp_forward_sparse from and to host memory, through the head
+ * pipeline of fa_lp_attention_host: the block lists are copied to the device once per call,
+ * then every chunk of heads is copied in, quantized and run through the block-sparse forward
+ * with its heads' lists (offsets from h0 * G on), and copied out, chunks overlapping as there.
+ * Passage and semantics: those of fa_lp_forward_sparse (SGLang PR #40116, Modifications); the
+ * result equals fa_lp_quantize + fa_lp_forward_sparse on the same data bit for bit.
+ *   q, k, v, out, heads_per_chunk, stream : as fa_lp_attention_host.
+ *   block_offsets : host int32 [heads * G + 1]; block_indices: host int32 [num_indices]; the list
+ *                   contract of fa_lp_forward_sparse (checked on the device, reported through
+ *                   fa_lp_get_last_error on the plan).
+ * Device memory: that of fa_lp_attention_host plus a copy of the lists, kept by the plan.
+ * Errors: INVALID_ARG, UNSUPPORTED (NVFP4 plan), OOM, CUDA.
+ */
+FA_LP_API int fa_lp_attention_sparse_host(fa_lp_plan* plan, const void* q, int64_t q_stride_tok,
+                                          int64_t q_stride_head, const void* k,
+                                          int64_t k_stride_tok, int64_t k_stride_head,
+                                          const void* v, int64_t v_stride_tok,
+                                          int64_t v_stride_head, const int32_t* block_offsets,
+                                          const int32_t* block_indices, int64_t num_indices,
+                                          void* out, int64_t out_stride_tok,
+                                          int64_t out_stride_head, int heads_per_chunk,
+                                          void* stream);
+
+/*
  * Inspection of the quantized operands (for bit-exact tests). `which` selects one array of the
  * workspace; the descriptor gives its device address and layout. Valid until the next call that
  * may grow the workspace.

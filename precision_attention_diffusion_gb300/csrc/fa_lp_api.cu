@@ -214,6 +214,7 @@ int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[4]) {
   if (hp.s_in && cudaStreamSynchronize(hp.s_in) != cudaSuccess) st = FA_LP_ERR_CUDA;
   if (hp.s_out && cudaStreamSynchronize(hp.s_out) != cudaSuccess) st = FA_LP_ERR_CUDA;
   if (hp.buf && cudaFree(hp.buf) != cudaSuccess) st = FA_LP_ERR_CUDA;
+  if (hp.lists && cudaFree(hp.lists) != cudaSuccess) st = FA_LP_ERR_CUDA;
   for (cudaEvent_t* e : {&hp.start, &hp.end, &hp.in_done[0], &hp.in_done[1], &hp.in_free[0],
                          &hp.in_free[1], &hp.out_ready[0], &hp.out_ready[1], &hp.out_free[0],
                          &hp.out_free[1]})
@@ -641,10 +642,21 @@ int fa_lp_attention(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, cons
   return fa_lp_forward_varlen(p, cu_seqlens_dev, out, ost, osh, stream);
 }
 
-int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
-                         int64_t kst, int64_t ksh, const void* v, int64_t vst, int64_t vsh,
-                         void* out, int64_t ost, int64_t osh, int heads_per_chunk,
-                         void* stream_) {
+}  // extern "C"
+
+namespace {
+
+// Block lists of the block-sparse host entry (host arrays), or none for the dense forward.
+struct HostLists {
+  const int32_t* off;
+  const int32_t* idx;
+  int64_t n_idx;
+};
+
+int host_pipeline(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
+                  int64_t kst, int64_t ksh, const void* v, int64_t vst, int64_t vsh, void* out,
+                  int64_t ost, int64_t osh, int heads_per_chunk, void* stream_,
+                  const HostLists* lists) {
   if (!p) return FA_LP_ERR_INVALID_ARG;
   if (heads_per_chunk < 0 || heads_per_chunk > p->heads) return FA_LP_ERR_INVALID_ARG;
   if (p->tokens > 0 && (bad_view(q, qst, qsh) || bad_view(k, kst, ksh) || bad_view(v, vst, vsh) ||
@@ -716,6 +728,39 @@ int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
     cudaGetLastError();
     return FA_LP_ERR_CUDA;
   }
+  // block lists: one copy ahead of the first chunk's inputs on the copy-in stream (so every
+  // chunk's in_done event covers it); chunk [h0, h0 + n) reads offsets from h0 G on
+  const int32_t* d_off = nullptr;
+  const int32_t* d_idx = nullptr;
+  if (lists) {
+    const size_t n_off = size_t(H) * size_t(p->sp_G) + 1;
+    const size_t need = (n_off + size_t(std::max<int64_t>(lists->n_idx, 1))) * sizeof(int32_t);
+    if (hp.lists_bytes < need) {
+      if (hp.lists && cudaFree(hp.lists) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_LP_ERR_CUDA;
+      }
+      hp.lists = nullptr;
+      hp.lists_bytes = 0;
+      if (cudaMalloc(&hp.lists, need) != cudaSuccess) {
+        cudaGetLastError();
+        hp.lists = nullptr;
+        return FA_LP_ERR_OOM;
+      }
+      hp.lists_bytes = need;
+    }
+    int32_t* lo = static_cast<int32_t*>(hp.lists);
+    if (!ok_(cudaMemcpyAsync(lo, lists->off, n_off * sizeof(int32_t), cudaMemcpyHostToDevice,
+                             hp.s_in)) ||
+        (lists->n_idx > 0 &&
+         !ok_(cudaMemcpyAsync(lo + n_off, lists->idx, size_t(lists->n_idx) * sizeof(int32_t),
+                              cudaMemcpyHostToDevice, hp.s_in)))) {
+      cudaGetLastError();
+      return FA_LP_ERR_CUDA;
+    }
+    d_off = lo;
+    d_idx = lo + n_off;
+  }
   const int nchunks = int(hp.sizes.size());
   for (int c = 0, h0 = 0; c < nchunks; h0 += hp.sizes[c], ++c) {
     const int n = hp.sizes[c], slot = c & 1;
@@ -750,7 +795,9 @@ int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
       cudaGetLastError();
       return FA_LP_ERR_CUDA;
     }
-    st = fa_lp_forward_varlen(sp, nullptr, dev(slot, 3), dst, dsh, stream);
+    st = lists ? fa_lp_forward_sparse(sp, nullptr, d_off + int64_t(h0) * p->sp_G, d_idx,
+                                      lists->n_idx, dev(slot, 3), dst, dsh, nullptr, 0, stream)
+               : fa_lp_forward_varlen(sp, nullptr, dev(slot, 3), dst, dsh, stream);
     if (st != FA_LP_OK) return st;
     // copy-out of chunk c
     good = ok_(cudaEventRecord(hp.out_ready[slot], stream)) &&
@@ -769,6 +816,32 @@ int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
     return FA_LP_ERR_CUDA;
   }
   return FA_LP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_lp_attention_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const void* k,
+                         int64_t kst, int64_t ksh, const void* v, int64_t vst, int64_t vsh,
+                         void* out, int64_t ost, int64_t osh, int heads_per_chunk,
+                         void* stream) {
+  return host_pipeline(p, q, qst, qsh, k, kst, ksh, v, vst, vsh, out, ost, osh, heads_per_chunk,
+                       stream, nullptr);
+}
+
+int fa_lp_attention_sparse_host(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh,
+                                const void* k, int64_t kst, int64_t ksh, const void* v,
+                                int64_t vst, int64_t vsh, const int32_t* block_offsets,
+                                const int32_t* block_indices, int64_t num_indices, void* out,
+                                int64_t ost, int64_t osh, int heads_per_chunk, void* stream) {
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  if (p->mode != FA_LP_MODE_FP8) return FA_LP_ERR_UNSUPPORTED;
+  if (num_indices < 0 || (p->tokens > 0 && !block_offsets) || (num_indices > 0 && !block_indices))
+    return FA_LP_ERR_INVALID_ARG;
+  const HostLists lists{block_offsets, block_indices, num_indices};
+  return host_pipeline(p, q, qst, qsh, k, kst, ksh, v, vst, vsh, out, ost, osh, heads_per_chunk,
+                       stream, &lists);
 }
 
 int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {

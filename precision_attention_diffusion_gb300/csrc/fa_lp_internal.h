@@ -83,6 +83,8 @@ struct HostPipe {
   int sub_n[4] = {0, 0, 0, 0};                // (fewer heads than the plan; a chunk of all
                                               // the heads runs on the plan itself)
   void* buf = nullptr;                        // 2 slots x {q, k, v, out} x tokens x maxn x 128 BF16
+  void* lists = nullptr;                      // block-sparse entry: device copy of the lists
+  size_t lists_bytes = 0;
   cudaStream_t s_in = nullptr, s_out = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
   cudaEvent_t in_done[2] = {}, in_free[2] = {}, out_ready[2] = {}, out_free[2] = {};

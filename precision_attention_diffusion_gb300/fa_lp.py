@@ -37,6 +37,7 @@ EXPORTS = (
     "fa_lp_get_last_error", "fa_lp_plan_set_wait_limit", "fa_lp_release_workspace",
     "fa_lp_encode", "fa_lp_fp8_descale_noalloc", "fa_lp_forward_varlen_lse",
     "fa_lp_attention_host", "fa_lp_forward_sparse", "fa_lp_sparse_query_blocks",
+    "fa_lp_attention_sparse_host",
 )
 
 _lib = None
@@ -86,6 +87,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.fa_lp_forward_varlen_lse.argtypes = [P, P, P, i64, i64, P, i64, P]
         L.fa_lp_forward_sparse.argtypes = [P, P, P, P, i64, P, i64, i64, P, i64, P]
         L.fa_lp_sparse_query_blocks.argtypes = [P, ctypes.POINTER(i64)]
+        L.fa_lp_attention_sparse_host.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, P,
+                                                  i64, P, i64, i64, i32, P]
         L.fa_lp_attention.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, P, i64, i64, P]
         L.fa_lp_attention_host.argtypes = [P, P, i64, i64, P, i64, i64, P, i64, i64, P, i64, i64,
                                            i32, P]
@@ -271,6 +274,26 @@ class Plan:
         _check(load().fa_lp_attention_host(self._h, qa, qs, qh, ka, ks, kh, va, vs, vh, oa, os_,
                                            oh, int(heads_per_chunk), _stream(stream)),
                "fa_lp_attention_host")
+        return out
+
+    def attention_sparse_host(self, q, k, v, block_offsets, block_indices, out,
+                              heads_per_chunk: int = 0, stream=None):
+        """fa_lp_attention_sparse_host: q, k, v, out BF16 [tokens, heads, 128] CPU tensors
+        (page-locked for overlap); block_offsets (int32 [heads G + 1]) and block_indices
+        (int32) contiguous CPU tensors."""
+        qa, qs, qh = _view(q, "q", host=True)
+        ka, ks, kh = _view(k, "k", host=True)
+        va, vs, vh = _view(v, "v", host=True)
+        oa, os_, oh = _view(out, "out", host=True)
+        for name, x in (("block_offsets", block_offsets), ("block_indices", block_indices)):
+            if x.dtype != torch.int32 or x.is_cuda or not x.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU int32 tensor")
+        if block_offsets.numel() != self.heads * self.sparse_query_blocks() + 1:
+            raise ValueError("block_offsets must hold heads * G + 1 entries")
+        _check(load().fa_lp_attention_sparse_host(
+            self._h, qa, qs, qh, ka, ks, kh, va, vs, vh, ctypes.c_void_p(block_offsets.data_ptr()),
+            ctypes.c_void_p(block_indices.data_ptr()), int(block_indices.numel()), oa, os_, oh,
+            int(heads_per_chunk), _stream(stream)), "fa_lp_attention_sparse_host")
         return out
 
     # -- inspection -------------------------------------------------------------------------------

@@ -109,3 +109,26 @@ def test_host_entry_default_schedule_many_heads(fa):
     plan.attention_host(buf[:, 0], buf[:, 1], buf[:, 2], out)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("hpc", [0, 3, 7])
+def test_sparse_host_entry_equals_device_call(fa, hpc):
+    """fa_lp_attention_sparse_host (block lists from host memory, head chunks with their lists'
+    offsets from h0 G on) returns the device-buffer block-sparse forward's output bit for bit."""
+    cu, H = [0, 0, 17, 300, 300, 1400, 1500], 7
+    T = cu[-1]
+    buf = fused_host(T, H, seed=21)
+    off, idx = inputs.block_sparse_lists(cu, H, density=0.4, seed=2, dense_every=5, empty_every=6)
+    plan = fa.Plan(cu, H, mode=fa.MODE_FP8)
+    d = buf.cuda()
+    ref = torch.empty((T, H, 128), dtype=torch.bfloat16, device="cuda")
+    plan.quantize(d[:, 0], d[:, 1], d[:, 2])
+    plan.forward_sparse(torch.from_numpy(off).cuda(), torch.from_numpy(idx).cuda(), ref)
+    torch.cuda.synchronize()
+    ref = ref.cpu()
+    out = torch.full((T, H, 128), 5.0, dtype=torch.bfloat16).pin_memory()
+    plan.attention_sparse_host(buf[:, 0], buf[:, 1], buf[:, 2], torch.from_numpy(off),
+                               torch.from_numpy(idx), out, heads_per_chunk=hpc)
+    torch.cuda.synchronize()
+    assert plan.last_error() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

@@ -245,8 +245,10 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
  *   out             : host pointer, BF16 [tokens, heads, 128] with element strides; every row
  *                     (all tokens lie in a segment) is written. Caller-owned.
  *   heads_per_chunk : 1..heads for chunks of that many heads (the last may be shorter), or 0 for
- *                     the library's choice: the size giving 4 to 8 chunks whose CTAs fill the
- *                     GPU's waves best (1-head chunks when heads < 4).
+ *                     the library's choice: the size n giving 4 to 8 chunks whose CTAs fill the
+ *                     GPU's waves best (1-head chunks when heads < 4), with the first chunk of
+ *                     ceil(n / 2) heads and the rest of n (the last takes what remains) when
+ *                     heads >= 3 n.
  *   stream          : the quantize and attention kernels run on it; the copies run on two
  *                     streams of the plan, ordered after the work already on `stream`, and
  *                     `stream` is ordered after the last copy-out: once `stream` completes, `out`

@@ -202,6 +202,20 @@ std::vector<int> host_schedule(const fa_lp_plan& p, int heads_per_chunk) {
     }
   }
   std::vector<int> out;
+  if (heads_per_chunk <= 0 && nh >= 2 && H >= 3 * nh) {
+    // the library's choice: half-size first and last chunks, whose copy-in and copy-out nothing
+    // overlaps; a half chunk computes about as long as a full chunk's copy-in takes (the copies
+    // move a head in about half the time its compute takes), so the pipeline does not stall
+    const int first = (nh + 1) / 2;
+    int rest = H - first;
+    out.push_back(first);
+    while (rest > nh) {
+      out.push_back(nh);
+      rest -= nh;
+    }
+    if (rest > 0) out.push_back(rest);
+    return out;
+  }
   for (int h0 = 0; h0 < H; h0 += nh) out.push_back(std::min(nh, H - h0));
   return out;
 }

@@ -58,8 +58,8 @@ NCU_TRAFFIC = {
         1.954e9 + 425.45e6,
     ("nvfp4_s30272_h56", "65044c1b6940a7fe0323b3d5f6417f07d1ec5d9a23830f8301be43b346afeac3"):
         2.383e9 + 424.98e6,
-    ("sparse_fp8_s30272_h56", "c98512c4ccec60f7e8a3e909664cb3e7e196615fa7e98b98a7cc93184cd7ae09"):
-        1.830e9 + 704.98e6,
+    ("sparse_fp8_s30272_h56", "3607c1f0c0bce02d7a02c4c42d1c5db232c42a385a3bef444ef7cf3f0f8354c1"):
+        1.533e9 + 425.53e6,
 }
 
 

@@ -128,35 +128,41 @@ __global__ void __launch_bounds__(128) sparse_merge_kernel(
   for (int i = tid; i < 2 * nw; i += 128) bm[i] = 0u;
   __syncthreads();
   const int64_t o0 = int64_t(h) * G + g0;
-  int64_t lo[2], hi[2];
   bool bad = false;
-  for (int L = 0; L < 2; ++L) {
-    lo[L] = hi[L] = 0;
-    if (L >= nlist) continue;
+  // list L of the tile: [lo_L, hi_L) of the indices (empty when its offsets are invalid)
+  auto range = [&](int L, int64_t& lo, int64_t& hi) {
+    lo = hi = 0;
+    if (L >= nlist) return;
     const int64_t a0 = off[o0 + L], a1 = off[o0 + L + 1];
     if (a0 < 0 || a1 < a0 || a1 > n_idx) {
       bad = true;
-      continue;
+      return;
     }
-    lo[L] = a0;
-    hi[L] = a1;
-  }
-  for (int L = 0; L < nlist; ++L)
-    for (int64_t i = lo[L] + tid; i < hi[L]; i += 128) {
+    lo = a0;
+    hi = a1;
+  };
+  int64_t lo0, hi0, lo1, hi1;
+  range(0, lo0, hi0);
+  range(1, lo1, hi1);
+  auto mark = [&](int L, int64_t lo, int64_t hi) {
+    for (int64_t i = lo + tid; i < hi; i += 128) {
       const int kb = idx[i];
-      const int prev = i > lo[L] ? idx[i - 1] : -1;
+      const int prev = i > lo ? idx[i - 1] : -1;
       if (kb < 0 || kb >= nkb || kb <= prev) {
         bad = true;
         continue;
       }
       atomicOr(&bm[L * nw + (kb >> 5)], 1u << (kb & 31));
     }
+  };
+  mark(0, lo0, hi0);
+  mark(1, lo1, hi1);
   if (bad) atomicCAS(err, 0, kErrBadList);
   __syncthreads();
   if (tid >= 32) return;
   // the merged list goes where the two lists were: [off[h G + g0], off[h G + g0 + nlist])
-  const int64_t base = (hi[0] > lo[0] || nlist == 1) ? lo[0] : lo[1];
-  const bool contiguous = nlist == 1 || hi[0] == lo[1] || hi[0] == lo[0] || hi[1] == lo[1];
+  const int64_t base = (hi0 > lo0 || nlist == 1) ? lo0 : lo1;
+  const bool contiguous = nlist == 1 || hi0 == lo1 || hi0 == lo0 || hi1 == lo1;
   int64_t pos = 0;
   for (int w0 = 0; w0 < nw; w0 += 32) {
     const int w = w0 + tid;
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(128) sparse_merge_kernel(
   }
   if (tid == 0) {
     // a merged list may only use the room of the two lists it replaces
-    const bool fits = contiguous && pos <= (hi[0] - lo[0]) + (hi[1] - lo[1]);
+    const bool fits = contiguous && pos <= (hi0 - lo0) + (hi1 - lo1);
     tbase[int64_t(h) * nblocks + b] = base;
     tcnt[int64_t(h) * nblocks + b] = fits ? int32_t(pos) : 0;
     if (!fits) atomicCAS(err, 0, kErrBadList);
@@ -471,20 +477,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SparseCta cta = a.ctas[blockIdx.x];
-  // this CTA's tiles: merged list and its length (0 for a second tile the CTA does not hold)
-  TileRef tr[2];
-  const uint32_t* ent[2];
-  int n[2];
-  for (int t = 0; t < 2; ++t) {
-    const int id = t < cta.count ? a.order[cta.slot + t] : a.order[cta.slot];
-    const int hh = id / a.nblocks;
-    const BlockInfo bi = a.blocks[id - hh * a.nblocks];
-    tr[t].sg = a.segs[bi.seg];
-    tr[t].head = hh;
-    tr[t].qt = bi.blk;
-    ent[t] = a.uni + a.tbase[id];
-    n[t] = t < cta.count ? a.tcnt[id] : 0;
-  }
+  // the query tile this warp serves (TMA 16 / MMA 17 / softmax 0-7: tile 0; 19 / 18 / 8-15:
+  // tile 1), its merged list and length (0 for a second tile the CTA does not hold); one tile
+  // per warp, so nothing here is indexed by a runtime tile number (no local memory)
+  const int t = warp < 16 ? (warp >> 3) : ((warp == kTmaWarp0 || warp == kMmaWarp) ? 0 : 1);
+  const int id = t < cta.count ? a.order[cta.slot + t] : a.order[cta.slot];
+  const int hh = id / a.nblocks;
+  const BlockInfo bi = a.blocks[id - hh * a.nblocks];
+  TileRef tr;
+  tr.sg = a.segs[bi.seg];
+  tr.head = hh;
+  tr.qt = bi.blk;
+  const uint32_t* ent = a.uni + a.tbase[id];
+  const int n = t < cta.count ? a.tcnt[id] : 0;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -519,14 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == kTmaWarp0 || warp == kTmaWarp1) {
-    const int t = warp == kTmaWarp0 ? 0 : 1;
-    producer(&tm_q, &tm_k, &tm_v, S, a, tr[t], t, ent[t], n[t]);
+    producer(&tm_q, &tm_k, &tm_v, S, a, tr, t, ent, n);
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    const int t = warp - kMmaWarp;
-    mma_issuer(S, a, tmem, t, n[t]);
+    mma_issuer(S, a, tmem, t, n);
   } else if (warp < 16) {
-    const int t = warp >> 3;
-    if (t < cta.count) softmax_and_epilogue(S, a, tr[t], tmem, t, warp & 7, lane, ent[t], n[t]);
+    if (t < cta.count) softmax_and_epilogue(S, a, tr, tmem, t, warp & 7, lane, ent, n);
   }
   tc_fence_before();
   __syncthreads();

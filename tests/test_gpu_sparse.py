@@ -157,6 +157,32 @@ def test_sparse_list_breaking_the_contract_is_reported(fa):
     assert plan.last_error() == 0
 
 
+def test_sparse_deterministic_and_wait_limit(fa):
+    """Repeated calls give the same bits (the tiles are ordered on the device, ties in any order,
+    but every tile is computed on its own); a wait limit of one probe makes the block-sparse
+    kernel record an expired wait and return, and the next call with the normal limit is clean
+    and correct."""
+    cu, H = [0, 17, 700], 2
+    q, k, v = inputs.qkv_separate(cu[-1], H, seed=12)
+    off, idx = inputs.block_sparse_lists(cu, H, density=0.5, seed=3, empty_every=4)
+    plan, out, _ = run_sparse(fa, q, k, v, cu, H, off, idx)
+    d_off, d_idx = torch.from_numpy(off).cuda(), torch.from_numpy(idx).cuda()
+    again = torch.empty_like(out)
+    plan.forward_sparse(d_off, d_idx, again)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    plan.set_wait_limit(1)
+    plan.forward_sparse(d_off, d_idx, again)
+    torch.cuda.synchronize()
+    status = plan.last_error()
+    assert status != 0 and (status & 0xFF00) == 0x100
+    plan.set_wait_limit(20000)
+    plan.forward_sparse(d_off, d_idx, again)
+    torch.cuda.synchronize()
+    assert plan.last_error() == 0
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
 def test_sparse_h3_sampled(fa):
     """S=30272, H=56, a quarter of the key blocks listed per query block (the pages' sparsity
     0.75), every 16th list dense: the bench's launch; sampled rows against the oracle."""

@@ -88,14 +88,22 @@ __global__ void __launch_bounds__(256) nvfp4_block_sums_kernel(
   const BlockInfo bi = blocks[b];
   const uint16_t* x = z == 0 ? q : k;
   const int64_t st = z == 0 ? qst : kst, sh = z == 0 ? qsh : ksh;
-  // 128 rows x 16 chunks of 8 BF16
-  for (int i = threadIdx.x; i < kTile * 16; i += 256) {
-    const int r = i >> 4, c8 = (i & 15) * 8;
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (r < bi.nvalid)
-      w = __ldg(reinterpret_cast<const uint4*>(x + int64_t(bi.tok0 + r) * st + int64_t(h) * sh +
-                                               c8));
-    *reinterpret_cast<uint4*>(&tile[r][c8]) = w;
+  // 128 rows x 16 chunks of 8 BF16: all eight loads of a thread in flight, then the stores
+  {
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + 256 * j, r = i >> 4, c8 = (i & 15) * 8;
+      w[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < bi.nvalid)
+        w[j] = __ldg(reinterpret_cast<const uint4*>(x + int64_t(bi.tok0 + r) * st +
+                                                    int64_t(h) * sh + c8));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + 256 * j, r = i >> 4, c8 = (i & 15) * 8;
+      *reinterpret_cast<uint4*>(&tile[r][c8]) = w[j];
+    }
   }
   __syncthreads();
   const int c = threadIdx.x & (kD - 1), half = threadIdx.x >> 7;

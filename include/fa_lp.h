@@ -206,8 +206,11 @@ FA_LP_API int fa_lp_forward_varlen_lse(fa_lp_plan* plan, const int32_t* cu_seqle
  * The lists are read on the device: a list that breaks the contract has its offending entries
  * dropped (its rows' output is then unspecified, but no access leaves the arrays) and
  * fa_lp_get_last_error reports status 0x200 and returns FA_LP_ERR_INVALID_ARG.
- * Device memory: the plan keeps a scratch buffer of 4 * num_indices + 12 * heads * (Tpad / 128)
- * bytes (merged lists and tile tables), grown stream-ordered on `stream` when a call needs more.
+ * Device memory: the plan keeps a scratch buffer of 4 * num_indices + 16 * heads * (Tpad / 128)
+ * bytes (merged lists and tile tables), grown stream-ordered on `stream` when a call needs more;
+ * block-sparse calls on one plan share it, so they must be ordered (one stream, or synchronized).
+ * Three kernels per call: the list merge, the tile order and the attention (the quantize
+ * kernels belong to fa_lp_quantize).
  * Errors: STATE (no quantize on this plan yet), UNSUPPORTED (NVFP4 plan, or a segment longer
  * than 12.5 M tokens), INVALID_ARG, OOM, CUDA.
  */

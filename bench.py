@@ -46,8 +46,9 @@ D = 128
 FP8_OVER_BF16 = 2.0
 FP4_OVER_BF16 = 6.0
 # kernels per step: FP8 amax, pack Q/K, pack V^T, attention; NVFP4 block sums, K means, pack
-# Q/K, pack V^T, attention
-KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 5, "sparse": 5}
+# Q/K, pack V^T, qm K^T table, attention; block-sparse FP8 the FP8 quantize kernels, list merge,
+# tile order, attention
+KERNELS_PER_STEP = {"fp8": 4, "nvfp4": 6, "sparse": 6}
 METRICS = {"fp8": METRIC, "nvfp4": METRIC_NVFP4, "sparse": METRIC_SPARSE}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes) of one attention launch from

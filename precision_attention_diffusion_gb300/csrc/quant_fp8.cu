@@ -134,16 +134,25 @@ __global__ void __launch_bounds__(256) fp8_pack_vt_kernel(const uint16_t* __rest
     descale[2 * H + h] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
   }
   const int sub = threadIdx.x & 15;
-  for (int r = threadIdx.x >> 4; r < kTile; r += 16) {
-    uint2 c = make_uint2(0u, 0u);
-    if (r < bi.nvalid) {
-      const uint4 w =
-          __ldg(reinterpret_cast<const uint4*>(v + int64_t(bi.tok0 + r) * vst + int64_t(h) * vsh) + sub);
-      c = pack8(w, inv);
+  {
+    // all eight 16-byte loads of a thread in flight before any is packed
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = (threadIdx.x >> 4) + 16 * j;
+      w[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < bi.nvalid)
+        w[j] = __ldg(reinterpret_cast<const uint4*>(v + int64_t(bi.tok0 + r) * vst +
+                                                    int64_t(h) * vsh) + sub);
     }
-    uint32_t* row = reinterpret_cast<uint32_t*>(&tile[r][sub * 8]);
-    row[0] = c.x;
-    row[1] = c.y;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = (threadIdx.x >> 4) + 16 * j;
+      const uint2 c = r < bi.nvalid ? pack8(w[j], inv) : make_uint2(0u, 0u);
+      uint32_t* row = reinterpret_cast<uint32_t*>(&tile[r][sub * 8]);
+      row[0] = c.x;
+      row[1] = c.y;
+    }
   }
   __syncthreads();
   uint8_t* dst = vt + int64_t(h) * kD * Tp + int64_t(b) * kTile;

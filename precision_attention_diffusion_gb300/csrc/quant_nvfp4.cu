@@ -243,13 +243,21 @@ __global__ void __launch_bounds__(256) nvfp4_pack_vt_kernel(
   __shared__ __align__(16) uint16_t tile[kTile][kD + 8];  // +8: rows start on distinct banks
   const int b = blockIdx.x, h = blockIdx.y;
   const BlockInfo bi = blocks[b];
-  for (int i = threadIdx.x; i < kTile * 16; i += 256) {
-    const int r = i >> 4, c8 = (i & 15) * 8;
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (r < bi.nvalid)
-      w = __ldg(reinterpret_cast<const uint4*>(v + int64_t(bi.tok0 + r) * vst + int64_t(h) * vsh +
-                                               c8));
-    *reinterpret_cast<uint4*>(&tile[r][c8]) = w;
+  {  // all eight 16-byte loads of a thread in flight, then the shared-memory stores
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + 256 * j, r = i >> 4, c8 = (i & 15) * 8;
+      w[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < bi.nvalid)
+        w[j] = __ldg(reinterpret_cast<const uint4*>(v + int64_t(bi.tok0 + r) * vst +
+                                                    int64_t(h) * vsh + c8));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = threadIdx.x + 256 * j, r = i >> 4, c8 = (i & 15) * 8;
+      *reinterpret_cast<uint4*>(&tile[r][c8]) = w[j];
+    }
   }
   __syncthreads();
   // 128 channels x 8 groups; a warp takes 32 consecutive channels of one group

@@ -183,10 +183,12 @@ def test_sparse_deterministic_and_wait_limit(fa):
     assert torch.equal(out.view(torch.int16), again.view(torch.int16))
 
 
-def test_sparse_h3_sampled(fa):
-    """S=30272, H=56, a quarter of the key blocks listed per query block (the pages' sparsity
-    0.75), every 16th list dense: the bench's launch; sampled rows against the oracle."""
-    cu, H = [0, 30272], 56
+@pytest.mark.parametrize("cu", [[0, 30272], [0, 0, 17, 4113, 4113, 31800, 32768]])
+def test_sparse_h3_sampled(fa, cu):
+    """H=56, a quarter of the key blocks listed per query block (the pages' sparsity 0.75), every
+    16th list dense: the bench's launch at S=30272, and the packed varlen layout with empty, short
+    and trailing segments; sampled rows against the oracle."""
+    H = 56
     q, k, v = inputs.qkv_separate(cu[-1], H, seed=0)
     off, idx = inputs.block_sparse_lists(cu, H, density=0.25, seed=0, dense_every=16)
     plan, out, _ = run_sparse(fa, q, k, v, cu, H, off, idx)

@@ -303,3 +303,17 @@ def test_nvfp4_means_wide_exponent_columns(fa):
         x[20:30, :, 11] = 2.0 ** -130
     q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
     check_nvfp4_quant(fa, q, k, v, cu, H)
+
+
+def test_nvfp4_many_small_segments(fa):
+    """300 segments of 0 to 200 tokens (seeded), H=2, K with a channel offset: every row."""
+    g = np.random.default_rng(32)
+    lens = g.integers(0, 201, 300)
+    lens[g.integers(0, 300, 40)] = 0
+    cu = [0] + np.cumsum(lens).tolist()
+    H = 2
+    q, k, v = inputs.qkv_separate(cu[-1], H, seed=32)
+    k = with_k_offset(k, H, 32)
+    plan, out = run_nvfp4(fa, q, k, v, cu, H)
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    check_nvfp4_out(out, q, k, v, z, cu, all_rows(cu, H))

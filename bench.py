@@ -256,6 +256,8 @@ def oracle_sample(cu, H, seconds, seed=0, mode="fp8", sparse_name=None):
     # full-workload estimate: each head quantizes once and runs every query row of every segment
     per_row = t_attn / R
     # per-row cost grows with its segment's length: scale by L_s / L_longest
+    qlabel = "NVFP4" if mode == "nvfp4" else "FP8"
+    alabel = {"fp8": "FP8", "nvfp4": "NVFP4", "sparse": "block-sparse FP8"}[mode]
     if mode == "sparse":
         est_s = H * (t_quant + per_row * T)
         value = sparse_flops(cu, H, off_all, idx_all) / est_s / 1e12
@@ -263,8 +265,8 @@ def oracle_sample(cu, H, seconds, seed=0, mode="fp8", sparse_name=None):
         est_s = H * (t_quant + per_row * sum(x * x for x in lens) / L)
         value = attn_flops(cu, H) / est_s / 1e12
     return dict(value=value, unit=UNIT, cores=ncores, kind="oracle",
-                sample=(f"head 0 of {H}: {mode.upper()} quantize of its full Q/K/V ({T} tokens, "
-                        f"{t_quant:.2f} s) + {mode.upper()}-emulating attention of {R} random query "
+                sample=(f"head 0 of {H}: {qlabel} quantize of its full Q/K/V ({T} tokens, "
+                        f"{t_quant:.2f} s) + {alabel}-emulating attention of {R} random query "
                         f"rows of "
                         f"the {L}-token segment ({t_attn:.2f} s); extrapolated to all {H} heads "
                         f"and rows"),

@@ -324,6 +324,23 @@ def run_reference(args):
     return 0
 
 
+def link_rates(hbuf, dbuf, stream):
+    """Host-device link rates on this machine (GB/s): one copy of the page-locked input buffer each
+    way, timed on the device. They bound the end-to-end numbers, which move with them."""
+    import torch
+    res = {}
+    for name, dst, src in (("h2d_gbs", dbuf, hbuf), ("d2h_gbs", hbuf, dbuf)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    return res
+
+
 def config_of(name, cu, H):
     T = cu[-1]
     c = {"workload": name, "tokens": T, "heads": H, "head_dim": D,
@@ -473,6 +490,8 @@ def run_ours(args):
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "call": "fa_lp_attention_sparse_host (page-locked host buffers and lists, head "
                        "chunks of the library's choice, copies overlapping the compute)"}
+        with torch.cuda.stream(stream):
+            e2e["link"] = link_rates(hbuf, buf, stream)
     elif not args.no_e2e:
         hbuf = buf.cpu().pin_memory()
         hout = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
@@ -500,6 +519,8 @@ def run_ours(args):
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "call": "fa_lp_attention_host (page-locked host buffers, head chunks of the "
                        "library's choice, copies overlapping the compute)"}
+        with torch.cuda.stream(stream):
+            e2e["link"] = link_rates(hbuf, buf, stream)
 
     pk = peaks()
     achieved = flops / (fwd_ms / 1e3) / 1e12

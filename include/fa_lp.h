@@ -14,6 +14,9 @@
  *                      elements, K centred by its segment's per-channel mean, Q by its 128-row
  *                      block mean (the qm K^T term added back), V transposed with per-16-key
  *                      scales, two-level P scaling (row maximum brought to 448*6).
+ *   block-sparse      : fa_lp_forward_sparse on an FP8 plan: the FP8 arithmetic over the 64-key
+ *                      blocks the caller lists for every 64-row query block (SGLang PR #40116
+ *                      "Add SM120 Sage compute for SubBlock sparse attention", Modifications).
  *
  * Conventions (all entry points):
  *   - Every function returns an int status (FA_LP_OK or an FA_LP_ERR_* code); nothing throws

@@ -331,16 +331,33 @@ void build_plan(fa_lp_plan* p) {
     // 1.6 GB for one 30272-token segment at H = 56)
     p->c_off.assign(ns, 0);
     size_t floats = 0;
+    // N tiles per table CTA: the run r in [4, 16] whose CTAs (M tiles x runs x heads) fill the
+    // GPU's waves best, i.e. the least ceil(CTAs / SMs) * r; ties go to the longer run
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
+        sms <= 0) {
+      cudaGetLastError();
+      sms = 152;
+    }
     for (int s = 0; s < ns; ++s) {
       const int64_t nb = p->segs[s].nblk;
       p->c_off[s] = int64_t(floats);
       floats += size_t(H) * size_t(nb) * size_t(nb) * 128;
-      const int64_t ntiles = (nb * 128 + 255) / 256;
+      const int64_t ntiles = (nb * 128 + 255) / 256, nm = (nb + 127) / 128;
+      int run = falp::kQmkTilesPer;
+      double best = 1e300;
+      for (int r = 4; r <= 16; ++r) {
+        const double ctas = double(nm) * double((ntiles + r - 1) / r) * double(H);
+        const double cost = std::ceil(ctas / sms) * r;
+        if (cost < best - 1e-9 || (std::fabs(cost - best) <= 1e-9 && r > run)) {
+          best = cost;
+          run = r;
+        }
+      }
       for (int64_t mt = 0; mt * 128 < nb; ++mt)
-        for (int64_t nt = 0; nt < ntiles; nt += falp::kQmkTilesPer)
+        for (int64_t nt = 0; nt < ntiles; nt += run)
           p->qmk_items.push_back(falp::QmkItem{
-              s, int32_t(mt), int32_t(nt),
-              int32_t(std::min<int64_t>(falp::kQmkTilesPer, ntiles - nt))});
+              s, int32_t(mt), int32_t(nt), int32_t(std::min<int64_t>(run, ntiles - nt))});
     }
     w.qmk = take(floats * 4);
   }

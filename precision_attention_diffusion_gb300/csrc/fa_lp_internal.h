@@ -60,7 +60,7 @@ struct QmkItem {
   int32_t nt;       // first 256-key N tile
   int32_t ntiles;   // N tiles of this CTA
 };
-constexpr int kQmkTilesPer = 8;  // N tiles per table CTA
+constexpr int kQmkTilesPer = 8;  // N tiles per table CTA (default; the plan picks per segment)
 
 // Workspace layout of one plan (byte offsets from the workspace base, 1024-aligned).
 struct WsLayout {

@@ -11,8 +11,9 @@
 // attention kernel adds Tq to its scores. Layout: segment s at float offset c_off[s], then
 // [H][nb_s][128 nb_s].
 //
-// One CTA = one (segment, 128-block M tile, head) and a run of up to kQmkTilesPer 256-key N tiles
-// (A is built once per CTA; B, the MMAs and the stores repeat per N tile). qm is split into three BF16
+// One CTA = one (segment, 128-block M tile, head) and a run of up to 16 256-key N tiles (the plan
+// picks the run per segment so that the CTAs fill whole waves; A is built once per CTA; B, the
+// MMAs and the stores repeat per N tile). qm is split into three BF16
 // pieces (hi + mid + lo carries its 24 significant bits) and deq(Kc) = e2m1 x ue4m3 has at most 6
 // significant bits, exact in BF16; one tcgen05.mma kind::f16 stream (M=128, N=256, K=16 steps over
 // 3 x 128 channels) accumulates in FP32 in tensor memory. B tiles and accumulators are double

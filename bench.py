@@ -13,7 +13,9 @@ flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 --workload nvfp4_s30272_h56 times the NVFP4 path instead (K with a per-channel offset N(0, 4)),
-against the dense FP4 peak.
+against the dense FP4 peak. The default line also carries two sub-objects timed in the same
+process by the same procedure, each with its own clock sample: "nvfp4" (nvfp4_s30272_h56) and
+"sparse" (sparse_fp8_s30272_h56, block-sparse FP8 at density 0.25); --no-extra-arms skips them.
 
 N > 1 (torchrun, one process per GPU): independent replicas of the full workload on every rank
 (the path has no exchange step), max-over-ranks time, weak scaling.
@@ -73,6 +75,8 @@ def parse_args():
     ap.add_argument("--workload", default="fp8_s30272_h56")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-arms", action="store_true",
+                    help="default workload only: skip the nvfp4 and sparse sub-objects")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
 
@@ -357,29 +361,22 @@ def config_of(name, cu, H):
     return c
 
 
-def run_ours(args):
+def run_arm(args, name, ws, rank, with_e2e, with_cpu):
+    """One workload's device arm: W untimed steps, then K timed steps (quantize + forward on
+    resident inputs) bracketed by barriers and synchronizes, with the SM clocks sampled during
+    the timed region; optionally the end-to-end host-buffer leg and the CPU-oracle baseline.
+    Returns the JSON line of that workload."""
     import torch
 
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
     dev = torch.cuda.current_device()
-
-    from precision_attention_diffusion_gb300 import build as fbuild
-    fbuild.build()
     from precision_attention_diffusion_gb300 import fa_lp
 
-    cu, H = workload(args.workload)
-    mode = mode_of(args.workload)
+    cu, H = workload(name)
+    mode = mode_of(name)
     T = cu[-1]
     flops = attn_flops(cu, H)
     if mode == "sparse":
-        import numpy as np
-        off_h, idx_h = sparse_lists(args.workload, cu, H, seed=rank)
+        off_h, idx_h = sparse_lists(name, cu, H, seed=rank)
         flops = sparse_flops(cu, H, off_h, idx_h)
         d_off = torch.from_numpy(off_h).cuda()
         d_idx = torch.from_numpy(idx_h).cuda()
@@ -452,13 +449,12 @@ def run_ours(args):
         raise RuntimeError("device wait expired in the timed region")
     ms_per_step = total_ms / K
     value = ws * flops / (ms_per_step / 1e3) / 1e12
-
     # end to end through the public call with host buffers (fa_lp_attention_host): every step
     # copies the inputs from page-locked host memory, quantizes, runs the attention and copies the
     # output back; the library overlaps the copies of one chunk of heads with the compute of the
     # next
     e2e = None
-    if not args.no_e2e and mode == "sparse":
+    if with_e2e and mode == "sparse":
         # block-sparse end to end through fa_lp_attention_sparse_host: every step copies Q/K/V and
         # the block lists from page-locked host memory, quantizes, runs the block-sparse forward
         # and copies the output back; head chunks overlap their copies with the compute
@@ -492,7 +488,7 @@ def run_ours(args):
                        "chunks of the library's choice, copies overlapping the compute)"}
         with torch.cuda.stream(stream):
             e2e["link"] = link_rates(hbuf, buf, stream)
-    elif not args.no_e2e:
+    elif with_e2e:
         hbuf = buf.cpu().pin_memory()
         hout = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
         hq, hk, hv = hbuf[:, 0], hbuf[:, 1], hbuf[:, 2]
@@ -526,7 +522,7 @@ def run_ours(args):
     achieved = flops / (fwd_ms / 1e3) / 1e12
     kname = {"nvfp4": "attn_nvfp4", "fp8": "attn_fp8", "sparse": "attn_fp8_sparse"}[mode]
     sha = file_sha(os.path.join(ROOT, "precision_attention_diffusion_gb300", "csrc", kname + ".cu"))
-    traffic = NCU_TRAFFIC.get((args.workload, sha))
+    traffic = NCU_TRAFFIC.get((name, sha))
     pkey = "fp4" if mode == "nvfp4" else "fp8"
     # DRAM bytes the attention launch must move: the quantized operands once, the BF16 output once
     Tp = sum(-(-(b - a) // 128) * 128 for a, b in zip(cu[:-1], cu[1:]))
@@ -556,16 +552,48 @@ def run_ours(args):
         "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-        "data": "synthetic", "config": config_of(args.workload, cu, H),
+        "data": "synthetic", "config": config_of(name, cu, H),
         "forward_ms": fwd_ms, "forward_tflops": achieved, "quantize_ms": q_ms,
         "quantize_gbs": q_bytes / (q_ms / 1e3) / 1e9,
         "frac_of_fp8_peak": achieved / pk["fp8"],
         "roofline": roof, "clocks": clocks, "e2e": e2e,
         "gpu_launches": KERNELS_PER_STEP[mode] * K,
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds, mode=mode,
-                                             sparse_name=args.workload)
+    if with_cpu:
+        line["cpu_baseline"] = oracle_sample(cu, H, args.cpu_seconds, mode=mode, sparse_name=name)
+    del buf, q, k, v, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+# Sub-objects of the default line: the second hot path (NVFP4) and the block-sparse forward at the
+# same shape, each timed in the same process by the same procedure with its own clock sample.
+EXTRA_ARMS = (("nvfp4", "nvfp4_s30272_h56"), ("sparse", "sparse_fp8_s30272_h56"))
+ARM_KEYS = ("metric", "value", "unit", "ms_per_step", "forward_ms", "forward_tflops",
+            "quantize_ms", "quantize_gbs", "roofline", "clocks", "gpu_launches", "config", "dtype")
+
+
+def run_ours(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+
+    from precision_attention_diffusion_gb300 import build as fbuild
+    fbuild.build()
+
+    line = run_arm(args, args.workload, ws, rank, with_e2e=not args.no_e2e,
+                   with_cpu=rank == 0 and ws == 1 and not args.no_cpu_baseline)
+    if args.workload == "fp8_s30272_h56" and not args.no_extra_arms:
+        for key, name in EXTRA_ARMS:
+            sub = run_arm(args, name, ws, rank, with_e2e=False, with_cpu=False)
+            line[key] = {k: sub[k] for k in ARM_KEYS if k in sub}
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

@@ -160,7 +160,9 @@ FA_LP_API int fa_lp_quantize(fa_lp_plan* plan, const void* q, int64_t q_stride_t
  * (O and l rescaled by 2^(m_old - m) whenever it moves); P' = 2^(s - m) * 2688; per 16 keys a
  * UE4M3 scale E4M3_rn(max P' / 6) and E2M1_rn codes of P' / scale; l sums the dequantized P; O
  * accumulates deq(P) * deq(V) in FP32; out = BF16_rn(O / l).
- * Errors: STATE (no quantize on this plan yet), INVALID_ARG, UNSUPPORTED, CUDA.
+ * Errors: STATE (the device's workspace does not hold this plan's codes: no quantize of this
+ * plan yet, or another plan quantized on the device since, or the workspace was released),
+ * INVALID_ARG, UNSUPPORTED, CUDA.
  */
 FA_LP_API int fa_lp_forward_varlen(fa_lp_plan* plan, const int32_t* cu_seqlens_dev, void* out,
                          int64_t out_stride_tok, int64_t out_stride_head, void* stream);
@@ -214,7 +216,7 @@ FA_LP_API int fa_lp_forward_varlen_lse(fa_lp_plan* plan, const int32_t* cu_seqle
  * block-sparse calls on one plan share it, so they must be ordered (one stream, or synchronized).
  * Three kernels per call: the list merge, the tile order and the attention (the quantize
  * kernels belong to fa_lp_quantize).
- * Errors: STATE (no quantize on this plan yet), UNSUPPORTED (NVFP4 plan, or a segment longer
+ * Errors: STATE (as fa_lp_forward_varlen), UNSUPPORTED (NVFP4 plan, or a segment longer
  * than 12.5 M tokens), INVALID_ARG, OOM, CUDA.
  */
 FA_LP_API int fa_lp_forward_sparse(fa_lp_plan* plan, const int32_t* cu_seqlens_dev,
@@ -376,8 +378,12 @@ FA_LP_API int fa_lp_encode(int format, const float* x, int64_t n, uint8_t* codes
  * a fixed 12 KB device array inside the library, held by every GPU that loads it until the
  * process exits, shared by all calls on a device and cleared by each call. Calls that overlap
  * on the GPU race on it; order them on one stream or synchronize. The first call on a device
- * looks up the array's device address; make it before any stream capture begins.
- * Errors: INVALID_ARG (NULL, misaligned or non-positive strides, heads out of range),
+ * looks up the array's device address (cudaGetSymbolAddress, with that device current); make it
+ * before any stream capture begins. The address is kept per CUDA context: after the device's
+ * context is destroyed and re-created (cudaDeviceReset), the next call looks it up again, so
+ * that call too must come before any capture.
+ * Errors: INVALID_ARG (NULL, misaligned or non-positive strides, heads out of range, descale
+ * not 4-byte aligned),
  * UNSUPPORTED (device not sm_103), CUDA.
  */
 FA_LP_API int fa_lp_fp8_descale_noalloc(const void* q, int64_t q_stride_tok,

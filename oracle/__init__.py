@@ -64,13 +64,14 @@ def lib() -> ctypes.CDLL:
             L.orc_fp8_quantize.argtypes = [P, i64, i32, i64, i64, P, P, i32]
             L.orc_attn_exact.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32, P, i32,
                                          f64, P, i64, P, P, i32]
+            L.orc_fp8_quantize_seg.argtypes = [P, i64, i32, i64, i64, P, i32, P, P, i32]
             L.orc_attn_fp8.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, i32, i32, f64, P,
-                                       i64, P, P, P, i32]
+                                       i64, P, P, P, i32, i32]
             L.orc_attn_exact_sparse.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32,
                                                 P, i32, f64, P, P, P, i64, P, P, i32]
             L.orc_attn_exact_sparse.restype = i32
             L.orc_attn_fp8_sparse.argtypes = [P, P, P, P, P, P, i64, i32, P, i32, f64, P, P, i32,
-                                              f64, P, i64, P, P, P, i32]
+                                              f64, P, i64, P, P, P, i32, i32]
             L.orc_attn_fp8_sparse.restype = i32
             L.orc_nvfp4_kmean.argtypes = [P, i64, i64, i64, i32, P, i32, P, i32]
             L.orc_nvfp4_qblock_offsets.argtypes = [P, i32, P]; L.orc_nvfp4_qblock_offsets.restype = i64
@@ -150,6 +151,19 @@ def fp8_quantize(x, nthreads=0):
     return codes, d
 
 
+def fp8_quantize_seg(x, cu, nthreads=0):
+    """Per-segment FP8 mode: x [T,H,128] BF16 bits, cu_seqlens -> (codes [T,H,128] uint8,
+    descale [nseg,H] float32): one amax per (segment, head) over the segment's own tokens."""
+    arr, st, sh = _bf16_view(x)
+    T, H = x.shape[0], x.shape[1]
+    cu = np.ascontiguousarray(cu, np.int32)
+    codes = np.zeros((T, H, D), np.uint8)
+    d = np.empty((len(cu) - 1, H), np.float32)
+    lib().orc_fp8_quantize_seg(_p(arr), T, H, st, sh, _p(cu), len(cu) - 1, _p(codes), _p(d),
+                               _threads(nthreads))
+    return codes, d
+
+
 def attn_exact(q, k, v, cu, rows, scale, nthreads=0, lse=False):
     """C1: exact FP64 attention for rows [(token, head)] -> [n,128] float64; with lse=True also
     the row's log-sum-exp log sum_j exp(q.k_j scale) -> (out, lse [n])."""
@@ -164,9 +178,21 @@ def attn_exact(q, k, v, cu, rows, scale, nthreads=0, lse=False):
     return (out, ls) if lse else out
 
 
+def _seg_scales(dq, dk, dv, cu, H):
+    """1 when the descales are per (segment, head) ([nseg, H]), 0 when per head ([H])."""
+    nseg = len(cu) - 1
+    shapes = {tuple(np.shape(a)) for a in (dq, dk, dv)}
+    if shapes == {(H,)}:
+        return 0
+    if shapes == {(nseg, H)}:
+        return 1
+    raise ValueError("descales must all be [H] or all [nseg, H]")
+
+
 def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, tau=0.0,
              nthreads=0, lse=False):
     """C2: FP8-emulating attention from codes/descales -> (out fp64 [n,128], out bf16 bits).
+    Descales [H] (one per head, reading r1) or [nseg, H] (the per-segment mode).
     n_kv: key-tile width; tau: threshold (log2 units) for moving the reference maximum, 0 = the
     exact running maximum; p_shift: power-of-two shift applied to P before E4M3 rounding.
     lse=True appends the row's m + log(l) (reading r15) -> (o64, o16, lse [n])."""
@@ -177,10 +203,11 @@ def attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, scale, n_kv=128, p_shift=0, tau=0
     o64 = np.empty((rows.shape[0], D), np.float64)
     o16 = np.empty((rows.shape[0], D), np.uint16)
     ls = np.empty(rows.shape[0], np.float64)
+    seg = _seg_scales(dq, dk, dv, cu, cq.shape[1])
     lib().orc_attn_fp8(_p(cq), _p(ck), _p(cv), _p(dq), _p(dk), _p(dv), cq.shape[0], cq.shape[1],
                        _p(cu), len(cu) - 1, float(scale), int(n_kv), int(p_shift), float(tau),
                        _p(rows),
-                       rows.shape[0], _p(o64), _p(o16), _p(ls), _threads(nthreads))
+                       rows.shape[0], _p(o64), _p(o16), _p(ls), _threads(nthreads), seg)
     return (o64, o16, ls) if lse else (o64, o16)
 
 
@@ -225,10 +252,11 @@ def attn_fp8_sparse(cq, ck, cv, dq, dk, dv, cu, blk_off, blk_idx, rows, scale, p
     o64 = np.empty((rows.shape[0], D), np.float64)
     o16 = np.empty((rows.shape[0], D), np.uint16)
     ls = np.empty(rows.shape[0], np.float64)
+    seg = _seg_scales(dq, dk, dv, cu, cq.shape[1])
     st = lib().orc_attn_fp8_sparse(_p(cq), _p(ck), _p(cv), _p(dq), _p(dk), _p(dv), cq.shape[0],
                                    cq.shape[1], _p(cu), len(cu) - 1, float(scale), _p(off),
                                    _p(idx), int(p_shift), float(tau), _p(rows), rows.shape[0],
-                                   _p(o64), _p(o16), _p(ls), _threads(nthreads))
+                                   _p(o64), _p(o16), _p(ls), _threads(nthreads), seg)
     if st != 0:
         raise ValueError("block list outside its segment or not strictly ascending")
     return (o64, o16, ls) if lse else (o64, o16)

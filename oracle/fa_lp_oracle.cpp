@@ -18,7 +18,9 @@
 //    maximum brought to 448*6) and its Parameters list (cu_seqlens contract, default scale).
 //
 // Readings taken where the pages are silent (each is stated again where it is used):
-//  r1  FP8 amax is per (tensor, head) over all tokens of the packed input.
+//  r1  FP8 amax is per (tensor, head) over all tokens of the packed input. Opt-in alternative
+//      (the per-segment FP8 mode): one amax per (segment, tensor, head) over the segment's own
+//      tokens, so that one long segment does not set a short segment's scale.
 //  r2  inv = fl32(448/amax), code = E4M3(fl32(x*inv)), descale = fl32(amax/448); amax==0 -> 1.
 //  r3  E4M3: round to nearest, ties to even, saturate to +-448, sign of zero kept, subnormals kept.
 //  r4  FP8 P is the unscaled exp(S - m) in [0,1], rounded through fp32 then to E4M3 (shift p = 0;
@@ -365,6 +367,33 @@ void orc_fp8_quantize(const uint16_t* x, int64_t T, int H, int64_t st, int64_t s
   });
 }
 
+// The per-segment alternative of reading r1 (same arithmetic, r2 and r3, with the amax taken
+// over the tokens of one segment): descale: [nseg][H]; an empty segment gets descale 1 and no
+// codes.
+void orc_fp8_quantize_seg(const uint16_t* x, int64_t T, int H, int64_t st, int64_t sh,
+                          const int32_t* cu, int nseg, uint8_t* codes, float* descale,
+                          int nthreads) {
+  (void)T;
+  parallel_for(static_cast<int64_t>(nseg) * H, nthreads, [&](int64_t sh_idx) {
+    const int s = static_cast<int>(sh_idx / H), h = static_cast<int>(sh_idx % H);
+    const int64_t a = cu[s], b = cu[s + 1];
+    float amax = 0.0f;
+    for (int64_t t = a; t < b; ++t)
+      for (int c = 0; c < kD; ++c) amax = std::max(amax, std::fabs(load_bf16(x, t, h, c, st, sh)));
+    float inv = 1.0f, d = 1.0f;
+    if (amax > 0.0f) {
+      inv = 448.0f / amax;
+      d = amax / 448.0f;
+    }
+    descale[sh_idx] = d;
+    for (int64_t t = a; t < b; ++t)
+      for (int c = 0; c < kD; ++c) {
+        const float y = load_bf16(x, t, h, c, st, sh) * inv;
+        codes[(t * H + h) * kD + c] = e4m3_encode(y);
+      }
+  });
+}
+
 // ---------------------------------------------------------------------------------------------
 // C1: exact attention in FP64 for a list of query rows (token, head). The plain definition from
 // the FlashInfer docs' formula: out[i] = softmax(q_i k^T * scale) v over the keys of i's segment.
@@ -398,7 +427,7 @@ void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
                   const float* dq, const float* dk, const float* dv,
                   int64_t T, int H, const int32_t* cu, int nseg, double scale, int n_kv,
                   int p_shift, double tau, const int64_t* rows, int64_t nrows, double* out64,
-                  uint16_t* out16, double* lse, int nthreads) {
+                  uint16_t* out16, double* lse, int nthreads, int seg_scales) {
   (void)T;
   parallel_for(nrows, nthreads, [&](int64_t r) {
     const int64_t t = rows[2 * r];
@@ -407,8 +436,10 @@ void orc_attn_fp8(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
     Ranges tiles;
     for (int64_t j0 = cu[s]; j0 < cu[s + 1]; j0 += n_kv)
       tiles.push_back({j0, std::min<int64_t>(cu[s + 1], j0 + n_kv)});
-    fp8_row(cq, ck, cv, dq, dk, dv, H, t, h, tiles, scale, p_shift, tau, out64 + r * kD,
-            out16 ? out16 + r * kD : nullptr, lse ? lse + r : nullptr);
+    // per-segment scales: the descale rows of the query's segment ([nseg][H] arrays)
+    const int64_t so = seg_scales ? static_cast<int64_t>(s) * H : 0;
+    fp8_row(cq, ck, cv, dq + so, dk + so, dv + so, H, t, h, tiles, scale, p_shift, tau,
+            out64 + r * kD, out16 ? out16 + r * kD : nullptr, lse ? lse + r : nullptr);
   });
 }
 
@@ -446,7 +477,7 @@ int orc_attn_fp8_sparse(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
                         const int32_t* cu, int nseg, double scale, const int32_t* blk_off,
                         const int32_t* blk_idx, int p_shift, double tau, const int64_t* rows,
                         int64_t nrows, double* out64, uint16_t* out16, double* lse,
-                        int nthreads) {
+                        int nthreads, int seg_scales) {
   (void)T;
   std::vector<int64_t> qb0;
   const int64_t G = sparse_qblock_offsets(cu, nseg, qb0);
@@ -459,8 +490,9 @@ int orc_attn_fp8_sparse(const uint8_t* cq, const uint8_t* ck, const uint8_t* cv,
       bad[r] = 1;
       tiles.clear();
     }
-    fp8_row(cq, ck, cv, dq, dk, dv, H, t, h, tiles, scale, p_shift, tau, out64 + r * kD,
-            out16 ? out16 + r * kD : nullptr, lse ? lse + r : nullptr);
+    const int64_t so = seg_scales ? static_cast<int64_t>(segment_of(cu, nseg, t)) * H : 0;
+    fp8_row(cq, ck, cv, dq + so, dk + so, dv + so, H, t, h, tiles, scale, p_shift, tau,
+            out64 + r * kD, out16 ? out16 + r * kD : nullptr, lse ? lse + r : nullptr);
   });
   return std::count(bad.begin(), bad.end(), 1) ? -1 : 0;
 }

@@ -53,8 +53,23 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct DevWs {
   void* ptr = nullptr;
   size_t bytes = 0;
+  // the plan whose codes the workspace holds (the last quantize on this device) and that
+  // quantize's generation: a forward of any other plan finds its codes overwritten
+  const fa_lp_plan* owner = nullptr;
+  uint64_t gen = 0;
 };
 std::map<int, DevWs> g_ws;
+uint64_t g_quant_gen = 0;  // generations of fa_lp_quantize calls (under g_mu)
+
+// Workspace base of plan p for a forward, or FA_LP_ERR_STATE when the workspace no longer holds
+// p's codes (never quantized, released, grown, or another plan quantized since). Under g_mu.
+int workspace_of_plan(const fa_lp_plan* p, void** base) {
+  const DevWs& w = g_ws[p->device];
+  if (!w.ptr || w.bytes < p->ws.total || w.owner != p || w.gen != p->quant_gen)
+    return FA_LP_ERR_STATE;
+  *base = w.ptr;
+  return FA_LP_OK;
+}
 
 // ---- device capability check ---------------------------------------------------------------------
 int check_device(int device) {
@@ -331,29 +346,35 @@ void build_plan(fa_lp_plan* p) {
     // 1.6 GB for one 30272-token segment at H = 56)
     p->c_off.assign(ns, 0);
     size_t floats = 0;
-    // N tiles per table CTA: the run r in [4, 16] whose CTAs (M tiles x runs x heads) fill the
-    // GPU's waves best, i.e. the least ceil(CTAs / SMs) * r; ties go to the longer run
+    // N tiles per table CTA: one run r in [4, 16] for every segment, since the table kernel
+    // launches all segments' tiles in one grid: the r whose CTAs (sum over segments of M tiles x
+    // runs, times heads) fill the GPU's waves best, i.e. the least ceil(CTAs / SMs) * r (a CTA's
+    // time grows with its run); ties go to the longer run
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
         sms <= 0) {
       cudaGetLastError();
       sms = 152;
     }
+    auto ntiles_of = [&](int s) { return (int64_t(p->segs[s].nblk) * 128 + 255) / 256; };
+    auto nm_of = [&](int s) { return (int64_t(p->segs[s].nblk) + 127) / 128; };
+    int run = falp::kQmkTilesPer;
+    double best = 1e300;
+    for (int r = 4; r <= 16; ++r) {
+      double ctas = 0.0;
+      for (int s = 0; s < ns; ++s)
+        ctas += double(nm_of(s)) * double((ntiles_of(s) + r - 1) / r) * double(H);
+      const double cost = std::ceil(ctas / sms) * r;
+      if (cost < best - 1e-9 || (std::fabs(cost - best) <= 1e-9 && r > run)) {
+        best = cost;
+        run = r;
+      }
+    }
     for (int s = 0; s < ns; ++s) {
       const int64_t nb = p->segs[s].nblk;
       p->c_off[s] = int64_t(floats);
       floats += size_t(H) * size_t(nb) * size_t(nb) * 128;
-      const int64_t ntiles = (nb * 128 + 255) / 256, nm = (nb + 127) / 128;
-      int run = falp::kQmkTilesPer;
-      double best = 1e300;
-      for (int r = 4; r <= 16; ++r) {
-        const double ctas = double(nm) * double((ntiles + r - 1) / r) * double(H);
-        const double cost = std::ceil(ctas / sms) * r;
-        if (cost < best - 1e-9 || (std::fabs(cost - best) <= 1e-9 && r > run)) {
-          best = cost;
-          run = r;
-        }
-      }
+      const int64_t ntiles = ntiles_of(s);
       for (int64_t mt = 0; mt * 128 < nb; ++mt)
         for (int64_t nt = 0; nt < ntiles; nt += run)
           p->qmk_items.push_back(falp::QmkItem{
@@ -442,7 +463,9 @@ const char* fa_lp_status_string(int status) {
     case FA_LP_ERR_CUDA: return "CUDA error";
     case FA_LP_ERR_OOM: return "out of device memory";
     case FA_LP_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
-    case FA_LP_ERR_STATE: return "call out of order (quantize before forward)";
+    case FA_LP_ERR_STATE:
+      return "call out of order (quantize this plan before its forward; another plan's quantize "
+             "on the same device in between overwrites the shared workspace)";
     default: return "unknown status";
   }
 }
@@ -567,6 +590,13 @@ int fa_lp_quantize(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const
                                            ksh, v, vst, vsh, stream);
     if (st != FA_LP_OK) return st;
   }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevWs& w = g_ws[p->device];
+    w.owner = p;
+    w.gen = ++g_quant_gen;
+    p->quant_gen = w.gen;
+  }
   p->quantized = true;
   return FA_LP_OK;
 }
@@ -587,9 +617,7 @@ int fa_lp_forward_varlen_lse(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void*
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    const DevWs& w = g_ws[p->device];
-    if (!w.ptr || w.bytes < p->ws.total) return FA_LP_ERR_STATE;
-    base = w.ptr;
+    if ((st = workspace_of_plan(p, &base)) != FA_LP_OK) return st;
   }
   if (p->work.empty()) return FA_LP_OK;
   return (p->mode == FA_LP_MODE_FP8)
@@ -635,9 +663,7 @@ int fa_lp_forward_sparse(fa_lp_plan* p, const int32_t* cu_seqlens_dev,
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    const DevWs& w = g_ws[p->device];
-    if (!w.ptr || w.bytes < p->ws.total) return FA_LP_ERR_STATE;
-    base = w.ptr;
+    if ((st = workspace_of_plan(p, &base)) != FA_LP_OK) return st;
     // per-plan scratch: merged lists (as many entries as the lists) + tile tables; grow-only,
     // stream-ordered
     const size_t nb = p->blocks.size(), H = size_t(p->heads);

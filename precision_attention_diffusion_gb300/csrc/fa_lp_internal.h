@@ -132,6 +132,7 @@ struct fa_lp_plan {
   falp::SparseCta* d_sp_ctas = nullptr;
   int* d_err = nullptr;  // [0]: sticky device status, [1]: abort word (launch generation)
   bool quantized = false;
+  uint64_t quant_gen = 0;  // generation of this plan's last quantize (the workspace's owner tag)
   int refcount = 1;
   falp::HostPipe host;  // created by the first fa_lp_attention_host call
 };

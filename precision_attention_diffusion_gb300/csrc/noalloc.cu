@@ -12,8 +12,9 @@
 // keeps it until the process exits. All calls on a device share it and each call clears it first:
 // calls must be ordered on the GPU (one stream, or streams the caller synchronizes); calls that
 // overlap on the GPU race on it. The first call on each device looks up the array's device
-// address (cudaGetSymbolAddress, with that device current) and caches it; make that first call
-// before any stream capture begins.
+// address (cudaGetSymbolAddress, with that device current) and caches it for that device's CUDA
+// context; make that first call before any stream capture begins (and, after cudaDeviceReset,
+// the first call in the new context likewise).
 #include "fa_lp_internal.h"
 
 #include <mutex>
@@ -26,21 +27,55 @@ constexpr int kNoAllocTok = 256;  // tokens per block of the amax pass
 
 static __device__ __align__(256) uint32_t g_amax_scratch[3 * kMaxHeadsNoAlloc];
 
-// Address of g_amax_scratch on each device, taken once per device with that device current.
+// Address of g_amax_scratch on each device, taken with that device current and kept together
+// with the id of the CUDA context it belongs to: a context destroyed and re-created (after
+// cudaDeviceReset) loads the module again, possibly at another address, so a new context id
+// means a new lookup.
 std::mutex g_sym_mu;
 uint32_t* g_sym_addr[64] = {};
+unsigned long long g_sym_ctx[64] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the current context (0 when it cannot be read: the address is then looked up every call).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 int scratch_address(int device, uint32_t** out) {
   if (device < 0 || device >= 64) return FA_LP_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_sym_mu);
-  if (!g_sym_addr[device]) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_sym_addr[device] || ctx == 0 || ctx != g_sym_ctx[device]) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_amax_scratch);
     if (e != cudaSuccess || !p) {
       cudaGetLastError();
+      g_sym_addr[device] = nullptr;
       return FA_LP_ERR_CUDA;
     }
     g_sym_addr[device] = static_cast<uint32_t*>(p);
+    g_sym_ctx[device] = ctx;
   }
   *out = g_sym_addr[device];
   return FA_LP_OK;
@@ -108,7 +143,8 @@ extern "C" int fa_lp_fp8_descale_noalloc(const void* q, int64_t q_stride_tok,
                                          int64_t v_stride_head, int64_t tokens, int heads,
                                          float* descale, void* stream_) {
   using namespace falp;
-  if (heads < 1 || heads > kMaxHeadsNoAlloc || tokens < 0 || !descale)
+  if (heads < 1 || heads > kMaxHeadsNoAlloc || tokens < 0 || !descale ||
+      reinterpret_cast<uintptr_t>(descale) % 4 != 0)
     return FA_LP_ERR_INVALID_ARG;
   if (tokens > 0 && (bad_view(q, q_stride_tok, q_stride_head) ||
                      bad_view(k, k_stride_tok, k_stride_head) ||

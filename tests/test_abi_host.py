@@ -194,3 +194,17 @@ def test_sparse_query_blocks_and_argument_checks(lib):
                                         ctypes.c_void_p(16), 128, 128, None, 0, None) == 2
     finally:
         lib.fa_lp_plan_destroy(h)
+
+
+def test_noalloc_rejects_misaligned_or_oversized_arguments_before_any_cuda_call(lib):
+    """fa_lp_fp8_descale_noalloc validates its host-visible arguments first: a descale pointer
+    that is not 4-byte aligned, or more heads than its fixed scratch holds, returns
+    FA_LP_ERR_INVALID_ARG without touching a GPU (the pointers below are never dereferenced)."""
+    fake = ctypes.c_void_p(0x10000)
+    misaligned = ctypes.c_void_p(0x10002)
+    st = lib.fa_lp_fp8_descale_noalloc(fake, 512, 128, fake, 512, 128, fake, 512, 128, 0, 4,
+                                       misaligned, None)
+    assert st == 1
+    st = lib.fa_lp_fp8_descale_noalloc(fake, 512, 128, fake, 512, 128, fake, 512, 128, 0, 1025,
+                                       fake, None)
+    assert st == 1

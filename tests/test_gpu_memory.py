@@ -55,3 +55,28 @@ def test_distinct_shapes_release_memory(fa):
         del q, k, v, out
     after = free_bytes(fa)
     assert after >= base - SLACK, (base - after) / 2**20
+
+
+def test_forward_refuses_a_workspace_another_plan_overwrote(fa):
+    """The quantized operands live in one workspace per device shared by every plan: after plan
+    B quantizes, plan A's codes are gone, and A's forward returns FA_LP_ERR_STATE instead of
+    attending over B's codes. Quantizing A again makes its forward valid again."""
+    H = 2
+    qa, ka, va = (x.cuda() for x in inputs.qkv_separate(300, H, seed=1))
+    qb, kb, vb = (x.cuda() for x in inputs.qkv_separate(500, H, seed=2))
+    a = fa.Plan([0, 300], H)
+    b = fa.Plan([0, 200, 500], H)
+    out = torch.empty((300, H, 128), dtype=torch.bfloat16, device="cuda")
+    a.quantize(qa, ka, va)
+    b.quantize(qb, kb, vb)
+    with pytest.raises(fa.FaLpError) as e:
+        a.forward(out)
+    assert e.value.status == fa.FA_LP_ERR_STATE
+    a.quantize(qa, ka, va)
+    a.forward(out)
+    want = torch.empty_like(out)
+    a.attention(qa, ka, va, out=want)
+    torch.cuda.synchronize()
+    assert torch.equal(out, want)
+    a.close()
+    b.close()

@@ -293,3 +293,66 @@ def test_fp8_lazy_reference_max_rule():
     s = (dec(cq[0, 0]) @ dec(ck[:, 0]).T) * (float(dq[0]) * float(dk[0]) * SCALE)
     assert s[256:].max() - s[:256].max() > 8 * np.log(2)
     assert np.allclose(a, b, rtol=1e-3)
+
+
+# ---------------------------------------------------------------------------------------------
+# The per-segment FP8 mode (the alternative of reading r1 that SGLang PR #40175's per-head amax
+# leaves open for packed batches): one scale per (segment, tensor, head). Pinned by reduction to
+# the per-tensor path, which is pinned above: a packed batch quantized per segment gives, for
+# every segment, exactly the codes, descales and attention rows of that segment quantized and run
+# alone.
+# ---------------------------------------------------------------------------------------------
+def test_fp8_segment_scales_equal_each_segment_alone():
+    cu = [0, 0, 17, 150, 150, 333]
+    T, H = 333, 2
+    q, k, v = inputs.qkv_separate(T, H, seed=61)
+    # segment amax 100x apart: the short middle segment is small, the last one large
+    scale_rows = torch.ones(T, 1, 1)
+    scale_rows[17:150] = 0.01
+    scale_rows[150:] = 3.0
+    q, k, v = ((x.float() * scale_rows).to(torch.bfloat16) for x in (q, k, v))
+    quant = [oracle.fp8_quantize_seg(bits(x), cu) for x in (q, k, v)]
+    cq, ck, cv = (z[0] for z in quant)
+    dq, dk, dv = (z[1] for z in quant)
+    assert dq.shape == (5, H)
+    assert np.all(dq[[0, 3]] == 1.0)          # empty segments: descale 1
+    rows = [(t, h) for t in (0, 16, 17, 80, 149, 150, 332) for h in range(H)]
+    packed, _ = oracle.attn_fp8(cq, ck, cv, dq, dk, dv, cu, rows, SCALE, n_kv=64, tau=8.0)
+    for s, (a, b) in enumerate(zip(cu[:-1], cu[1:])):
+        if a == b:
+            continue
+        alone = [oracle.fp8_quantize(bits(x[a:b].contiguous())) for x in (q, k, v)]
+        for (c_seg, d_seg), (c_alone, d_alone) in zip(quant, alone):
+            assert np.array_equal(c_seg[a:b], c_alone)
+            assert np.array_equal(d_seg[s], d_alone)
+        for r, (t, h) in enumerate(rows):
+            if a <= t < b:
+                want, _ = oracle.attn_fp8(*(z[0] for z in alone), *(z[1] for z in alone),
+                                          [0, b - a], [(t - a, h)], SCALE, n_kv=64, tau=8.0)
+                assert np.array_equal(packed[r], want[0])
+    # one segment: the per-segment mode is the per-tensor mode
+    c1, d1 = oracle.fp8_quantize_seg(bits(v), [0, T])
+    c0, d0 = oracle.fp8_quantize(bits(v))
+    assert np.array_equal(c1, c0) and np.array_equal(d1[0], d0)
+
+
+def test_fp8_segment_scales_help_a_small_segment_beside_a_large_one():
+    """Why the mode exists: a segment whose V is 3e-5 times its neighbour's falls into the E4M3
+    subnormal range under the shared per-head scale (error 0.18 against exact attention) and keeps
+    the FP8 error band (below 0.06, the pages' 0.0535-0.0539) with its own scale."""
+    cu = [0, 200, 400]
+    T, H = 400, 1
+    q, k, v = inputs.qkv_separate(T, H, seed=62)
+    sr = torch.ones(T, 1, 1)
+    sr[:200] = 3e-5
+    v = (v.float() * sr).to(torch.bfloat16)
+    rows = [(t, 0) for t in range(0, 200, 9)]
+    exact = oracle.attn_exact(bits(q), bits(k), bits(v), cu, rows, SCALE)
+    shq = [oracle.fp8_quantize(bits(x)) for x in (q, k, v)]
+    shared, _ = oracle.attn_fp8(*(z[0] for z in shq), *(z[1] for z in shq), cu, rows, SCALE,
+                                n_kv=64, tau=8.0)
+    segq = [oracle.fp8_quantize_seg(bits(x), cu) for x in (q, k, v)]
+    own, _ = oracle.attn_fp8(*(z[0] for z in segq), *(z[1] for z in segq), cu, rows, SCALE,
+                             n_kv=64, tau=8.0)
+    assert rel_rms(own, exact) < 0.06
+    assert rel_rms(shared, exact) > 0.15

@@ -244,3 +244,80 @@ def test_nvfp4_tile_width_matters_when_max_moves():
     exact = oracle.attn_exact(bits(q), bits(k), bits(v), [0, T], rows, 0.02)
     assert not np.array_equal(a, b)
     assert rel_rms(a, exact) < 0.25 and rel_rms(b, exact) < 0.25
+
+
+# ---------------------------------------------------------------------------------------------
+# Brute force of C3 on rows whose segment fits one key tile: the online softmax then sees the
+# whole row at once (its running maximum is the row maximum), so C3 must equal the global formula
+# of the FlashInfer NVFP4 op's description, written here with numpy and ml_dtypes' own E2M1 /
+# E4M3 conversions (a library independent of the oracle's converters):
+#   S'  = scale (deq(Qc) + qm) deq(Kc)^T                      (qm K^T added back, reading r12)
+#   P'  = fl32(2688 exp(S' - max S'))                          (row maximum to 448 * 6, r11)
+#   per 16 keys from the segment start: sf = E4M3(fl32(amax16 / 6)),
+#                                       code = E2M1(fl32(P' / deq(sf)))   (r9; sf 0 -> codes 0)
+#   out = sum deq(P') deq(V) / sum deq(P')                      (l sums the dequantized P)
+# The negative controls plant each plausible slip in this brute force (32-key groups, groups
+# aligned to absolute token multiples of 16, 448 where 2688 belongs, the amax instead of amax / 6,
+# the qm K^T term dropped) and check that the oracle disagrees with every one of them.
+# ---------------------------------------------------------------------------------------------
+def _bruteforce_nvfp4_row(z, cu, t, h, scale, group=16, aligned_abs=False, first_level=2688.0,
+                          sf_div=6.0, with_qm=True):
+    md = pytest.importorskip("ml_dtypes")
+    e2 = lambda c: np.asarray(c, np.uint8).view(md.float4_e2m1fn).astype(np.float64)
+    e4 = lambda c: np.asarray(c, np.uint8).view(md.float8_e4m3fn).astype(np.float64)
+    s = max(i for i in range(len(cu) - 1) if cu[i] <= t < cu[i + 1])
+    a, b = cu[s], cu[s + 1]
+    qb = z["qoff"][s] + (t - a) // 128
+    H = z["cq"].shape[1]
+    dq = e2(z["cq"][t, h]) * np.repeat(e4(z["sq"][t, h]), 16)
+    qm = z["qm"][qb, h].astype(np.float64) if with_qm else 0.0
+    dk = e2(z["ck"][a:b, h]) * np.repeat(e4(z["sk"][a:b, h]), 16, axis=-1)
+    sc = ((dq + qm) @ dk.T) * scale
+    p = (first_level * np.exp(sc - sc.max())).astype(np.float32)
+    pd = np.zeros(b - a)
+    starts = range(a - (a % group if aligned_abs else 0), b, group)
+    for g0 in starts:
+        lo, hi = max(g0, a) - a, min(g0 + group, b) - a
+        amax = p[lo:hi].max()
+        # E4M3 satfinite (the correct path never exceeds 448: amax <= 2688)
+        sf = np.minimum(np.float32(amax) / np.float32(sf_div), np.float32(448)).astype(md.float8_e4m3fn)
+        dsf = np.float32(np.asarray(sf).astype(np.float64))
+        if dsf == 0:
+            continue
+        y = np.clip(p[lo:hi] / dsf, -6.0, 6.0)  # E2M1 satfinite: nothing rounds past 6
+        pd[lo:hi] = y.astype(md.float4_e2m1fn).astype(np.float64) * np.float64(dsf)
+    G = z["sv"].shape[2]
+    gi = z["goff"][s] + (np.arange(a, b) - a) // 16
+    dv = e2(z["cv"][a:b, h]) * e4(z["sv"][h][:, gi]).T
+    return (pd @ dv) / pd.sum()
+
+
+@pytest.mark.parametrize("case", ["gaussian_ragged", "offsets_qm_matters"])
+def test_nvfp4_single_tile_bruteforce_with_library_rounding(case):
+    pytest.importorskip("ml_dtypes")
+    if case == "gaussian_ragged":
+        # segments of 37 (not a multiple of 16, starting at token 0) and 90 (starting at 37)
+        cu, H, seed = [0, 37, 127], 2, 41
+        q, k, v = inputs.qkv_separate(cu[-1], H, seed=seed)
+    else:
+        # per-channel K and Q offsets: K is centred away, and Q's block mean qm is large, so the
+        # qm K^T term carries a visible share of every score
+        cu, H, seed = [0, 0, 128, 203], 2, 43
+        q, k, v = inputs.qkv_separate(cu[-1], H, seed=seed)
+        k = (k.float() + inputs.k_channel_offset(H, seed=seed)[None]).to(torch.bfloat16)
+        q = (q.float() + inputs.k_channel_offset(H, seed=seed + 1, std=1.5)[None]).to(torch.bfloat16)
+    T = cu[-1]
+    z = oracle.nvfp4_quantize(bits(q), bits(k), bits(v), cu)
+    rows = [(t, h) for t in range(0, T, 5) for h in range(H)]
+    o64, _ = oracle.attn_nvfp4(z, cu, rows, SCALE, n_kv=128)
+    for r, (t, h) in enumerate(rows):
+        want = _bruteforce_nvfp4_row(z, cu, t, h, SCALE)
+        assert np.allclose(o64[r], want, rtol=1e-12, atol=1e-12), (t, h)
+    # every planted slip moves some row by far more than the agreement above
+    slips = [dict(group=32), dict(first_level=448.0), dict(sf_div=1.0)]
+    # the ragged layout has a segment starting at token 37; the offset case has a large qm
+    slips += [dict(aligned_abs=True)] if case == "gaussian_ragged" else [dict(with_qm=False)]
+    for slip in slips:
+        worst = max(np.abs(o64[r] - _bruteforce_nvfp4_row(z, cu, t, h, SCALE, **slip)).max()
+                    for r, (t, h) in enumerate(rows))
+        assert worst > 1e-4, slip

@@ -50,6 +50,27 @@ def test_noalloc_descale_matches_regular_path_on_two_calls(fa):
     assert torch.equal(got3, want1)
 
 
+def test_noalloc_allocates_no_device_memory(fa):
+    """The property the entry point exists for: after a first call (which loads its kernels and
+    looks up the scratch address), further calls at other sizes leave the device's free memory
+    unchanged. Every tensor the calls touch is created before the first reading."""
+    cases = [(1000, 6), (3000, 40), (1, 1), (4097, 1024)]
+    ins = [tuple(x.cuda() for x in inputs.qkv_separate(T, H, seed=30 + i))
+           for i, (T, H) in enumerate(cases)]
+    outs = [torch.empty((3, H), dtype=torch.float32, device="cuda") for _, H in cases]
+    fa.fp8_descale_noalloc(*ins[0], out=outs[0])
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for (q, k, v), o in zip(ins[1:], outs[1:]):
+        fa.fp8_descale_noalloc(q, k, v, out=o)
+        fa.fp8_descale_noalloc(q, k, v, out=o)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    for (q, k, v), o in zip(ins, outs):
+        assert torch.equal(o, descale_regular(fa, q, k, v, q.shape[0], q.shape[1]))
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(fa):
     T, H = 4, 1025
     x = torch.zeros((T, H, 128), dtype=torch.bfloat16, device="cuda")

@@ -62,6 +62,10 @@ extern "C" {
 /* ---- modes ----------------------------------------------------------------------------------- */
 #define FA_LP_MODE_FP8 0
 #define FA_LP_MODE_NVFP4 1
+/* FP8 with one scale per (segment, tensor, head): the amax of each (tensor, head) is taken over
+ * the tokens of one segment instead of the whole packed input, so that in a packed batch a long
+ * segment does not set a short one's scale. Everything else is FA_LP_MODE_FP8. */
+#define FA_LP_MODE_FP8_SEGMENT 2
 
 #define FA_LP_HEAD_DIM 128
 
@@ -84,7 +88,10 @@ FA_LP_API const char* fa_lp_status_string(int status);
  *                     A batch of B sequences of length S is the segmentation [0, S, 2S, ..., BS]
  *                     over the [B*S, H, 128] token axis (each sequence attends to itself only).
  *   softmax_scale   : > 0 and finite; <= 0 or NaN selects 1/sqrt(128).
- *   mode            : FA_LP_MODE_FP8 or FA_LP_MODE_NVFP4.
+ *   mode            : FA_LP_MODE_FP8, FA_LP_MODE_NVFP4 or FA_LP_MODE_FP8_SEGMENT (the FP8 path
+ *                     with per-(segment, tensor, head) scales; SGLang PR #40175's fused_prep.py
+ *                     takes one amax per head, and this mode is the per-segment reading of it for
+ *                     packed batches).
  *   device          : CUDA device ordinal the plan will run on (not touched here).
  *   out             : receives the plan. A plan with an identical key is shared (reference
  *                     counted); every successful create needs one fa_lp_plan_destroy.
@@ -123,7 +130,9 @@ FA_LP_API int fa_lp_workspace_bytes(const fa_lp_plan* plan, size_t* bytes);
  *                   fused [T, 3, H, 128] buffer); channel stride 1; 16-byte aligned rows.
  *   stream        : cudaStream_t (as void*).
  * FP8 mode: per (tensor, head) amax over all tokens, descale = amax/448, codes
- * E4M3_rn_sat(x * (448/amax)). NVFP4 mode: K means, Q block means, E2M1/UE4M3 packing.
+ * E4M3_rn_sat(x * (448/amax)). FP8_SEGMENT mode: the same with the amax of each (segment, tensor,
+ * head) over the segment's tokens (an empty segment gets descale 1). NVFP4 mode: K means, Q block
+ * means, E2M1/UE4M3 packing.
  * Grows the device workspace if needed (stream-ordered cudaMallocAsync/cudaFreeAsync).
  * Retains no reference to q, k, v after the kernels read them.
  * Errors: INVALID_ARG (NULL, misaligned, non-positive strides), UNSUPPORTED (device not sm_103),
@@ -176,6 +185,12 @@ FA_LP_API int fa_lp_forward_varlen(fa_lp_plan* plan, const int32_t* cu_seqlens_d
  *           log sum_j exp(s_j) up to the E4M3 rounding of P;
  *   NVFP4 : LSE = m + ln(l / 2688) + (q . km) * softmax_scale, l = sum of deq(P'), q the BF16 query
  *           and km its segment's K mean, so that the K centring is undone.
+ * Precision of the FP8 l: each of a row's two softmax threads sums its 32 quantized P of a 64-key
+ * tile in f16 pairs (a value passes through at most four f16 additions), then in FP32; P spans
+ * 2^-9 .. 2^8, so l may differ from the exact sum of the quantized P by a relative 4 * 2^-11 =
+ * 1.95e-3 at most (the LSE by as much in absolute terms; measured on ragged varlen rows: at most
+ * 2.1e-4, mean 1.1e-5). An exact FP32 sum of the same values cost 5.6 % of the forward's time at
+ * S = 30272, H = 56 and was not kept. The NVFP4 l is accumulated in FP32 by the tensor core.
  *   lse             : device pointer, FP32; the row of token t, head h is written to
  *                     lse[h * lse_stride_head + t] for tokens inside segments only (others are
  *                     left untouched). Caller-owned. NULL: behaves as fa_lp_forward_varlen.
@@ -307,7 +322,8 @@ FA_LP_API int fa_lp_attention_sparse_host(fa_lp_plan* plan, const void* q, int64
 #define FA_LP_Q_CODES 0     /* FP8: u8 [H][Tpad][128]  NVFP4: u8 [H][Tpad][64] (2 codes/byte)   */
 #define FA_LP_K_CODES 1     /* same layout as Q                                                  */
 #define FA_LP_V_CODES 2     /* FP8: u8 [H][128][Tpad] (V^T)  NVFP4: u8 [H][128][Tpad/2]          */
-#define FA_LP_DESCALE 3     /* FP8: f32 [3][H] = amax/448 of q, k, v                             */
+#define FA_LP_DESCALE 3     /* FP8: f32 [1][3][H] = amax/448 of q, k, v; FP8_SEGMENT: f32        */
+                            /* [3][num_segments][H]                                              */
 #define FA_LP_Q_SCALES 4    /* NVFP4: u8 [H][Tpad][8] UE4M3, one per 16 channels                 */
 #define FA_LP_K_SCALES 5    /* NVFP4: u8 [H][Tpad][8]                                            */
 #define FA_LP_V_SCALES 6    /* NVFP4: u8 [H][Tpad/128][128][8], one per 16 keys per channel      */

@@ -86,7 +86,8 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 struct AttnArgs {
   const SegInfo* segs;
   const WorkItem* work;
-  const float* descale;  // [3][H]
+  const float* descale;  // [3][R][H]: R = 1, or one row per segment (per-segment scales)
+  int scale_rows;        // R
   __nv_bfloat16* out;
   int64_t ost, osh;
   float* lse;        // optional: FP32 row log-sum-exp at lse[h * lse_sh + token]
@@ -263,8 +264,10 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
                                                      uint32_t tmem, int t, int wq, int lane) {
   const int n_sub = (sg.len + kSub - 1) / kSub;
   const int h = wi.head;
-  const float c = a.descale[h] * a.descale[a.H + h] * a.scale_log2;
-  const float dv = a.descale[2 * a.H + h];
+  const int64_t d0 = (a.scale_rows > 1 ? wi.seg : 0) * int64_t(a.H) + h;  // this tile's scales
+  const int64_t dstride = int64_t(a.scale_rows) * a.H;
+  const float c = a.descale[d0] * a.descale[dstride + d0] * a.scale_log2;
+  const float dv = a.descale[2 * dstride + d0];
   // warp wq (0..7) of the tile: lane quarter wq & 3, half wq >> 2; the row is shared by threads
   // lane and lane ^ 16, which hold keys [0, 32) and [32, 64) of every sub-tile
   const int rbase = 32 * (wq & 3) + 16 * (wq >> 2);
@@ -461,6 +464,7 @@ int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t os
   a.segs = p.d_segs;
   a.work = p.d_work;
   a.descale = reinterpret_cast<const float*>(ws + p.ws.descale);
+  a.scale_rows = fp8_scale_rows(p);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.ost = ost;
   a.osh = osh;

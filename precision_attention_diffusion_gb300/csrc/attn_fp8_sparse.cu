@@ -80,7 +80,8 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct SpArgs {
   const SegInfo* segs;
-  const float* descale;    // [3][H]
+  const float* descale;    // [3][R][H]: R = 1, or one row per segment (per-segment scales)
+  int scale_rows;          // R
   const uint32_t* uni;     // merged lists
   const int64_t* tbase;    // [H][nblocks] first entry of each tile's merged list
   const int32_t* tcnt;     // [H][nblocks] entries
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(256) sparse_order_kernel(const SparseGroup* __
 // Attention roles. A query tile of a CTA: its segment, head and tile index in the segment.
 struct TileRef {
   SegInfo sg;
-  int head, qt;
+  int seg, head, qt;
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -333,8 +334,10 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const SpArgs& a, c
                                                      const uint32_t* ent, int n) {
   const SegInfo& sg = tr.sg;
   const int h = tr.head;
-  const float c = a.descale[h] * a.descale[a.H + h] * a.scale_log2;
-  const float dv = a.descale[2 * a.H + h];
+  const int64_t d0 = (a.scale_rows > 1 ? tr.seg : 0) * int64_t(a.H) + h;  // this tile's scales
+  const int64_t dstride = int64_t(a.scale_rows) * a.H;
+  const float c = a.descale[d0] * a.descale[dstride + d0] * a.scale_log2;
+  const float dv = a.descale[2 * dstride + d0];
   const int rbase = 32 * (wq & 3) + 16 * (wq >> 2);  // rows of this warp: rbase + [0, 16)
   const int kh = lane >> 4;                           // keys [32 kh, 32 kh + 32) of a block
   const uint32_t half_bit = 1u << (30 + ((wq & 3) >> 1));
@@ -486,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BlockInfo bi = a.blocks[id - hh * a.nblocks];
   TileRef tr;
   tr.sg = a.segs[bi.seg];
+  tr.seg = bi.seg;
   tr.head = hh;
   tr.qt = bi.blk;
   const uint32_t* ent = a.uni + a.tbase[id];
@@ -579,6 +583,7 @@ int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* off, cons
   a.ctas = p.d_sp_ctas;
   a.blocks = p.d_blocks;
   a.descale = reinterpret_cast<const float*>(ws + p.ws.descale);
+  a.scale_rows = fp8_scale_rows(p);
   a.uni = uni;
   a.tbase = tbase;
   a.tcnt = tcnt;

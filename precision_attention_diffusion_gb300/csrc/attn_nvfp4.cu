@@ -23,31 +23,35 @@
 //                (scale 1.0) after its 128 channels, so O has 144 columns and column 128 is l
 //   out        = BF16(O / l) for rows inside the segment.
 //
-// Roles (480 threads):
-//   warp 8      TMA: Q codes (64-byte rows, 64-byte swizzle) and, by plain bulk copies, the Q
-//               scale records once; then per 128-key tile K codes + K scale record + the query
-//               tiles' 128-entry rows of the qm K^T table, and V^T codes + V scale record, into
-//               a 4-stage ring;
-//   warps 9/10  MMA issue for query tile 0/1 (tensor memory allocated by warp 9):
+// Roles (640 threads, 96 registers each):
+//   warps 0-7 / 8-15  softmax of query tile 0 / 1, two threads per row through the 16x32bx2
+//               tensor-memory shapes: warp w of a tile covers lanes 32 (w & 3) + 16 (w >> 2) +
+//               [0, 16); threads t and t ^ 16 hold keys [0, 32) and [32, 64) of the row's
+//               sub-tile (two 16-key scale groups each) and share the row maximum through one
+//               shuffle; they also write the row's Q scale factors into tensor memory once;
+//   warp 16     TMA: Q codes and (bulk copies) Q scale records once; per 128-key tile K codes, the
+//               K scale record, the query tiles' 128-entry rows of the qm K^T table, V^T codes and
+//               the V scale record, into a 4-stage ring;
+//   warps 17/18 MMA issue for query tile 0/1 (two independent in-order streams; warp 17 allocates
+//               tensor memory), each with the tcgen05.cp copies of the K and V scale factors its
+//               MMAs read, from shared into its tile's tensor memory (ordered before its MMAs):
 //                 S_t(u)  = deq(Qc_t) deq(Kc(u))^T   2 MMAs M=128 N=64  K=64, A, B in smem
 //                 S_t(u) += 1 Tq_t(u)^T              1 kind::f16 MMA  M=128 N=64 K=16 (A =
 //                                                    rows [1, 1, 1, 0...], B = the table
 //                                                    entries as three BF16 pieces)
 //                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=144 K=64, A = P in TMEM
 //                                                    (N 128-143: the 1.0 rows, giving l)
-//   warps 11-14 per sub-tile: K and V scale factors into tensor memory (the MMA reads the B-side
-//               scales of row n from column n / 32 of every lane quarter, so each of the four
-//               warps writes its own quarter; the 1.0 rows' scale column is written once),
-//               and the BF16 pieces of the table entries;
-//   warps 0-7   softmax of tile 0 (warps 0-3) and 1 (warps 4-7), one thread per query row (row ==
-//               tensor-memory lane); S and the maxima of its 16-key groups come from
-//               tcgen05.ld.red; P codes and P scales go to tensor memory (A-side scales: row r in
-//               lane r, column r / 32), O is rescaled in tensor memory when a row's maximum
-//               moves, and the same threads run the epilogue.
-// Tensor memory (512 columns): per query tile t a 144-column O, one P slot (8 columns of codes, 4
-// of scales: PV(u-1) has read it long before P(u) is ready), a 64-column S; Q, K (two buffers)
-// and V (two buffers) scale blocks in the gaps. Every barrier wait is bounded; on expiry the kernel records an error, drains its
-// in-flight copies and MMAs, frees its tensor memory and returns.
+//               S_t(u+1) is issued as soon as the softmax has read S_t(u), so the scores of the
+//               next sub-tile are computed while the softmax works on the current ones;
+//   warp 19     per sub-tile, from the stage's records: the K and V scale factors re-laid out as
+//               32-row x 16-byte blocks for tcgen05.cp, and each query tile's fold tile (every
+//               key's qm K^T table entry as three BF16 pieces).
+// Tensor memory (512 columns), per query tile t at 256 t: O [0, 144) (column 128: l), P codes
+// [144, 152), P scales [152, 156) (A side: row r in lane r, column r / 32; [156, 160) takes the
+// second thread's copy of the word), Q scales [160, 168), K scales [168, 184) (two buffers of two
+// K steps), V scales [184, 189) (column 188: scale 1.0 of the 1.0 rows), S [192, 256).
+// Every barrier wait is bounded; on expiry the kernel records an error, drains its in-flight
+// copies and MMAs, frees its tensor memory and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -59,11 +63,12 @@ namespace falp {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 480;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;      // warps 9 and 10
-constexpr int kCorrWarp = 11;    // warps 11-14
+constexpr int kThreads = 640;
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;     // warps 17 and 18 issue the MMAs of query tiles 0 and 1
+constexpr int kAuxWarp = 19;
 constexpr int kSub = 64;         // keys per sub-tile
+constexpr int kAuxBufs = 4;      // re-laid-out scale blocks and fold tiles (two stages)
 constexpr uint32_t kCodeTile = 128 * 64;  // 128 rows of 128 E2M1 codes
 constexpr uint32_t kSfTile = 128 * 8;     // 128 rows of 8 UE4M3 scales
 constexpr uint32_t kIdescS = idesc_mxf4nvf4(128, kSub);
@@ -74,43 +79,45 @@ constexpr uint32_t kIdescFold = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(
                                 ((128u >> 4) << 24);
 constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
 constexpr float kLog2_6 = 2.5849625007211562f;
+constexpr uint32_t kHintNs = 20000;  // first probe of a steady-state wait: park up to 20 us
 
-// tensor-memory columns (512): per query tile t at 256 t -- O 144 (channels, then 16 columns that
-// accumulate the row sum l through the 1.0 rows of V^T), the P codes (8) and P scales (4) of one
-// sub-tile, S 64 -- and, in the gaps, the Q scales, the K and V scale blocks (double buffered; a V
-// block has a fifth column for the 1.0 rows). Starts: O and S 32-aligned, P codes 16-aligned,
-// scale blocks 8-aligned (4 for the B side).
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u * uint32_t(t); }
 __device__ __forceinline__ uint32_t col_p(int t) { return 256u * uint32_t(t) + 144u; }
 __device__ __forceinline__ uint32_t col_psf(int t) { return 256u * uint32_t(t) + 152u; }
+__device__ __forceinline__ uint32_t col_qsf(int t) { return 256u * uint32_t(t) + 160u; }
+__device__ __forceinline__ uint32_t col_ksf(int t, int b) {
+  return 256u * uint32_t(t) + 168u + 8u * uint32_t(b);
+}
+__device__ __forceinline__ uint32_t col_vsf(int t) { return 256u * uint32_t(t) + 184u; }
 __device__ __forceinline__ uint32_t col_s(int t) { return 256u * uint32_t(t) + 192u; }
-__device__ __forceinline__ uint32_t col_vsf(int b) { return b ? 416u : 160u; }
-__device__ __forceinline__ uint32_t col_qsf(int t) { return 168u + 8u * uint32_t(t); }
-__device__ __forceinline__ uint32_t col_ksf(int b) { return b ? 424u : 184u; }
 
 struct Smem {
   uint8_t q[2][kCodeTile];
   uint8_t k[kStages][kCodeTile];
   uint8_t v[kStages][kVTile];      // V^T: 128 channel rows of 128 keys, 16 rows of 1.0
-  // qm K^T fold into S (one kind::f16 MMA per sub-tile): A = 128 identical rows [1, 1, 1, 0...]
-  // (one core matrix repeated, then a zero core matrix), B = per key the table entry as three
-  // BF16 pieces (64 keys x 16 bytes, then 1 KB of zeros for K 8..15)
+  // qm K^T fold into S (one kind::f16 MMA per sub-tile and query tile): A = 128 identical rows
+  // [1, 1, 1, 0...] (one core matrix repeated, then a zero core matrix), B = per key the table
+  // entry as three BF16 pieces (64 keys x 16 bytes, then 1 KB of zeros for K 8..15)
+  uint8_t fb[kAuxBufs][2][2048];   // [u mod 4][t]
+  uint8_t ksf_cp[kAuxBufs][2][512];  // [u mod 4][K step]: row i = scales of keys i, 32 + i, 0, 0
+  uint8_t vsf_cp[kAuxBufs][512];     // [u mod 4]: row i = scales of channels i, 32+i, 64+i, 96+i
+  uint8_t ones_cp[512];              // row i = scale 1.0 (x4) for i < 16, else 0
   uint8_t fa[256];
-  uint8_t fb[2][2][2048];          // [u & 1][t]
   uint8_t qsf[2][kSfTile];
   uint8_t ksf[kStages][kSfTile];   // [key][8]
   uint8_t vsf[kStages][kSfTile];   // [channel][8]
   float cq[kStages][2][kTile];     // [stage][t][key]: the qm K^T table row of query tile t
   uint64_t bar_q;
-  uint64_t bar_k[kStages];
-  uint64_t bar_v[kStages];
-  uint64_t bar_free[kStages];      // MMA commits + scale-factor warps
+  uint64_t bar_qsf[2];             // [t]: Q scale factors in tensor memory (256 arrivals)
+  uint64_t bar_ld[kStages];        // K, V codes, their scale records and the table rows landed
+  uint64_t bar_free[kStages];      // MMA commits + the auxiliary warp
+  uint64_t bar_aux[kAuxBufs];      // [u mod 4]: scale blocks and fold tiles of u written (32);
+                                   // implies the stage of u has landed
+  uint64_t bar_auxfree[kAuxBufs];  // [u mod 4]: the MMAs and copies of u that read them done
   uint64_t bar_s[2];               // [t]: S_t(u) written (MMA commit)
-  uint64_t bar_sr[2];              // [t]: S_t(u) read by the softmax (128 arrivals)
-  uint64_t bar_p[2][2];            // [t][u & 1]: P_t(u) written and O rescaled (128 arrivals)
+  uint64_t bar_sr[2];              // [t]: S_t(u) read by the softmax (256 arrivals)
+  uint64_t bar_p[2][2];            // [t][u & 1]: P_t(u) written and O rescaled (256 arrivals)
   uint64_t bar_o[2][2];            // [t][u & 1]: PV_t(u) done (MMA commit)
-  uint64_t bar_sf[2];              // [u & 1]: K and V scale factors of u in TMEM (128)
-  uint64_t bar_sffree[2];          // [u & 1]: MMAs of u done, scale buffers free (nq commits)
   uint64_t bar_drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -140,18 +147,73 @@ struct Nvfp4Args {
 enum Role : int { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleEpilogue = 4,
                   kRoleScales = 5 };
 
+// Warp-uniform bounded wait.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, Smem& S,
                                          const Nvfp4Args& a, int role) {
   return __all_sync(0xffffffffu, wait_phase(smem_u32(bar), parity, &S.abort_flag, a.w, role));
 }
 
+// Warp-uniform wait of the steady state: one probe that parks the warp in hardware until the phase
+// completes (or kHintNs passes), so that a waiting warp takes no issue slots from the warps it
+// shares a scheduler with; then the bounded wait.
+__device__ __forceinline__ bool wait_hinted(uint64_t* bar, uint32_t parity, Smem& S,
+                                            const Nvfp4Args& a, int role) {
+  if (__all_sync(0xffffffffu, mbar_try_wait_sleep(smem_u32(bar), parity, kHintNs))) return true;
+  return wait_all(bar, parity, S, a, role);
+}
+
+// One elect.sync for the whole S group of a query tile and sub-tile (a tcgen05 instruction group
+// behind a single elect costs the issuing warp far less than one elect per instruction): the two K
+// scale blocks into tensor memory, the two block-scaled K = 64 MMAs (the first overwriting S), the
+// BF16 fold MMA adding the qm K^T term, and the commit of all of them to `bar`.
+__device__ __forceinline__ void s_group_elect(uint32_t d, uint64_t qa, uint64_t kb, uint32_t sfa,
+                                              uint32_t ks, uint64_t ksf0, uint64_t ksf1,
+                                              uint64_t fa, uint64_t fb, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 qa1, kb1;\n\t.reg .b32 sfa1, ks1;\n\t"
+      "setp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "add.s64 qa1, %1, 2;\n\tadd.s64 kb1, %2, 2;\n\t"
+      "add.s32 sfa1, %3, 4;\n\tadd.s32 ks1, %4, 4;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [ks1], %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %9, "
+      "[%3], [%4], p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], qa1, kb1, %9, "
+      "[sfa1], [ks1], p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %10, p1;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}"
+      ::"r"(d), "l"(qa), "l"(kb), "r"(sfa), "r"(ks), "l"(ksf0), "l"(ksf1), "l"(fa), "l"(fb),
+      "r"(kIdescS), "r"(kIdescFold), "r"(bar)
+      : "memory");
+}
+
+// One elect.sync for the PV group: the V scale block into tensor memory, the block-scaled PV MMA
+// (A = P from tensor memory; accumulating unless `first`), and the commits to the PV barrier and the
+// auxiliary-buffer barrier, plus the stage barrier when `release`.
+__device__ __forceinline__ void pv_group_elect(uint32_t d, uint32_t pa, uint64_t vb, uint32_t psf,
+                                               uint32_t vs, uint64_t vsf, uint32_t accumulate,
+                                               uint32_t bar_o, uint32_t bar_aux,
+                                               uint32_t release, uint32_t bar_free) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, r;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.ne.b32 r, %9, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %11, "
+      "[%3], [%4], p;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+      "and.pred r, r, e;\n\t"
+      "@r tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}"
+      ::"r"(d), "r"(pa), "l"(vb), "r"(psf), "r"(vs), "l"(vsf), "r"(accumulate), "r"(bar_o),
+      "r"(bar_aux), "r"(release), "r"(bar_free), "r"(kIdescPV)
+      : "memory");
+}
+
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   const uint32_t h2 = cvt_e4m3x2_to_f16x2(uint16_t(code & 0xFF));
   return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
-}
-
-__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -175,37 +237,33 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
   int issued = 0;
   for (int j = 0; j < n_kv; ++j) {
     const int st = j % kStages;
-    if (j >= kStages && !wait_all(&S.bar_free[st], ((j / kStages) - 1) & 1, S, a, kRoleProducer))
+    if (j >= kStages &&
+        !wait_hinted(&S.bar_free[st], ((j / kStages) - 1) & 1, S, a, kRoleProducer))
       break;
     const int row = sg.row0 + j * kTile;
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]),
-                                kCodeTile + kSfTile + uint32_t(wi.nq) * kTile * 4);
-    tma_load_3d_elect(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_k[st]), 0, row, wi.head);
-    bulk_load_elect(smem_u32(S.ksf[st]), a.k_sf + (h * Tp + row) * 8, kSfTile,
-                    smem_u32(&S.bar_k[st]));
+    const uint32_t bar = smem_u32(&S.bar_ld[st]);
+    mbar_arrive_expect_tx_elect(bar, 2 * (kCodeTile + kSfTile) + uint32_t(wi.nq) * kTile * 4);
+    tma_load_3d_elect(smem_u32(S.k[st]), tm_k, bar, 0, row, wi.head);
+    bulk_load_elect(smem_u32(S.ksf[st]), a.k_sf + (h * Tp + row) * 8, kSfTile, bar);
     for (int t = 0; t < wi.nq; ++t)
-      bulk_load_elect(smem_u32(S.cq[st][t]), tab + t * lp + int64_t(j) * kTile, kTile * 4,
-                      smem_u32(&S.bar_k[st]));
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[st]), kCodeTile + kSfTile);
-    tma_load_3d_elect(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_v[st]), row / 2, 0, wi.head);
+      bulk_load_elect(smem_u32(S.cq[st][t]), tab + t * lp + int64_t(j) * kTile, kTile * 4, bar);
+    tma_load_3d_elect(smem_u32(S.v[st]), tm_v, bar, row / 2, 0, wi.head);
     bulk_load_elect(smem_u32(S.vsf[st]), a.v_sf + (h * (Tp / kTile) + row / kTile) * kSfTile,
-                    kSfTile, smem_u32(&S.bar_v[st]));
+                    kSfTile, bar);
     issued = j + 1;
   }
   // No copy may still be landing in shared memory when the CTA exits.
   drain_phase(smem_u32(&S.bar_q), 0);
-  for (int j = max(0, issued - kStages); j < issued; ++j) {
-    const int st = j % kStages;
-    drain_phase(smem_u32(&S.bar_k[st]), (j / kStages) & 1);
-    drain_phase(smem_u32(&S.bar_v[st]), (j / kStages) & 1);
-  }
+  for (int j = max(0, issued - kStages); j < issued; ++j)
+    drain_phase(smem_u32(&S.bar_ld[j % kStages]), (j / kStages) & 1);
 }
 
 // ---------------------------------------------------------------------------------------------
 // MMA issue for query tile t (whole warp, converged; one elected lane issues). Order per step u:
-// S_t(u) as soon as the softmax has read S_t(u-1) and the scale factors of u are in tensor
-// memory, then PV_t(u-1) once P_t(u-1) is written: the tensor pipe computes the next scores while
-// the softmax works on the current ones.
+// S_t(u) as soon as the softmax has read S_t(u-1) (and the K tile and the auxiliary blocks of u are
+// in shared memory), then PV_t(u-1) once P_t(u-1) is written: the tensor pipe computes the next
+// scores while the softmax works on the current ones. The scale factors reach tensor memory by
+// tcgen05.cp from this thread, ordered before its later MMAs.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
                                            const SegInfo& sg, uint32_t tmem, int t) {
@@ -216,223 +274,237 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
   const uint64_t dk = sdesc_kmajor_sw64(smem_u32(S.k[0]));
   const uint64_t dv = sdesc_kmajor_sw64(smem_u32(S.v[0]));
   const uint64_t dfa = sdesc_kmajor_noswz(smem_u32(S.fa), 128, 0);
+  // 32 rows x 16 bytes, row i at byte 16 i (core matrices of 8 rows 128 bytes apart)
+  const uint64_t dksf = sdesc_kmajor_noswz(smem_u32(S.ksf_cp[0][0]), 128, 128);
+  const uint64_t dvsf = sdesc_kmajor_noswz(smem_u32(S.vsf_cp[0]), 128, 128);
+  const uint64_t dones = sdesc_kmajor_noswz(smem_u32(S.ones_cp), 128, 128);
+  const uint32_t d_s = tmem + col_s(t);
   auto issue_s = [&](int u) {
-    const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
-    const uint64_t kb = dk + (((j % kStages) * kCodeTile + h * (kSub * 64)) >> 4);
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-      mma_mxf4_ss_elect(tmem + col_s(t), dq + 2 * kk, kb + 2 * kk, kIdescS,
-                        tmem + col_qsf(t) + 4 * kk, tmem + col_ksf(int(h)) + 4 * kk, kk > 0);
-    // S += 1 . (hi + mid + lo) of the table: the qm K^T term, exact to FP32 accumulation
-    mma_f16_ss_elect(tmem + col_s(t), dfa, sdesc_kmajor_noswz(smem_u32(S.fb[h][t]), 1024, 128),
-                     kIdescFold, 1u);
-    mma_commit_elect(smem_u32(&S.bar_s[t]));
+    const int x = u % kAuxBufs, h = u & 1, st = (u >> 1) % kStages;
+    // K scales of u into buffer u & 1, last read by S_t(u-2): complete, since the softmax has
+    // read S_t(u-1); S += 1 . (hi + mid + lo) of the table: the qm K^T term, exact to FP32
+    // accumulation
+    const uint64_t kb = dk + (((st * kCodeTile) + h * (kSub * 64)) >> 4);
+    s_group_elect(d_s, dq, kb, tmem + col_qsf(t), tmem + col_ksf(t, u & 1),
+                  dksf + ((uint32_t(x) * 1024u) >> 4), dksf + ((uint32_t(x) * 1024u + 512u) >> 4),
+                  dfa, sdesc_kmajor_noswz(smem_u32(S.fb[x][t]), 1024, 128),
+                  smem_u32(&S.bar_s[t]));
   };
   // keys [64h, 64h + 64) of a 128-key tile are bytes [32h, 32h + 32) of each V^T row
   auto issue_pv = [&](int u) {
-    const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
-    const uint64_t vb = dv + (((j % kStages) * kVTile) >> 4) + 2 * h;
-    mma_mxf4_ts_elect(tmem + col_o(t), tmem + col_p(t), vb, kIdescPV,
-                      tmem + col_psf(t), tmem + col_vsf(int(h)), u > 0 ? 1u : 0u);
-    mma_commit_elect(smem_u32(&S.bar_o[t][h]));
-    mma_commit_elect(smem_u32(&S.bar_sffree[h]));
-    if (h == 1 || u + 1 == n_sub) mma_commit_elect(smem_u32(&S.bar_free[j % kStages]));
+    const int x = u % kAuxBufs, h = u & 1, st = (u >> 1) % kStages;
+    // V scales of u (the columns were last read by PV_t(u-1), complete before the softmax wrote
+    // P_t(u)); the 1.0 rows' scale column was written once
+    const uint64_t vb = dv + ((uint32_t(st) * kVTile) >> 4) + 2 * h;
+    pv_group_elect(tmem + col_o(t), tmem + col_p(t), vb, tmem + col_psf(t), tmem + col_vsf(t),
+                   dvsf + ((uint32_t(x) * 512u) >> 4), u > 0 ? 1u : 0u,
+                   smem_u32(&S.bar_o[t][u & 1]), smem_u32(&S.bar_auxfree[x]),
+                   (h == 1 || u + 1 == n_sub) ? 1u : 0u, smem_u32(&S.bar_free[st]));
   };
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    return wait_hinted(bar, parity, S, a, kRoleMma);
+  };
+  // scale 1.0 of the 1.0 rows: columns [188, 192) of the tile are written by nothing else
+  tmem_cp_32x128b_warpx4_elect(tmem + col_vsf(t) + 4, dones);
   do {
-    if (!wait_all(&S.bar_q, 0, S, a, kRoleMma)) break;
+    if (!wait(&S.bar_q, 0)) break;
+    if (!wait(&S.bar_qsf[t], 0)) break;
     bool ok = true;
     for (int u = 0; u <= n_sub && ok; ++u) {
       if (u < n_sub) {
-        const int j = u >> 1;
-        if (u > 0 && !(ok = wait_all(&S.bar_sr[t], (u - 1) & 1, S, a, kRoleMma))) break;
-        if ((u & 1) == 0 &&
-            !(ok = wait_all(&S.bar_k[j % kStages], (j / kStages) & 1, S, a, kRoleMma)))
-          break;
-        if (!(ok = wait_all(&S.bar_sf[u & 1], (u >> 1) & 1, S, a, kRoleMma))) break;
+        // the auxiliary warp's blocks of u (written after the stage of u landed)
+        if (u > 0 && !(ok = wait(&S.bar_sr[t], (u - 1) & 1))) break;
+        if (!(ok = wait(&S.bar_aux[u % kAuxBufs], (u / kAuxBufs) & 1))) break;
         tc_fence_after();
         issue_s(u);
       }
       if (u > 0) {
-        const int w = u - 1, j = w >> 1;
-        if ((w & 1) == 0 &&
-            !(ok = wait_all(&S.bar_v[j % kStages], (j / kStages) & 1, S, a, kRoleMma)))
-          break;
-        if (!(ok = wait_all(&S.bar_p[t][w & 1], (w >> 1) & 1, S, a, kRoleMma))) break;
+        const int w = u - 1;
+        if (!(ok = wait(&S.bar_p[t][w & 1], (w >> 1) & 1))) break;
         tc_fence_after();
         issue_pv(w);
       }
     }
   } while (false);
-  // Every MMA issued so far must finish before the tensor memory is released.
+  // Every MMA and copy issued so far must finish before the tensor memory is released.
   mma_commit_elect(smem_u32(&S.bar_drain[t]));
   drain_phase(smem_u32(&S.bar_drain[t]), 0);
 }
 
 // ---------------------------------------------------------------------------------------------
-// Scale-factor warps: the Q scale factors once, then per sub-tile the K and V scale factors into
-// tensor memory. Each warp writes its own lane quarter (the MMA reads A-side scales of row r from
-// lane r and B-side scales from every lane quarter).
+// Auxiliary warp: once per 128-key stage, for both of its sub-tiles, the two K scale blocks and the
+// V scale block in the row layout tcgen05.cp takes, and the fold tile of every query tile.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void scale_factor_warps(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
-                                                   const SegInfo& sg, uint32_t tmem, int cw,
-                                                   int lane) {
+__device__ __forceinline__ void aux_warp(Smem& S, const Nvfp4Args& a, const WorkItem& wi,
+                                         const SegInfo& sg, int lane) {
   const int n_sub = (sg.len + kSub - 1) / kSub;
-  const int quarter = (kCorrWarp + cw) & 3;  // tensor-memory lane quarter this warp may access
-  const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-  if (!wait_all(&S.bar_q, 0, S, a, kRoleScales)) return;
-  // Q scale factors (A side: row r in lane r, column r / 32; K step kk at +4kk).
-  {
-    const int r = quarter * 32 + lane;
-    for (int t = 0; t < wi.nq; ++t) {
-      const uint2 w = *reinterpret_cast<const uint2*>(S.qsf[t] + r * 8);
-      tmem_st1(tmem + col_qsf(t) + uint32_t(quarter) + lane_off, w.x);
-      tmem_st1(tmem + col_qsf(t) + 4u + uint32_t(quarter) + lane_off, w.y);
-    }
-  }
-  // rows 128-143 of V^T (the 1.0 rows): scale 1.0 in column 4 of both V scale blocks
-  tmem_st1(tmem + col_vsf(0) + 4u + lane_off, lane < 16 ? 0x38383838u : 0u);
-  tmem_st1(tmem + col_vsf(1) + 4u + lane_off, lane < 16 ? 0x38383838u : 0u);
-  for (int u = 0; u < n_sub; ++u) {
-    const int j = u >> 1, h = u & 1, st = j % kStages, b = u & 1;
-    if (h == 0) {
-      if (!wait_all(&S.bar_k[st], (j / kStages) & 1, S, a, kRoleScales)) break;
-      if (!wait_all(&S.bar_v[st], (j / kStages) & 1, S, a, kRoleScales)) break;
-    }
-    if (u >= 2 && !wait_all(&S.bar_sffree[b], ((u - 2) >> 1) & 1, S, a, kRoleScales)) break;
-    // B-side scale factors, every lane quarter: K rows (keys) 32c + lane in column c of K step kk;
-    // V rows (channels) 32c + lane in column c, word h of the channel's 8-byte record.
-    const uint2 k0 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + lane) * 8);
-    const uint2 k1 = *reinterpret_cast<const uint2*>(S.ksf[st] + (64 * h + 32 + lane) * 8);
-    const uint32_t kw[8] = {k0.x, k1.x, 0u, 0u, k0.y, k1.y, 0u, 0u};
-    tmem_st8(tmem + col_ksf(b) + lane_off, kw);
-    const uint32_t* vs = reinterpret_cast<const uint32_t*>(S.vsf[st]);
-    tmem_st4(tmem + col_vsf(b) + lane_off, vs[lane * 2 + h], vs[(32 + lane) * 2 + h],
-             vs[(64 + lane) * 2 + h], vs[(96 + lane) * 2 + h]);
-    // fold B tile of query tile ft: key row `key` = the table entry as three BF16 pieces
-    {
-      const int idx = cw * 32 + lane, ft = idx >> 6, key = idx & 63;
-      if (ft < wi.nq) {
-        float x = S.cq[st][ft][kSub * h + key];
-        uint32_t pc[3];
+  const int n_kv = sg.nblk;
+  const bool two = wi.nq == 2;
+  for (int j = 0; j < n_kv; ++j) {
+    const int st = j % kStages, u0 = 2 * j;
+    if (!wait_hinted(&S.bar_ld[st], (j / kStages) & 1, S, a, kRoleScales)) break;
+    // the blocks of u0 - 4 and u0 - 3 (same buffers) must have been consumed by every query
+    // tile: the commit after PV(u0 - 3) covers every earlier MMA and copy of the issuing thread
+    if (u0 >= kAuxBufs && !wait_hinted(&S.bar_auxfree[(u0 - 3) % kAuxBufs],
+                                       ((u0 - 3) / kAuxBufs) & 1, S, a, kRoleScales))
+      break;
+    const int nh = min(2, n_sub - u0);  // sub-tiles of this stage inside the segment
+    // K scale records of the stage's 128 keys, V scale words of its 128 channels, table entries
+    uint2 kw[4];
 #pragma unroll
-        for (int p = 0; p < 3; ++p) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(x);
-          pc[p] = uint32_t(__bfloat16_as_ushort(v));
-          x = x - __bfloat162float(v);  // exact: x and its BF16 rounding share the top bits
+    for (int i = 0; i < 4; ++i)
+      kw[i] = *reinterpret_cast<const uint2*>(S.ksf[st] + (32 * i + lane) * 8);
+    uint2 vw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      vw[i] = *reinterpret_cast<const uint2*>(S.vsf[st] + (32 * i + lane) * 8);
+    float cv[2][4];
+#pragma unroll
+    for (int ft = 0; ft < 2; ++ft)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cv[ft][i] = (ft == 0 || two) ? S.cq[st][ft][32 * i + lane] : 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h >= nh) break;
+      const int x = (u0 + h) % kAuxBufs;
+      // K scale blocks, one per K step kk: row i = (key i, key 32 + i) of the sub-tile, then two
+      // zero words (an N = 64 MMA reads the first two columns)
+      *reinterpret_cast<uint4*>(S.ksf_cp[x][0] + 16 * lane) =
+          make_uint4(kw[2 * h].x, kw[2 * h + 1].x, 0u, 0u);
+      *reinterpret_cast<uint4*>(S.ksf_cp[x][1] + 16 * lane) =
+          make_uint4(kw[2 * h].y, kw[2 * h + 1].y, 0u, 0u);
+      // V scale block: row i = channels i, 32 + i, 64 + i, 96 + i, the word of keys [64h, 64h+64)
+      *reinterpret_cast<uint4*>(S.vsf_cp[x] + 16 * lane) =
+          h ? make_uint4(vw[0].y, vw[1].y, vw[2].y, vw[3].y)
+            : make_uint4(vw[0].x, vw[1].x, vw[2].x, vw[3].x);
+      // fold B tiles: key row `key` = the table entry of query tile ft as three BF16 pieces
+#pragma unroll
+      for (int ft = 0; ft < 2; ++ft) {
+        if (ft == 1 && !two) break;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int key = lane + 32 * r;
+          float v = cv[ft][2 * h + r];
+          uint32_t pc[3];
+#pragma unroll
+          for (int p = 0; p < 3; ++p) {
+            const __nv_bfloat16 bv = __float2bfloat16_rn(v);
+            pc[p] = uint32_t(__bfloat16_as_ushort(bv));
+            v = v - __bfloat162float(bv);  // exact: v and its BF16 rounding share the top bits
+          }
+          *reinterpret_cast<uint4*>(S.fb[x][ft] + (key >> 3) * 128 + (key & 7) * 16) =
+              make_uint4(pc[0] | (pc[1] << 16), pc[2], 0u, 0u);
         }
-        *reinterpret_cast<uint4*>(S.fb[b][ft] + (key >> 3) * 128 + (key & 7) * 16) =
-            make_uint4(pc[0] | (pc[1] << 16), pc[2], 0u, 0u);
       }
-      fence_proxy_async_smem();  // the fold MMA reads the tile through the async proxy
+      fence_proxy_async_smem();  // the copies and the fold MMAs read these through the async proxy
+      mbar_arrive(smem_u32(&S.bar_aux[x]));
     }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(smem_u32(&S.bar_sf[b]));  // the MMAs of u may start
-    if (h == 1 || u + 1 == n_sub) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.bar_free[st]));
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&S.bar_free[st]));
   }
-  tmem_wait_st();
-}
-
-// Maximum of 16 values (3-input max tree).
-__device__ __forceinline__ float max16(const float (&p)[16]) {
-  const float a = max3f(p[0], p[1], p[2]), b = max3f(p[3], p[4], p[5]);
-  const float c = max3f(p[6], p[7], p[8]), d = max3f(p[9], p[10], p[11]);
-  const float e = max3f(p[12], p[13], p[14]);
-  return fmaxf(max3f(a, b, c), max3f(d, e, p[15]));
 }
 
 // ---------------------------------------------------------------------------------------------
-// Softmax of query tile t (one thread per row, row == tensor-memory lane) and the epilogue.
+// Softmax of query tile t (two threads per row) and the epilogue.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a,
                                                      const WorkItem& wi, const SegInfo& sg,
                                                      uint32_t tmem, int t, int wq, int lane) {
   const int n_sub = (sg.len + kSub - 1) / kSub;
   const float cs = a.scale_log2;
-  const uint32_t lane_off = uint32_t(wq * 32) << 16;
-  const uint32_t s_addr = tmem + col_s(t) + lane_off;
+  const int q4 = wq & 3;
+  const int rbase = 32 * q4 + 16 * (wq >> 2);  // rows of this warp: rbase + [0, 16)
+  const int kh = lane >> 4;                    // keys [32 kh, 32 kh + 32) of every sub-tile
+  const uint32_t lane_off = uint32_t(rbase) << 16;
   const uint32_t o_addr = tmem + col_o(t) + lane_off;
   const int last_valid = sg.len - (n_sub - 1) * kSub;  // keys of the last sub-tile, 1..64
-  float m = -INFINITY;                                  // running maximum (log2 units)
+  // Q scale factors, A side: row r reads lane r, column r / 32 of each K step's 4-column block;
+  // thread kh writes K step kh's word (the 16x32bx2 store's second half lands 4 columns on)
+  if (!wait_all(&S.bar_q, 0, S, a, kRoleSoftmax)) return;
+  {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(S.qsf[t] + (rbase + (lane & 15)) * 8 +
+                                                          4 * kh);
+    tmem_st1x2<4>(tmem + col_qsf(t) + uint32_t(q4) + lane_off, w);
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&S.bar_qsf[t]));
+  }
+  const uint32_t s_addr = tmem + col_s(t) + lane_off;
+  float m = -INFINITY;  // running maximum (log2 units)
   bool ok = true;
   for (int u = 0; u < n_sub; ++u) {
-    const int x = u & 1;
-    if (!(ok = wait_all(&S.bar_s[t], uint32_t(u) & 1, S, a, kRoleSoftmax))) break;
+    if (!(ok = wait_hinted(&S.bar_s[t], uint32_t(u) & 1, S, a, kRoleSoftmax))) break;
     tc_fence_after();
-    // S already holds the qm K^T term (the fold MMA); the loads also return the maxima of the
-    // four 16-key groups (the tensor-memory load unit reduces)
-    uint32_t r[4][16];
-    float gm[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) gm[g] = tmem_ld16_max(s_addr + 16 * g, r[g]);
+    // S already holds the qm K^T term (the fold MMA); the loads also return the maxima of this
+    // thread's two 16-key scale groups
+    uint32_t r[2][16];
+    float gm[2];
+    gm[0] = tmem_ld16x2_max<32>(s_addr, r[0]);
+    gm[1] = tmem_ld16x2_max<32>(s_addr + 16, r[1]);
     tmem_wait_ld();
     tc_fence_before();
     mbar_arrive(smem_u32(&S.bar_sr[t]));  // S_t(u+1) may now overwrite S
-    // raw S; s'' = S c enters only as the exp2 argument S c + gb (one FMA). c > 0, so the group
-    // maxima of s'' are the raw maxima times c, exactly.
-    float s[64];
+    float s[32];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r[i >> 4][i & 15]);
+    for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i >> 4][i & 15]);
     if (u == n_sub - 1 && last_valid < kSub) {  // keys past the segment: mask, then reduce
+      gm[0] = gm[1] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i >= last_valid) s[i] = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float v[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = s[16 * g + e];
-        gm[g] = max16(v);
+      for (int i = 0; i < 32; ++i) {
+        if (32 * kh + i >= last_valid) s[i] = -INFINITY;
+        gm[i >> 4] = fmaxf(gm[i >> 4], s[i]);
       }
     }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) gm[g] *= cs;
-    const float mx = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
+    // raw S; s'' = S c enters only as the exp2 argument S c + gb (one FMA). c > 0, so the group
+    // maxima of s'' are the raw maxima times c, exactly.
+    gm[0] *= cs;
+    gm[1] *= cs;
+    float mx = fmaxf(gm[0], gm[1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const bool move = mx > m;  // exact running maximum
     const float m_new = move ? mx : m;
     const float alpha = move ? ex2_approx(m - m_new) : 1.f;  // m = -inf gives 0
     const float bias = kLog2_2688 - m_new;                  // s'' + bias = log2 P'
-    uint32_t pk[8];
+    uint32_t pk[4];
     uint32_t sfw = 0u;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {  // 16 keys per scale group
+    for (int gi = 0; gi < 2; ++gi) {  // 16 keys per scale group
       // second level: UE4M3 scale of the group = E4M3(max P' / 6), max P' / 6 = 2^(gm + bias) / 6;
       // codes E2M1(P' / deq(scale)) = E2M1(2^(s'' + bias - log2 deq(scale))); scale 0 -> codes 0
-      const uint32_t sf = cvt_e4m3x2(ex2_approx(gm[g] + (bias - kLog2_6)), 0.f) & 0xFFu;
+      const uint32_t sf = cvt_e4m3x2(ex2_approx(gm[gi] + (bias - kLog2_6)), 0.f) & 0xFFu;
       const float ds = e4m3_to_f32(sf);
       const float gb = sf ? bias - lg2_approx(ds) : -INFINITY;
-      uint32_t b[8];
+      uint32_t bt[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float x0, x1;
-        fma2(x0, x1, s[16 * g + 2 * i], s[16 * g + 2 * i + 1], cs, gb);
-        b[i] = uint32_t(cvt_e2m1x2(ex2_approx(x0), ex2_approx(x1)));
+        fma2(x0, x1, s[16 * gi + 2 * i], s[16 * gi + 2 * i + 1], cs, gb);
+        bt[i] = uint32_t(cvt_e2m1x2(ex2_approx(x0), ex2_approx(x1)));
       }
-      pk[2 * g] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040),
-                              0x5410);
-      pk[2 * g + 1] = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
-                                  __byte_perm(b[6], b[7], 0x0040), 0x5410);
-      sfw |= sf << (8 * g);
+      pk[2 * gi] = __byte_perm(__byte_perm(bt[0], bt[1], 0x0040),
+                               __byte_perm(bt[2], bt[3], 0x0040), 0x5410);
+      pk[2 * gi + 1] = __byte_perm(__byte_perm(bt[4], bt[5], 0x0040),
+                                   __byte_perm(bt[6], bt[7], 0x0040), 0x5410);
+      sfw |= sf << (8 * gi);
     }
+    // the row's four group scales: groups 0, 1 from thread kh = 0, groups 2, 3 from kh = 1
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, sfw, 16);
+    const uint32_t sfrow = kh ? (other | (sfw << 16)) : (sfw | (other << 16));
     // the P slot was last read by PV_t(u-1)
     if (u >= 1) {
-      if (!(ok = wait_all(&S.bar_o[t][x ^ 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax))) break;
+      if (!(ok = wait_hinted(&S.bar_o[t][(u - 1) & 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax)))
+        break;
       tc_fence_after();
     }
-    tmem_st8(tmem + col_p(t) + lane_off, pk);
-    tmem_st1(tmem + col_psf(t) + uint32_t(wq) + lane_off, sfw);
+    // P codes (thread kh: keys 32 kh.., columns 4 kh..), the A-side P scales in column row / 32
+    tmem_st4x2<4>(tmem + col_p(t) + lane_off, pk);
+    tmem_st1x2<4>(tmem + col_psf(t) + uint32_t(q4) + lane_off, sfrow);
     if (u > 0 && __any_sync(0xffffffffu, move)) {
-      // rescale O between PV_t(u-1) and PV_t(u), two 32-column loads in flight
-      if (!(ok = wait_all(&S.bar_o[t][x ^ 1], ((u - 1) >> 1) & 1, S, a, kRoleSoftmax))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int i = 0; i < 4; i += 2) {
-        uint32_t o[32], o2[32];
-        tmem_ld32(o_addr + 32 * i, o);
-        tmem_ld32(o_addr + 32 * i + 32, o2);
+      // rescale O between PV_t(u-1) and PV_t(u): this thread's 72 of the 144 columns
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
+        uint32_t o[32];
+        tmem_ld32x2<72>(o_addr + 32 * i, o);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -440,48 +512,47 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
           fma2(a0, a1, __uint_as_float(o[e]), __uint_as_float(o[e + 1]), alpha, 0.f);
           o[e] = __float_as_uint(a0);
           o[e + 1] = __float_as_uint(a1);
-          fma2(a0, a1, __uint_as_float(o2[e]), __uint_as_float(o2[e + 1]), alpha, 0.f);
-          o2[e] = __float_as_uint(a0);
-          o2[e + 1] = __float_as_uint(a1);
         }
-        tmem_st32(o_addr + 32 * i, o);
-        tmem_st32(o_addr + 32 * i + 32, o2);
+        tmem_st32x2<72>(o_addr + 32 * i, o);
       }
-      uint32_t o3[16];  // the row-sum columns
-      tmem_ld16_max(o_addr + 128, o3);
+      uint32_t o3[8];  // the last 8 of this thread's columns (l among them for kh = 1)
+      tmem_ld8x2<72>(o_addr + 64, o3);
       tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) o3[e] = __float_as_uint(__uint_as_float(o3[e]) * alpha);
-      tmem_st16(o_addr + 128, o3);
+      for (int e = 0; e < 8; ++e) o3[e] = __float_as_uint(__uint_as_float(o3[e]) * alpha);
+      tmem_st8x2<72>(o_addr + 64, o3);
     }
     tmem_wait_st();
     tc_fence_before();
-    mbar_arrive(smem_u32(&S.bar_p[t][x]));
+    mbar_arrive(smem_u32(&S.bar_p[t][u & 1]));
     m = m_new;
   }
   if (!ok) {
     tmem_wait_st();
     return;
   }
-  // PV_t(n_sub - 1) done implies every earlier PV of this in-order stream is done
+  // PV_t(n_sub - 1) done implies every earlier PV of the in-order stream is done
   if (!wait_all(&S.bar_o[t][(n_sub - 1) & 1], ((n_sub - 1) >> 1) & 1, S, a, kRoleEpilogue))
     return;
   tc_fence_after();
-  const float l = __uint_as_float(tmem_ld1(o_addr + 128));  // sum of the dequantized P
+  // sum of the dequantized P: columns 128 and 129 both hold it (the 16 row-sum columns agree)
+  const float l = __uint_as_float(tmem_ld1x2<1>(o_addr + 128));
   tmem_wait_ld();
   const float f = __frcp_rn(l);
-  const int qrow = (wi.qt0 + t) * kTile + wq * 32 + lane;
+  const int qrow = (wi.qt0 + t) * kTile + rbase + (lane & 15);
   const bool valid = qrow < sg.len;
   // LSE of the uncentred scores: (m + log2(l) - log2 2688) ln 2 + (q . km) scale
-  if (a.lse && valid)
+  if (a.lse && valid && kh == 0)
     a.lse[int64_t(wi.head) * a.lse_sh + sg.tok0 + qrow] =
         (m + log2f(l) - kLog2_2688) * 0.6931471805599453f +
         a.q_km[int64_t(wi.head) * a.tpad + sg.row0 + qrow] * a.scale;
-  __nv_bfloat16* dst = a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(wi.head) * a.osh;
+  // this thread's channels: [0, 64) (kh = 0) or [64, 128) (kh = 1)
+  __nv_bfloat16* dst =
+      a.out + int64_t(sg.tok0 + qrow) * a.ost + int64_t(wi.head) * a.osh + 64 * kh;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
     uint32_t o[32];
-    tmem_ld32(o_addr + 32 * i, o);
+    tmem_ld32x2<64>(o_addr + 32 * i, o);
     tmem_wait_ld();
     uint32_t w[16];
 #pragma unroll
@@ -514,22 +585,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&S.bar_q), 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&S.bar_k[i]), 1);
-      mbar_init(smem_u32(&S.bar_v[i]), 1);
-      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 4);  // MMA commits + scale-factor warps
+      mbar_init(smem_u32(&S.bar_ld[i]), 1);
+      mbar_init(smem_u32(&S.bar_free[i]), wi.nq + 1);  // MMA commits + the auxiliary warp
+    }
+    for (int x = 0; x < kAuxBufs; ++x) {
+      mbar_init(smem_u32(&S.bar_aux[x]), 32);
+      mbar_init(smem_u32(&S.bar_auxfree[x]), wi.nq);
     }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&S.bar_qsf[t]), 256);
       mbar_init(smem_u32(&S.bar_s[t]), 1);
-      mbar_init(smem_u32(&S.bar_sr[t]), 128);
+      mbar_init(smem_u32(&S.bar_sr[t]), 256);
       for (int x = 0; x < 2; ++x) {
-        mbar_init(smem_u32(&S.bar_p[t][x]), 128);
+        mbar_init(smem_u32(&S.bar_p[t][x]), 256);
         mbar_init(smem_u32(&S.bar_o[t][x]), 1);
       }
       mbar_init(smem_u32(&S.bar_drain[t]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&S.bar_sf[b]), 128);
-      mbar_init(smem_u32(&S.bar_sffree[b]), wi.nq);
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -543,14 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&S.tmem_base), 512);
     tmem_relinquish();
   }
-  // fold operands: A rows [1, 1, 1, 0 ...] (BF16 1.0 = 0x3F80) then zeros; B zero halves
+  // fold operands: A rows [1, 1, 1, 0 ...] (BF16 1.0 = 0x3F80) then zeros; B zero halves;
+  // the 1.0 rows' scale block; the 1.0 rows of every V^T stage
   if (threadIdx.x < 16) {
     const uint4 v1 = threadIdx.x < 8 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u)
                                      : make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4*>(S.fa)[threadIdx.x] = v1;
   }
-  for (int i = threadIdx.x; i < 4 * 64; i += kThreads)
+  for (int i = threadIdx.x; i < kAuxBufs * 2 * 64; i += kThreads)
     reinterpret_cast<uint4*>(S.fb[i >> 7][(i >> 6) & 1] + 1024)[i & 63] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x < 32) {  // UE4M3 1.0 = 0x38 for the 16 rows of 1.0 (lanes 0-15)
+    const uint32_t one = threadIdx.x < 16 ? 0x38383838u : 0u;
+    reinterpret_cast<uint4*>(S.ones_cp)[threadIdx.x] = make_uint4(one, 0u, 0u, 0u);
+  }
   for (int i = threadIdx.x; i < kStages * 64; i += kThreads)  // E2M1 1.0 = 0x2, two per byte
     reinterpret_cast<uint4*>(S.v[i >> 6] + kCodeTile)[i & 63] =
         make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
@@ -565,11 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     const int t = warp - kMmaWarp;
     if (t < wi.nq) mma_issuer(S, a, wi, sg, tmem, t);
-  } else if (warp >= kCorrWarp) {
-    scale_factor_warps(S, a, wi, sg, tmem, warp - kCorrWarp, lane);
+  } else if (warp == kAuxWarp) {
+    aux_warp(S, a, wi, sg, lane);
   } else {
-    const int t = warp >> 2;
-    if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 3, lane);
+    const int t = warp >> 3;
+    if (t < wi.nq) softmax_and_epilogue(S, a, wi, sg, tmem, t, warp & 7, lane);
   }
   tc_fence_before();
   __syncthreads();

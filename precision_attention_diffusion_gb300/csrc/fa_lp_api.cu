@@ -325,12 +325,13 @@ void build_plan(fa_lp_plan* p) {
     off = align_up(off + std::max<size_t>(bytes, 1), 1024);
     return o;
   };
-  if (p->mode == FA_LP_MODE_FP8) {
+  if (falp::is_fp8(*p)) {
+    const size_t R = size_t(falp::fp8_scale_rows(*p));
     w.q_codes = take(H * Tp * 128);
     w.k_codes = take(H * Tp * 128);
     w.v_codes = take(H * 128 * Tp);
-    w.amax = take(3 * H * 4);
-    w.descale = take(3 * H * 4);
+    w.amax = take(3 * R * H * 4);
+    w.descale = take(3 * R * H * 4);
   } else {
     w.q_codes = take(H * Tp * 64);
     w.k_codes = take(H * Tp * 64);
@@ -476,7 +477,8 @@ int fa_lp_plan_create(int64_t tokens, int heads, const int32_t* cu, int num_segm
   *out = nullptr;
   if (tokens < 0 || tokens > (int64_t(1) << 30)) return FA_LP_ERR_INVALID_ARG;
   if (heads < 1 || heads > 1024 || num_segments < 1 || device < 0) return FA_LP_ERR_INVALID_ARG;
-  if (mode != FA_LP_MODE_FP8 && mode != FA_LP_MODE_NVFP4) return FA_LP_ERR_INVALID_ARG;
+  if (mode != FA_LP_MODE_FP8 && mode != FA_LP_MODE_NVFP4 && mode != FA_LP_MODE_FP8_SEGMENT)
+    return FA_LP_ERR_INVALID_ARG;
   if (cu[0] != 0 || int64_t(cu[num_segments]) != tokens) return FA_LP_ERR_INVALID_ARG;
   for (int s = 0; s < num_segments; ++s)
     if (cu[s + 1] < cu[s]) return FA_LP_ERR_INVALID_ARG;
@@ -583,7 +585,7 @@ int fa_lp_quantize(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const
   void* base = nullptr;
   if ((st = falp::workspace_acquire(p->device, p->ws.total, stream, &base)) != FA_LP_OK) return st;
   if (p->tokens > 0) {
-    st = (p->mode == FA_LP_MODE_FP8)
+    st = falp::is_fp8(*p)
              ? falp::launch_fp8_quantize(*p, static_cast<uint8_t*>(base), q, qst, qsh, k, kst, ksh,
                                          v, vst, vsh, stream)
              : falp::launch_nvfp4_quantize(*p, static_cast<uint8_t*>(base), q, qst, qsh, k, kst,
@@ -620,7 +622,7 @@ int fa_lp_forward_varlen_lse(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void*
     if ((st = workspace_of_plan(p, &base)) != FA_LP_OK) return st;
   }
   if (p->work.empty()) return FA_LP_OK;
-  return (p->mode == FA_LP_MODE_FP8)
+  return falp::is_fp8(*p)
              ? falp::launch_fp8_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, lse,
                                           lse_stride_head, stream)
              : falp::launch_nvfp4_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, lse,
@@ -644,7 +646,7 @@ int fa_lp_forward_sparse(fa_lp_plan* p, const int32_t* cu_seqlens_dev,
                          int64_t lse_stride_head, void* stream_) {
   (void)cu_seqlens_dev;
   if (!p) return FA_LP_ERR_INVALID_ARG;
-  if (p->mode != FA_LP_MODE_FP8) return FA_LP_ERR_UNSUPPORTED;
+  if (!falp::is_fp8(*p)) return FA_LP_ERR_UNSUPPORTED;
   if (!p->quantized) return FA_LP_ERR_STATE;
   if (p->tokens > 0 && bad_view(out, ost, osh)) return FA_LP_ERR_INVALID_ARG;
   if (num_indices < 0 || (p->tokens > 0 && !block_offsets) || (num_indices > 0 && !block_indices))
@@ -893,7 +895,7 @@ int fa_lp_attention_sparse_host(fa_lp_plan* p, const void* q, int64_t qst, int64
                                 const int32_t* block_indices, int64_t num_indices, void* out,
                                 int64_t ost, int64_t osh, int heads_per_chunk, void* stream) {
   if (!p) return FA_LP_ERR_INVALID_ARG;
-  if (p->mode != FA_LP_MODE_FP8) return FA_LP_ERR_UNSUPPORTED;
+  if (!falp::is_fp8(*p)) return FA_LP_ERR_UNSUPPORTED;
   if (num_indices < 0 || (p->tokens > 0 && !block_offsets) || (num_indices > 0 && !block_indices))
     return FA_LP_ERR_INVALID_ARG;
   const HostLists lists{block_offsets, block_indices, num_indices};
@@ -923,12 +925,14 @@ int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
     d->elem_bytes = eb;
     return FA_LP_OK;
   };
-  if (p->mode == FA_LP_MODE_FP8) {
+  if (falp::is_fp8(*p)) {
     switch (which) {
       case FA_LP_Q_CODES: return set(p->ws.q_codes, H, Tp, 128, 1);
       case FA_LP_K_CODES: return set(p->ws.k_codes, H, Tp, 128, 1);
       case FA_LP_V_CODES: return set(p->ws.v_codes, H, 128, Tp, 1);
-      case FA_LP_DESCALE: return set(p->ws.descale, 1, 3, H, 4);
+      case FA_LP_DESCALE:
+        return p->mode == FA_LP_MODE_FP8_SEGMENT ? set(p->ws.descale, 3, p->nseg, H, 4)
+                                                 : set(p->ws.descale, 1, 3, H, 4);
       default: return FA_LP_ERR_INVALID_ARG;
     }
   }

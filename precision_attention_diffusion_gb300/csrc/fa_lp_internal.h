@@ -70,7 +70,7 @@ struct WsLayout {
   size_t k_chunk = 0;                            // NVFP4 scratch: f64 [nblk][H][128] chunk sums
   size_t q_km = 0;                               // NVFP4: f32 [H][Tp] q . km (row LSE term)
   size_t qmk = 0;                                // NVFP4: f32 qm K^T table (per segment)
-  size_t amax = 0, descale = 0;                  // FP8: u32 [3][H], f32 [3][H]
+  size_t amax = 0, descale = 0;                  // FP8: u32 / f32 [3][R][H], R = 1 or nseg
   size_t total = 0;
 };
 
@@ -168,6 +168,15 @@ int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStr
 int next_launch_generation();
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FA_LP_OK : FA_LP_ERR_CUDA; }
+
+// FP8 plans: one scale per (tensor, head), or per (segment, tensor, head).
+inline bool is_fp8(const fa_lp_plan& p) {
+  return p.mode == FA_LP_MODE_FP8 || p.mode == FA_LP_MODE_FP8_SEGMENT;
+}
+// Rows of the FP8 amax / descale arrays per tensor: 1, or the number of segments.
+inline int fp8_scale_rows(const fa_lp_plan& p) {
+  return p.mode == FA_LP_MODE_FP8_SEGMENT ? p.nseg : 1;
+}
 
 // Raise a kernel's dynamic shared-memory limit on `device` once (the attribute belongs to the
 // device's context, so every device is set up on its own first launch). `done` holds one bit per

@@ -14,7 +14,8 @@
 // segment starts on a 128-row boundary, rows past L_s are zero):
 //   Q, K codes : u8 [H][Tpad][128]  (K-major tiles for the QK^T tensor-core product)
 //   V codes    : u8 [H][128][Tpad]  (V^T, K-major along keys for the PV product)
-//   descale    : f32 [3][H]
+//   descale    : f32 [3][R][H], R = 1 (one scale per (tensor, head)) or the number of segments
+//                (the per-segment mode: amax over the segment's own tokens)
 // Both passes are HBM-bound streaming kernels: 16-byte vector loads and stores, grid sized to the
 // data (many waves over the 152 SMs).
 #include <cuda_bf16.h>
@@ -65,6 +66,59 @@ __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint16_t* __restric
   }
 }
 
+// Pass 1 of the per-segment mode: per (tensor, segment, head) max |x| over the 128-row blocks of
+// the padded token axis (every block lies in one segment), one block of 256 threads per (block,
+// head, tensor): 16 lanes x 16 bytes per row, eight rows per thread, loads issued together.
+__global__ void __launch_bounds__(256) fp8_amax_seg_kernel(
+    const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
+    int64_t kst, int64_t ksh, const uint16_t* __restrict__ v, int64_t vst, int64_t vsh,
+    const BlockInfo* __restrict__ blocks, int H, int R, uint32_t* __restrict__ amax) {
+  const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  const BlockInfo bi = blocks[b];
+  const uint16_t* x = z == 0 ? q : (z == 1 ? k : v);
+  const int64_t st = z == 0 ? qst : (z == 1 ? kst : vst);
+  const int64_t sh = z == 0 ? qsh : (z == 1 ? ksh : vsh);
+  const int tid = threadIdx.x, sub = tid & 15;
+  uint4 w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = (tid >> 4) + 16 * j;
+    w[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < bi.nvalid)
+      w[j] = __ldg(reinterpret_cast<const uint4*>(x + int64_t(bi.tok0 + r) * st + int64_t(h) * sh) +
+                   sub);
+  }
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    m = __vmaxu2(m, w[j].x & 0x7FFF7FFFu);
+    m = __vmaxu2(m, w[j].y & 0x7FFF7FFFu);
+    m = __vmaxu2(m, w[j].z & 0x7FFF7FFFu);
+    m = __vmaxu2(m, w[j].w & 0x7FFF7FFFu);
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[8];
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t r = red[0];
+    for (int i = 1; i < 8; ++i) r = max(r, red[i]);
+    atomicMax(amax + (int64_t(z) * R + bi.seg) * H + h, r << 16);
+  }
+}
+
+// Descales of the per-segment mode, one thread per (tensor, segment, head); a segment without
+// tokens keeps amax 0 and gets descale 1.
+__global__ void fp8_descale_kernel(const uint32_t* __restrict__ amax, int n,
+                                   float* __restrict__ descale) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float a = __uint_as_float(amax[i]);
+  descale[i] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
+}
+
 __device__ __forceinline__ float inv_of(uint32_t amax_bits) {
   const float a = __uint_as_float(amax_bits);
   return a > 0.f ? __fdiv_rn(448.f, a) : 1.f;
@@ -89,16 +143,18 @@ __device__ __forceinline__ uint2 pack8(const uint4 w, float inv) {
 __global__ void __launch_bounds__(256) fp8_pack_qk_kernel(
     const uint16_t* __restrict__ q, int64_t qst, int64_t qsh, const uint16_t* __restrict__ k,
     int64_t kst, int64_t ksh, const BlockInfo* __restrict__ blocks, int H, int64_t Tp,
-    const uint32_t* __restrict__ amax, uint8_t* __restrict__ qc, uint8_t* __restrict__ kc,
+    const uint32_t* __restrict__ amax, int R, uint8_t* __restrict__ qc, uint8_t* __restrict__ kc,
     float* __restrict__ descale) {
   const int b = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const BlockInfo bi = blocks[b];
   const uint16_t* x = z == 0 ? q : k;
   const int64_t st = z == 0 ? qst : kst, sh = z == 0 ? qsh : ksh;
   uint8_t* dst = (z == 0 ? qc : kc) + (int64_t(h) * Tp + int64_t(b) * kTile) * kD;
-  const uint32_t ab = amax[z * H + h];
+  // R == 1: one scale per (tensor, head), descales written here; R == nseg: per segment, the
+  // descales come from fp8_descale_kernel
+  const uint32_t ab = amax[(int64_t(z) * R + (R > 1 ? bi.seg : 0)) * H + h];
   const float inv = inv_of(ab);
-  if (b == 0 && threadIdx.x == 0) {
+  if (R == 1 && b == 0 && threadIdx.x == 0) {
     const float a = __uint_as_float(ab);
     descale[z * H + h] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
   }
@@ -122,14 +178,14 @@ __global__ void __launch_bounds__(256) fp8_pack_vt_kernel(const uint16_t* __rest
                                                           const BlockInfo* __restrict__ blocks,
                                                           int H, int64_t Tp,
                                                           const uint32_t* __restrict__ amax,
-                                                          uint8_t* __restrict__ vt,
+                                                          int R, uint8_t* __restrict__ vt,
                                                           float* __restrict__ descale) {
   __shared__ __align__(16) uint8_t tile[kTile][kD + 4];
   const int b = blockIdx.x, h = blockIdx.y;
   const BlockInfo bi = blocks[b];
-  const uint32_t ab = amax[2 * H + h];
+  const uint32_t ab = amax[(2 * int64_t(R) + (R > 1 ? bi.seg : 0)) * H + h];
   const float inv = inv_of(ab);
-  if (b == 0 && threadIdx.x == 0) {
+  if (R == 1 && b == 0 && threadIdx.x == 0) {
     const float a = __uint_as_float(ab);
     descale[2 * H + h] = a > 0.f ? __fdiv_rn(a, 448.f) : 1.f;
   }
@@ -185,25 +241,33 @@ __global__ void encode_kernel(int format, const float* __restrict__ x, int64_t n
 int launch_fp8_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t qst, int64_t qsh,
                         const void* k, int64_t kst, int64_t ksh, const void* v, int64_t vst,
                         int64_t vsh, cudaStream_t stream) {
-  const int H = p.heads;
+  const int H = p.heads, R = fp8_scale_rows(p);
   uint32_t* amax = reinterpret_cast<uint32_t*>(ws + p.ws.amax);
-  if (cudaMemsetAsync(amax, 0, size_t(3) * H * sizeof(uint32_t), stream) != cudaSuccess)
+  float* descale = reinterpret_cast<float*>(ws + p.ws.descale);
+  if (cudaMemsetAsync(amax, 0, size_t(3) * R * H * sizeof(uint32_t), stream) != cudaSuccess)
     return FA_LP_ERR_CUDA;
   const auto* qb = static_cast<const uint16_t*>(q);
   const auto* kb = static_cast<const uint16_t*>(k);
   const auto* vb = static_cast<const uint16_t*>(v);
-  dim3 g1(unsigned((p.tokens + kAmaxTok - 1) / kAmaxTok), unsigned(H), 3);
-  fp8_amax_kernel<<<g1, 256, 0, stream>>>(qb, qst, qsh, kb, kst, ksh, vb, vst, vsh, p.tokens, H,
-                                          amax);
   const unsigned nblk = unsigned(p.blocks.size());
+  if (R == 1) {
+    dim3 g1(unsigned((p.tokens + kAmaxTok - 1) / kAmaxTok), unsigned(H), 3);
+    fp8_amax_kernel<<<g1, 256, 0, stream>>>(qb, qst, qsh, kb, kst, ksh, vb, vst, vsh, p.tokens, H,
+                                            amax);
+  } else {
+    dim3 g1(nblk, unsigned(H), 3);
+    fp8_amax_seg_kernel<<<g1, 256, 0, stream>>>(qb, qst, qsh, kb, kst, ksh, vb, vst, vsh,
+                                                p.d_blocks, H, R, amax);
+    const int n = 3 * R * H;
+    fp8_descale_kernel<<<(n + 255) / 256, 256, 0, stream>>>(amax, n, descale);
+  }
   dim3 g2(nblk, unsigned(H), 2);
   fp8_pack_qk_kernel<<<g2, 256, 0, stream>>>(qb, qst, qsh, kb, kst, ksh, p.d_blocks, H, p.tpad,
-                                             amax, ws + p.ws.q_codes, ws + p.ws.k_codes,
-                                             reinterpret_cast<float*>(ws + p.ws.descale));
+                                             amax, R, ws + p.ws.q_codes, ws + p.ws.k_codes,
+                                             descale);
   dim3 g3(nblk, unsigned(H));
-  fp8_pack_vt_kernel<<<g3, 256, 0, stream>>>(vb, vst, vsh, p.d_blocks, H, p.tpad, amax,
-                                             ws + p.ws.v_codes,
-                                             reinterpret_cast<float*>(ws + p.ws.descale));
+  fp8_pack_vt_kernel<<<g3, 256, 0, stream>>>(vb, vst, vsh, p.d_blocks, H, p.tpad, amax, R,
+                                             ws + p.ws.v_codes, descale);
   return cuda_status(cudaGetLastError());
 }
 

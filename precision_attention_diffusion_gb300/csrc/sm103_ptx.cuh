@@ -299,9 +299,69 @@ __device__ __forceinline__ void tmem_st8x2(uint32_t taddr, const uint32_t (&r)[8
                "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
+template <int kSplit>
+__device__ __forceinline__ float tmem_ld16x2_max(uint32_t taddr, uint32_t (&r)[16]) {
+  float mx;
+  asm volatile("tcgen05.ld.red.sync.aligned.16x32bx2.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,"
+               "%10,%11,%12,%13,%14,%15}, %16, [%17], %18;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(mx)
+               : "r"(taddr), "n"(kSplit)
+               : "memory");
+  return mx;
+}
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld8x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr), "n"(kSplit)
+               : "memory");
+}
+template <int kSplit>
+__device__ __forceinline__ uint32_t tmem_ld1x2(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%0}, [%1], %2;"
+               : "=r"(r)
+               : "r"(taddr), "n"(kSplit)
+               : "memory");
+  return r;
+}
+template <int kSplit>
+__device__ __forceinline__ void tmem_st4x2(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x4.b32 [%0], %1, {%2,%3,%4,%5};" ::"r"(taddr),
+               "n"(kSplit), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+template <int kSplit>
+__device__ __forceinline__ void tmem_st1x2(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x1.b32 [%0], %1, {%2};" ::"r"(taddr),
+               "n"(kSplit), "r"(v)
+               : "memory");
+}
 #undef FALP_OUT32
 #undef FALP_IN32
 #undef FALP_LIST32
+
+// tcgen05.cp of a 32-row x 128-bit matrix from shared memory (no-swizzle K-major descriptor:
+// row i at byte 16 i when the stride byte offset is 128) into columns [col, col + 4) of lanes
+// i, 32 + i, 64 + i and 96 + i (replicated into every lane quarter), as B-side scale factors
+// need. Asynchronous, ordered before the issuing thread's later tcgen05.mma; completion is
+// tracked by tcgen05.commit like an MMA.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Warp-converged form: the whole warp executes the call, one elected lane (lane 0, the lane that
+// issues the warp's MMAs and commits) issues the copy.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr), "l"(sdesc)
+      : "memory");
+}
 
 // ------------------------------------------------------------------------------------------------
 // tcgen05.mma descriptors

@@ -25,6 +25,7 @@ FA_LP_ERR_STATE = 6
 
 MODE_FP8 = 0
 MODE_NVFP4 = 1
+MODE_FP8_SEGMENT = 2  # FP8 with one scale per (segment, tensor, head)
 
 (Q_CODES, K_CODES, V_CODES, DESCALE, Q_SCALES, K_SCALES, V_SCALES, Q_MEANS, K_MEANS, Q_KM,
  QMK_TABLE) = range(11)

@@ -11,7 +11,7 @@
 // What one CTA computes (readings r5 with tau = 0, r9, r11, r12): for the two 128-row query tiles
 // Q0, Q1 of one (segment, head), over 64-key sub-tiles u from the segment start,
 //   s''(i, j)  = (deq(Qc_i) . deq(Kc_j) + Tq_t(j)) c,  Tq_t(j) = qm_t . deq(Kc_j) (the table
-//                qmk_nvfp4.cu writes during quantization, added to S by a BF16 MMA),
+//                qmk_nvfp4.cu writes during quantization, added to S by a TF32 MMA),
 //                with c = softmax_scale log2(e)            (log2 units)
 //   m_i        = running row maximum of s'' (exact: it moves whenever a sub-tile exceeds it)
 //   P'(i, j)   = 2^(s'' - m_i + log2 2688)                  (= 2688 exp(S' - m) of the pages)
@@ -36,16 +36,16 @@
 //               tensor memory), each with the tcgen05.cp copies of the K and V scale factors its
 //               MMAs read, from shared into its tile's tensor memory (ordered before its MMAs):
 //                 S_t(u)  = deq(Qc_t) deq(Kc(u))^T   2 MMAs M=128 N=64  K=64, A, B in smem
-//                 S_t(u) += 1 Tq_t(u)^T              1 kind::f16 MMA  M=128 N=64 K=16 (A =
+//                 S_t(u) += 1 Tq_t(u)^T              1 kind::tf32 MMA M=128 N=64 K=8 (A =
 //                                                    rows [1, 1, 1, 0...], B = the table
-//                                                    entries as three BF16 pieces)
+//                                                    entries as three TF32 pieces)
 //                 O_t    += deq(P_t(u)) deq(V(u))    1 MMA  M=128 N=144 K=64, A = P in TMEM
 //                                                    (N 128-143: the 1.0 rows, giving l)
 //               S_t(u+1) is issued as soon as the softmax has read S_t(u), so the scores of the
 //               next sub-tile are computed while the softmax works on the current ones;
 //   warp 19     per sub-tile, from the stage's records: the K and V scale factors re-laid out as
 //               32-row x 16-byte blocks for tcgen05.cp, and each query tile's fold tile (every
-//               key's qm K^T table entry as three BF16 pieces).
+//               key's qm K^T table entry as three TF32 pieces, exact).
 // Tensor memory (512 columns), per query tile t at 256 t: O [0, 144) (column 128: l), P codes
 // [144, 152), P scales [152, 156) (A side: row r in lane r, column r / 32; [156, 160) takes the
 // second thread's copy of the word), Q scales [160, 168), K scales [168, 184) (two buffers of two
@@ -74,8 +74,8 @@ constexpr uint32_t kSfTile = 128 * 8;     // 128 rows of 8 UE4M3 scales
 constexpr uint32_t kIdescS = idesc_mxf4nvf4(128, kSub);
 constexpr uint32_t kVTile = 144 * 64;    // V^T stage: 128 channel rows + 16 rows of E2M1 1.0
 constexpr uint32_t kIdescPV = idesc_mxf4nvf4(128, 144);  // channels + 16 row-sum columns
-// kind::f16: D f32, A and B BF16, K-major, M=128, N=64
-constexpr uint32_t kIdescFold = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(kSub) >> 3) << 17) |
+// kind::tf32: D f32, A and B TF32 (format 2), K-major, M=128, N=64
+constexpr uint32_t kIdescFold = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t(kSub) >> 3) << 17) |
                                 ((128u >> 4) << 24);
 constexpr float kLog2_2688 = 11.392317422778761f;  // log2(448 * 6)
 constexpr float kLog2_6 = 2.5849625007211562f;
@@ -95,9 +95,9 @@ struct Smem {
   uint8_t q[2][kCodeTile];
   uint8_t k[kStages][kCodeTile];
   uint8_t v[kStages][kVTile];      // V^T: 128 channel rows of 128 keys, 16 rows of 1.0
-  // qm K^T fold into S (one kind::f16 MMA per sub-tile and query tile): A = 128 identical rows
-  // [1, 1, 1, 0...] (one core matrix repeated, then a zero core matrix), B = per key the table
-  // entry as three BF16 pieces (64 keys x 16 bytes, then 1 KB of zeros for K 8..15)
+  // qm K^T fold into S (one kind::tf32 MMA per sub-tile and query tile): A = 128 identical rows
+  // [1, 1, 1, 0 | 0, 0, 0, 0] (one core matrix repeated, then a zero core matrix), B = per key the
+  // table entry as three TF32 pieces (64 keys x 16 bytes, then 1 KB of zeros for K 4..7)
   uint8_t fb[kAuxBufs][2][2048];   // [u mod 4][t]
   uint8_t ksf_cp[kAuxBufs][2][512];  // [u mod 4][K step]: row i = scales of keys i, 32 + i, 0, 0
   uint8_t vsf_cp[kAuxBufs][512];     // [u mod 4]: row i = scales of channels i, 32+i, 64+i, 96+i
@@ -165,7 +165,7 @@ __device__ __forceinline__ bool wait_hinted(uint64_t* bar, uint32_t parity, Smem
 // One elect.sync for the whole S group of a query tile and sub-tile (a tcgen05 instruction group
 // behind a single elect costs the issuing warp far less than one elect per instruction): the two K
 // scale blocks into tensor memory, the two block-scaled K = 64 MMAs (the first overwriting S), the
-// BF16 fold MMA adding the qm K^T term, and the commit of all of them to `bar`.
+// TF32 fold MMA adding the qm K^T term, and the commit of all of them to `bar`.
 __device__ __forceinline__ void s_group_elect(uint32_t d, uint64_t qa, uint64_t kb, uint32_t sfa,
                                               uint32_t ks, uint64_t ksf0, uint64_t ksf1,
                                               uint64_t fa, uint64_t fb, uint32_t bar) {
@@ -181,7 +181,7 @@ __device__ __forceinline__ void s_group_elect(uint32_t d, uint64_t qa, uint64_t 
       "[%3], [%4], p0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], qa1, kb1, %9, "
       "[sfa1], [ks1], p1;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %10, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %7, %8, %10, p1;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}"
       ::"r"(d), "l"(qa), "l"(kb), "r"(sfa), "r"(ks), "l"(ksf0), "l"(ksf1), "l"(fa), "l"(fb),
       "r"(kIdescS), "r"(kIdescFold), "r"(bar)
@@ -282,8 +282,8 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
   auto issue_s = [&](int u) {
     const int x = u % kAuxBufs, h = u & 1, st = (u >> 1) % kStages;
     // K scales of u into buffer u & 1, last read by S_t(u-2): complete, since the softmax has
-    // read S_t(u-1); S += 1 . (hi + mid + lo) of the table: the qm K^T term, exact to FP32
-    // accumulation
+    // read S_t(u-1); S += 1 . (hi + mid + lo) of the table (TF32 pieces whose sum is the FP32
+    // entry exactly): the qm K^T term, to FP32 accumulation
     const uint64_t kb = dk + (((st * kCodeTile) + h * (kSub * 64)) >> 4);
     s_group_elect(d_s, dq, kb, tmem + col_qsf(t), tmem + col_ksf(t, u & 1),
                   dksf + ((uint32_t(x) * 1024u) >> 4), dksf + ((uint32_t(x) * 1024u + 512u) >> 4),
@@ -377,23 +377,22 @@ __device__ __forceinline__ void aux_warp(Smem& S, const Nvfp4Args& a, const Work
       *reinterpret_cast<uint4*>(S.vsf_cp[x] + 16 * lane) =
           h ? make_uint4(vw[0].y, vw[1].y, vw[2].y, vw[3].y)
             : make_uint4(vw[0].x, vw[1].x, vw[2].x, vw[3].x);
-      // fold B tiles: key row `key` = the table entry of query tile ft as three BF16 pieces
+      // fold B tiles: key row `key` = the table entry of query tile ft as three TF32 pieces:
+      // hi = the entry's top 11 significant bits, mid = the next 11 of the exact remainder, lo =
+      // the rest (at most 2 bits); each is exact in TF32 and hi + mid + lo is the entry
 #pragma unroll
       for (int ft = 0; ft < 2; ++ft) {
         if (ft == 1 && !two) break;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int key = lane + 32 * r;
-          float v = cv[ft][2 * h + r];
-          uint32_t pc[3];
-#pragma unroll
-          for (int p = 0; p < 3; ++p) {
-            const __nv_bfloat16 bv = __float2bfloat16_rn(v);
-            pc[p] = uint32_t(__bfloat16_as_ushort(bv));
-            v = v - __bfloat162float(bv);  // exact: v and its BF16 rounding share the top bits
-          }
+          const float v = cv[ft][2 * h + r];
+          const uint32_t hi = __float_as_uint(v) & 0xFFFFE000u;
+          const float rem = v - __uint_as_float(hi);
+          const uint32_t mid = __float_as_uint(rem) & 0xFFFFE000u;
+          const float lo = rem - __uint_as_float(mid);
           *reinterpret_cast<uint4*>(S.fb[x][ft] + (key >> 3) * 128 + (key & 7) * 16) =
-              make_uint4(pc[0] | (pc[1] << 16), pc[2], 0u, 0u);
+              make_uint4(hi, mid, __float_as_uint(lo), 0u);
         }
       }
       fence_proxy_async_smem();  // the copies and the fold MMAs read these through the async proxy
@@ -614,10 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&S.tmem_base), 512);
     tmem_relinquish();
   }
-  // fold operands: A rows [1, 1, 1, 0 ...] (BF16 1.0 = 0x3F80) then zeros; B zero halves;
-  // the 1.0 rows' scale block; the 1.0 rows of every V^T stage
+  // fold operands: A rows [1, 1, 1, 0] (TF32 1.0 = 0x3F800000) then a zero core matrix; B zero
+  // halves; the 1.0 rows' scale block; the 1.0 rows of every V^T stage
   if (threadIdx.x < 16) {
-    const uint4 v1 = threadIdx.x < 8 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u)
+    const uint4 v1 = threadIdx.x < 8 ? make_uint4(0x3F800000u, 0x3F800000u, 0x3F800000u, 0u)
                                      : make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4*>(S.fa)[threadIdx.x] = v1;
   }

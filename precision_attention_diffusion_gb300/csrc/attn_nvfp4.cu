@@ -312,9 +312,11 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
     bool ok = true;
     for (int u = 0; u <= n_sub && ok; ++u) {
       if (u < n_sub) {
-        // the auxiliary warp's blocks of u (written after the stage of u landed)
-        if (u > 0 && !(ok = wait(&S.bar_sr[t], (u - 1) & 1))) break;
+        // the auxiliary warp's blocks of u (written after the stage of u landed; the auxiliary
+        // warp runs well ahead, so this wait is done before the one S_t(u) really waits for:
+        // the softmax's read of S_t(u-1))
         if (!(ok = wait(&S.bar_aux[u % kAuxBufs], (u / kAuxBufs) & 1))) break;
+        if (u > 0 && !(ok = wait(&S.bar_sr[t], (u - 1) & 1))) break;
         tc_fence_after();
         issue_s(u);
       }

@@ -59,8 +59,8 @@ METRICS = {"fp8": METRIC, "nvfp4": METRIC_NVFP4, "sparse": METRIC_SPARSE}
 NCU_TRAFFIC = {
     ("fp8_s30272_h56", "851fe009161411867603b2b56aad0561092e6d859922ef3391f860603af88f41"):
         1.954e9 + 425.45e6,
-    ("nvfp4_s30272_h56", "65044c1b6940a7fe0323b3d5f6417f07d1ec5d9a23830f8301be43b346afeac3"):
-        2.383e9 + 424.98e6,
+    ("nvfp4_s30272_h56", "672840bb516a3c5d4479ef3daa7d2ef81e7f0c13a8d1f8d4ba30d34472782ff5"):
+        2.35e9 + 425.01e6,
     ("sparse_fp8_s30272_h56", "3607c1f0c0bce02d7a02c4c42d1c5db232c42a385a3bef444ef7cf3f0f8354c1"):
         1.533e9 + 425.53e6,
 }

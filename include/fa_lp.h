@@ -212,8 +212,9 @@ FA_LP_API int fa_lp_forward_varlen_lse(fa_lp_plan* plan, const int32_t* cu_seqle
  * with the arithmetic of fa_lp_forward_varlen (E4M3 Q K^T and P V, FP32 accumulation, online
  * softmax with the lazy reference maximum over the listed blocks in list order, l from the
  * quantized P); a row whose list is empty is written as 0 (LSE -inf). The pages' SM120 mode
- * takes Q K^T in INT8; here both products are E4M3, on the same quantized operands as the dense
- * forward (call fa_lp_quantize first).
+ * takes Q K^T in INT8; sm_103a has no INT8 tensor-core MMA (tcgen05.mma kind::i8 does not
+ * assemble for it), so here both products are E4M3, on the same quantized operands as the dense
+ * forward (call fa_lp_quantize first; FP8 and FP8_SEGMENT plans).
  *   block_offsets : device int32 [heads * G + 1], non-decreasing, block_offsets[0] >= 0; the list
  *                   of (head h, query block g) is block_indices[block_offsets[h G + g] ..
  *                   block_offsets[h G + g + 1]). G = fa_lp_sparse_query_blocks(plan) = sum over

@@ -6,7 +6,8 @@
 // Tests (ragged lengths, variable block counts, empty rows). The per-block arithmetic is the
 // dense FP8 path's (SGLang PR #40175, Modifications, kernel.py): E4M3 QK and PV with FP32
 // accumulation, online softmax, P packed to E4M3. The pages' SM120 mode computes QK in INT8;
-// GB300's INT8 tensor rate is far below its FP8 rate, so both products stay in E4M3 here.
+// sm_103a has no INT8 tcgen05.mma (ptxas rejects kind::i8 for this target), so both products
+// stay in E4M3 here.
 //
 // Semantics (reading r16): a query row in the g-th 64-row block of its segment attends to the
 // keys of the 64-key blocks listed for (head, g) -- block kb covers keys [64 kb, 64 kb + 64) of

@@ -119,3 +119,24 @@ def test_fp8_segment_host_entry_equals_device_call(fa):
     plan.attention_host(hbuf[:, 0], hbuf[:, 1], hbuf[:, 2], hout, heads_per_chunk=4)
     torch.cuda.synchronize()
     assert torch.equal(hout, out.cpu())
+
+
+def test_fp8_segment_lse(fa):
+    """Row log-sum-exp on a per-segment plan: within the f16 row-sum bound (2.5e-3, as for the
+    FP8 mode) of the emulating oracle run with the per-segment descales."""
+    cu, H = [0, 0, 17, 300, 300, 1400, 1500], 3
+    T = cu[-1]
+    q, k, v = scaled_segments(cu, H, 73, [1.0, 0.02, 4.0, 1.0, 0.25, 30.0])
+    plan = fa.Plan(cu, H, mode=fa.MODE_FP8_SEGMENT)
+    plan.quantize(q.cuda(), k.cuda(), v.cuda())
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((H, T), 7.0, dtype=torch.float32, device="cuda")
+    plan.forward(out, lse=lse)
+    torch.cuda.synchronize()
+    nat, ds = check_codes(fa, plan, cu, q, k, v)
+    rows = all_rows(cu, H)
+    _, _, emu = oracle.attn_fp8(nat["q"], nat["k"], nat["v"], ds[0], ds[1], ds[2], cu, rows,
+                                SCALE, n_kv=KV_TILE, tau=TAU, lse=True)
+    g = lse.cpu().numpy()
+    got = np.array([g[h, t] for t, h in rows], np.float64)
+    assert np.abs(got - emu).max() < 2.5e-3, np.abs(got - emu).max()

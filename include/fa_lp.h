@@ -371,6 +371,37 @@ FA_LP_API int fa_lp_get_last_error(fa_lp_plan* plan, int* device_status);
  * frees tensor memory and returns. Small values are for tests of that path. spins >= 1. */
 FA_LP_API int fa_lp_plan_set_wait_limit(fa_lp_plan* plan, int64_t spins);
 
+/*
+ * fa_lp_plan_set_table_limit -- the largest qm K^T table (bytes) an NVFP4 plan holds at once.
+ *
+ * Passage: FlashInfer docs, flashinfer.diffusion_ops.minimax_h3_sm120_varlen_attention_nvfp4,
+ * description (Q is centred by its 128-row block mean qm and the qm K^T term is added back to the
+ * scores). The term is kept as a table of H x sum over segments of nb_s^2 x 128 floats
+ * (nb_s = ceil(L_s / 128)): quadratic in the segment length, 1.63 GB for one 30272-token segment
+ * at H = 56.
+ *
+ * When the whole table fits in `bytes`, fa_lp_quantize writes it and the forward reads it. When
+ * it does not, the plan holds two table slots of at most bytes / 2 each (one head's table at the
+ * least), and the forward builds the table of one group of heads into a slot right before that
+ * group's attention launch. The groups alternate between two internal streams; both start after
+ * the work already queued on the caller's stream, and the caller's stream then waits for both.
+ * Outputs and LSE are bit-identical either way. bytes = 0 restores the library default (4 GB:
+ * the whole table up to one segment of about 49.5k tokens at H = 56).
+ *
+ * The call re-lays the plan's workspace, so the plan must be quantized again. Plans are shared
+ * between identical fa_lp_plan_create calls, and the limit applies to every holder; no kernel of
+ * the plan may be running. No effect on FP8 plans. While a plan holds the ring,
+ * fa_lp_get_quantized(FA_LP_QMK_TABLE) returns UNSUPPORTED.
+ * Errors: INVALID_ARG (NULL plan), CUDA (releasing the plan's device tables failed).
+ */
+FA_LP_API int fa_lp_plan_set_table_limit(fa_lp_plan* plan, size_t bytes);
+
+/* The NVFP4 table layout of a plan: heads per slot, slots (1: the whole table, written by
+ * fa_lp_quantize; 2: the ring filled by the forward) and bytes per slot; zeros for FP8 plans.
+ * Any output pointer may be NULL. Errors: INVALID_ARG (NULL plan). */
+FA_LP_API int fa_lp_plan_table_layout(const fa_lp_plan* plan, int* heads_per_slot, int* slots,
+                                      size_t* slot_bytes);
+
 /* Free the workspace of `device` (stream-ordered on `stream`). Plans stay valid; the next
  * quantize allocates again. */
 FA_LP_API int fa_lp_release_workspace(int device, void* stream);

@@ -11,7 +11,8 @@
 // What one CTA computes (readings r5 with tau = 0, r9, r11, r12): for the two 128-row query tiles
 // Q0, Q1 of one (segment, head), over 64-key sub-tiles u from the segment start,
 //   s''(i, j)  = (deq(Qc_i) . deq(Kc_j) + Tq_t(j)) c,  Tq_t(j) = qm_t . deq(Kc_j) (the table
-//                qmk_nvfp4.cu writes during quantization, added to S by a TF32 MMA),
+//                qmk_nvfp4.cu writes, during quantization or right before the launch of a
+//                group of heads, added to S by a TF32 MMA),
 //                with c = softmax_scale log2(e)            (log2 units)
 //   m_i        = running row maximum of s'' (exact: it moves whenever a sub-tile exceeds it)
 //   P'(i, j)   = 2^(s'' - m_i + log2 2688)                  (= 2688 exp(S' - m) of the pages)
@@ -131,8 +132,9 @@ struct Nvfp4Args {
   const uint8_t* q_sf;     // [H][Tp][8]
   const uint8_t* k_sf;     // [H][Tp][8]
   const uint8_t* v_sf;     // [H][Tp/128][128][8]
-  const float* qmk;        // qm K^T table: segment s at c_off[s], [H][nb_s][128 nb_s]
+  const float* qmk;        // qm K^T table slot: segment s at c_off[s], [h - tbl_h0][nb_s][128 nb_s]
   const int64_t* c_off;
+  int tbl_h0;              // first head of the slot
   const float* q_km;       // [H][Tp]: q . km per query row
   __nv_bfloat16* out;
   int64_t ost, osh;
@@ -233,7 +235,7 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
   }
   // rows of the qm K^T table of this (segment, head) for the CTA's query tiles
   const int64_t lp = int64_t(sg.nblk) * kTile;
-  const float* tab = a.qmk + a.c_off[wi.seg] + (h * sg.nblk + wi.qt0) * lp;
+  const float* tab = a.qmk + a.c_off[wi.seg] + ((h - a.tbl_h0) * sg.nblk + wi.qt0) * lp;
   int issued = 0;
   for (int j = 0; j < n_kv; ++j) {
     const int st = j % kStages;
@@ -658,8 +660,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
-                           float* lse, int64_t lse_sh, cudaStream_t stream) {
+int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, int g, void* out, int64_t ost,
+                           int64_t osh, float* lse, int64_t lse_sh, cudaStream_t stream) {
+  const int w0 = p.tbl_work_off[g], nw = p.tbl_work_off[g + 1] - w0;
+  if (nw <= 0) return FA_LP_OK;
   static std::atomic<uint64_t> smem_set{0};
   if (set_smem_limit_once(reinterpret_cast<const void*>(attn_nvfp4_kernel), int(kSmemBytes), p.device,
                           smem_set) != FA_LP_OK)
@@ -678,12 +682,13 @@ int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t 
   if (st != FA_LP_OK) return st;
   Nvfp4Args a;
   a.segs = p.d_segs;
-  a.work = p.d_work;
+  a.work = p.d_work + w0;
   a.q_sf = ws + p.ws.q_sf;
   a.k_sf = ws + p.ws.k_sf;
   a.v_sf = ws + p.ws.v_sf;
-  a.qmk = reinterpret_cast<const float*>(ws + p.ws.qmk);
+  a.qmk = reinterpret_cast<const float*>(ws + p.ws.qmk) + size_t(g % p.tbl_slots) * p.tbl_slot_floats;
   a.c_off = p.d_coff;
+  a.tbl_h0 = g * p.tbl_hg;
   a.q_km = reinterpret_cast<const float*>(ws + p.ws.q_km);
   a.lse = lse;
   a.lse_sh = lse_sh;
@@ -697,7 +702,7 @@ int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t 
   a.w.abort_word = p.d_err + 1;
   a.w.gen = next_launch_generation();
   a.w.spin_limit = p.spin_limit;
-  attn_nvfp4_kernel<<<unsigned(p.work.size()), kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
+  attn_nvfp4_kernel<<<unsigned(nw), kThreads, kSmemBytes, stream>>>(tq, tk, tv, a);
   return cuda_status(cudaGetLastError());
 }
 

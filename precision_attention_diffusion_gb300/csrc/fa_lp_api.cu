@@ -235,6 +235,66 @@ std::vector<int> host_schedule(const fa_lp_plan& p, int heads_per_chunk) {
   return out;
 }
 
+// Streams and events of the NVFP4 table ring (device already current).
+int table_ring_release(fa_lp_plan* p) {
+  int st = FA_LP_OK;
+  for (int i = 0; i < 2; ++i) {
+    if (p->tbl_stream[i]) {
+      if (cudaStreamSynchronize(p->tbl_stream[i]) != cudaSuccess) st = FA_LP_ERR_CUDA;
+      cudaStreamDestroy(p->tbl_stream[i]);
+      p->tbl_stream[i] = nullptr;
+    }
+    if (p->tbl_join[i]) cudaEventDestroy(p->tbl_join[i]);
+    p->tbl_join[i] = nullptr;
+  }
+  if (p->tbl_fork) cudaEventDestroy(p->tbl_fork);
+  p->tbl_fork = nullptr;
+  if (st != FA_LP_OK) cudaGetLastError();
+  return st;
+}
+
+// NVFP4 forward with the qm K^T table held as a ring of two head-group slots. Group g's table
+// build and attention launch go to internal stream g % 2: a slot is rewritten only after the
+// attention launch that read it (stream order), and one stream's table build and attention run
+// beside the other stream's attention. Both streams start after the work already queued on
+// `stream`, and `stream` continues after both.
+int nvfp4_ring_forward(fa_lp_plan* p, uint8_t* base, void* out, int64_t ost, int64_t osh,
+                       float* lse, int64_t lse_sh, cudaStream_t stream) {
+  if (!p->tbl_fork) {
+    bool ok = cudaEventCreateWithFlags(&p->tbl_fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 2 && ok; ++i)
+      ok = cudaStreamCreateWithFlags(&p->tbl_stream[i], cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&p->tbl_join[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      table_ring_release(p);
+      return FA_LP_ERR_CUDA;
+    }
+  }
+  if (cudaEventRecord(p->tbl_fork, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(p->tbl_stream[0], p->tbl_fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(p->tbl_stream[1], p->tbl_fork, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_LP_ERR_CUDA;
+  }
+  const int ng = int(p->tbl_work_off.size()) - 1;
+  int st = FA_LP_OK;
+  for (int g = 0; g < ng && st == FA_LP_OK; ++g) {
+    cudaStream_t sg = p->tbl_stream[g & 1];
+    st = falp::launch_nvfp4_qmk(*p, base, g, sg);
+    if (st == FA_LP_OK)
+      st = falp::launch_nvfp4_attention(*p, base, g, out, ost, osh, lse, lse_sh, sg);
+  }
+  // joined after a failed launch as well, so that `stream` never runs ahead of queued work
+  for (int i = 0; i < 2; ++i)
+    if (cudaEventRecord(p->tbl_join[i], p->tbl_stream[i]) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, p->tbl_join[i], 0) != cudaSuccess) {
+      cudaGetLastError();
+      st = FA_LP_ERR_CUDA;
+    }
+  return st;
+}
+
 // Free the pipeline's device buffer, streams and events (device already current); hands the
 // sub-plans to the caller, which releases them outside the plan-cache lock.
 int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[4]) {
@@ -255,6 +315,26 @@ int host_pipe_release(fa_lp_plan* p, fa_lp_plan* subs[4]) {
   if (st != FA_LP_OK) cudaGetLastError();
   return st;
 }
+
+// Heads per block of the work list (and per block-sparse tile group).
+constexpr int kHeadGroup = 8;
+// Largest NVFP4 qm K^T table a plan holds whole (bytes); a larger one is held as a ring of two
+// head-group slots that the forward fills group by group. Holding the whole table keeps its build
+// in the quantize, where it runs alone at full width (0.61 ms at S = 30272, H = 56, against
+// 0.84 ms spread over the forward's head groups); above 4 GB (one segment of about 49.5k tokens at
+// H = 56) the ring bounds it.
+constexpr size_t kTableLimitDefault = size_t(4) << 30;
+
+// Segments, longest first (ties in index order).
+std::vector<int> lpt_order(const fa_lp_plan* p) {
+  std::vector<int> order(p->nseg);
+  for (int s = 0; s < p->nseg; ++s) order[s] = s;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return p->segs[a].len > p->segs[b].len; });
+  return order;
+}
+
+void layout_work_and_workspace(fa_lp_plan* p);
 
 void build_plan(fa_lp_plan* p) {
   const int ns = p->nseg;
@@ -283,23 +363,7 @@ void build_plan(fa_lp_plan* p) {
     p->sp_nw_max = std::max<int>(p->sp_nw_max, int((nkb + 31) / 32));
   }
 
-  // Work list: longest segment first (LPT); within a segment, blocks of kHeadGroup heads, and in
-  // a block the query-tile pairs of its heads interleaved. The CTAs resident at one time then
-  // read the K/V of a few heads (a working set that stays in L2) while no single K/V line is
-  // requested by all of them at once.
-  constexpr int kHeadGroup = 8;
-  std::vector<int> order(ns);
-  for (int s = 0; s < ns; ++s) order[s] = s;
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int a, int b) { return p->segs[a].len > p->segs[b].len; });
-  for (int s : order) {
-    const int nb = p->segs[s].nblk;
-    if (nb == 0) continue;
-    for (int h0 = 0; h0 < p->heads; h0 += kHeadGroup)
-      for (int t = 0; t < nb; t += 2)
-        for (int h = h0; h < std::min(p->heads, h0 + kHeadGroup); ++h)
-          p->work.push_back(WorkItem{s, h, t, std::min(2, nb - t)});
-  }
+  std::vector<int> order = lpt_order(p);
   // Block-sparse forward: the same segment / head-group order; a group's tiles are paired on the
   // device once their list lengths are known.
   int32_t slot = 0;
@@ -315,9 +379,57 @@ void build_plan(fa_lp_plan* p) {
       slot += nt;
     }
   }
+  layout_work_and_workspace(p);
+}
+
+// Table groups of the NVFP4 qm K^T table (heads per group, slots), the work list ordered by
+// group, and the workspace layout. Re-run when the plan's table limit changes.
+void layout_work_and_workspace(fa_lp_plan* p) {
+  const int ns = p->nseg;
+  const std::vector<int> order = lpt_order(p);
+  // one head's table, in floats, over all segments
+  size_t head_floats = 0;
+  for (int s = 0; s < ns; ++s)
+    head_floats += size_t(p->segs[s].nblk) * size_t(p->segs[s].nblk) * 128;
+  p->tbl_hg = p->heads;
+  p->tbl_slots = 1;
+  if (!falp::is_fp8(*p) && head_floats > 0) {
+    const size_t limit = p->tbl_limit ? p->tbl_limit : kTableLimitDefault;
+    if (size_t(p->heads) * head_floats * 4 > limit) {
+      // a ring of two slots of at most limit / 2 bytes each (one head's table at the least);
+      // groups of equal size
+      const size_t fit = std::max<size_t>(1, (limit / 2) / (head_floats * 4));
+      const int ng = int((size_t(p->heads) + fit - 1) / fit);
+      p->tbl_hg = (p->heads + ng - 1) / ng;
+      p->tbl_slots = 2;
+    }
+  }
+  p->tbl_slot_floats = size_t(p->tbl_hg) * head_floats;
+
+  // Work list, per table group (one group of all heads unless the table is held as a ring):
+  // longest segment first (LPT); within a segment, blocks of kHeadGroup heads, and in a block
+  // the query-tile pairs of its heads interleaved. The CTAs resident at one time then read the
+  // K/V of a few heads (a working set that stays in L2) while no single K/V line is requested by
+  // all of them at once.
+  p->work.clear();
+  p->tbl_work_off.clear();
+  for (int g0 = 0; g0 < p->heads; g0 += p->tbl_hg) {
+    const int g1 = std::min(p->heads, g0 + p->tbl_hg);
+    p->tbl_work_off.push_back(int32_t(p->work.size()));
+    for (int s : order) {
+      const int nb = p->segs[s].nblk;
+      if (nb == 0) continue;
+      for (int h0 = g0; h0 < g1; h0 += kHeadGroup)
+        for (int t = 0; t < nb; t += 2)
+          for (int h = h0; h < std::min(g1, h0 + kHeadGroup); ++h)
+            p->work.push_back(WorkItem{s, h, t, std::min(2, nb - t)});
+    }
+  }
+  p->tbl_work_off.push_back(int32_t(p->work.size()));
 
   // Workspace layout.
   const size_t H = size_t(p->heads), Tp = size_t(p->tpad);
+  p->ws = falp::WsLayout();
   falp::WsLayout& w = p->ws;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -343,14 +455,18 @@ void build_plan(fa_lp_plan* p) {
     w.k_mean = take(size_t(p->nseg) * H * 128 * 4);
     w.k_chunk = take(p->blocks.size() * H * 128 * 8);
     w.q_km = take(H * Tp * 4);
-    // qm K^T table: segment s holds [H][nb_s][128 nb_s] floats (quadratic in the segment length:
-    // 1.6 GB for one 30272-token segment at H = 56)
+    // qm K^T table slot: segment s holds [tbl_hg][nb_s][128 nb_s] floats (quadratic in the
+    // segment length: 1.6 GB for one 30272-token segment at H = 56 when one slot holds every
+    // head)
     p->c_off.assign(ns, 0);
+    p->qmk_items.clear();
     size_t floats = 0;
-    // N tiles per table CTA: one run r in [4, 16] for every segment, since the table kernel
-    // launches all segments' tiles in one grid: the r whose CTAs (sum over segments of M tiles x
-    // runs, times heads) fill the GPU's waves best, i.e. the least ceil(CTAs / SMs) * r (a CTA's
-    // time grows with its run); ties go to the longer run
+    // N tiles per table CTA: one run r for every segment, since the table kernel launches all
+    // segments' tiles of a head group in one grid: the r whose CTAs (sum over segments of M tiles
+    // x runs, times the group's heads) fill the GPU's waves best, i.e. the least
+    // ceil(CTAs / SMs) * r (a CTA's time grows with its run); ties go to the longer run. r is at
+    // least 4 when one launch covers every head (the per-CTA set-up then stays small against
+    // its run), at least 1 for a head group
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
         sms <= 0) {
@@ -361,27 +477,28 @@ void build_plan(fa_lp_plan* p) {
     auto nm_of = [&](int s) { return (int64_t(p->segs[s].nblk) + 127) / 128; };
     int run = falp::kQmkTilesPer;
     double best = 1e300;
-    for (int r = 4; r <= 16; ++r) {
+    for (int r = p->tbl_slots == 1 ? 4 : 1; r <= 16; ++r) {
       double ctas = 0.0;
       for (int s = 0; s < ns; ++s)
-        ctas += double(nm_of(s)) * double((ntiles_of(s) + r - 1) / r) * double(H);
+        ctas += double(nm_of(s)) * double((ntiles_of(s) + r - 1) / r) * double(p->tbl_hg);
       const double cost = std::ceil(ctas / sms) * r;
       if (cost < best - 1e-9 || (std::fabs(cost - best) <= 1e-9 && r > run)) {
         best = cost;
         run = r;
       }
     }
+    p->qmk_run = run;
     for (int s = 0; s < ns; ++s) {
       const int64_t nb = p->segs[s].nblk;
       p->c_off[s] = int64_t(floats);
-      floats += size_t(H) * size_t(nb) * size_t(nb) * 128;
+      floats += size_t(p->tbl_hg) * size_t(nb) * size_t(nb) * 128;
       const int64_t ntiles = ntiles_of(s);
       for (int64_t mt = 0; mt * 128 < nb; ++mt)
         for (int64_t nt = 0; nt < ntiles; nt += run)
           p->qmk_items.push_back(falp::QmkItem{
               s, int32_t(mt), int32_t(nt), int32_t(std::min<int64_t>(run, ntiles - nt))});
     }
-    w.qmk = take(floats * 4);
+    w.qmk = take(floats * 4 * size_t(p->tbl_slots));
   }
   w.total = off;
 }
@@ -520,11 +637,12 @@ int fa_lp_plan_destroy(fa_lp_plan* p) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (--p->refcount > 0) return FA_LP_OK;
     g_plans.erase(key_of(*p));
-    if (p->dmeta || p->host.buf || p->host.s_in || p->sp_buf) {
+    if (p->dmeta || p->host.buf || p->host.s_in || p->sp_buf || p->tbl_fork) {
       int cur = -1;
       cudaGetDevice(&cur);
       if (cur != p->device) cudaSetDevice(p->device);
       st = host_pipe_release(p, subs);
+      if (table_ring_release(p) != FA_LP_OK) st = FA_LP_ERR_CUDA;
       if (p->sp_buf &&
           (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->sp_buf) != cudaSuccess)) {
         cudaGetLastError();
@@ -569,6 +687,38 @@ int fa_lp_plan_row_offsets(const fa_lp_plan* p, int64_t* row_offsets) {
 int fa_lp_plan_set_wait_limit(fa_lp_plan* p, int64_t spins) {
   if (!p || spins < 1) return FA_LP_ERR_INVALID_ARG;
   p->spin_limit = spins;
+  return FA_LP_OK;
+}
+
+int fa_lp_plan_set_table_limit(fa_lp_plan* p, size_t bytes) {
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (falp::is_fp8(*p) || bytes == p->tbl_limit) return FA_LP_OK;
+  if (p->dmeta) {  // the device copy of the work list is rebuilt on next use
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    const bool ok = cudaDeviceSynchronize() == cudaSuccess && cudaFree(p->dmeta) == cudaSuccess;
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    p->dmeta = nullptr;
+    if (!ok) {
+      cudaGetLastError();
+      return FA_LP_ERR_CUDA;
+    }
+  }
+  p->tbl_limit = bytes;
+  layout_work_and_workspace(p);
+  p->quantized = false;
+  return FA_LP_OK;
+}
+
+int fa_lp_plan_table_layout(const fa_lp_plan* p, int* heads_per_slot, int* slots,
+                            size_t* slot_bytes) {
+  if (!p) return FA_LP_ERR_INVALID_ARG;
+  const bool fp8 = falp::is_fp8(*p);
+  if (heads_per_slot) *heads_per_slot = fp8 ? 0 : p->tbl_hg;
+  if (slots) *slots = fp8 ? 0 : p->tbl_slots;
+  if (slot_bytes) *slot_bytes = fp8 ? 0 : p->tbl_slot_floats * 4;
   return FA_LP_OK;
 }
 
@@ -622,11 +772,12 @@ int fa_lp_forward_varlen_lse(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void*
     if ((st = workspace_of_plan(p, &base)) != FA_LP_OK) return st;
   }
   if (p->work.empty()) return FA_LP_OK;
-  return falp::is_fp8(*p)
-             ? falp::launch_fp8_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, lse,
-                                          lse_stride_head, stream)
-             : falp::launch_nvfp4_attention(*p, static_cast<uint8_t*>(base), out, ost, osh, lse,
-                                            lse_stride_head, stream);
+  uint8_t* ws = static_cast<uint8_t*>(base);
+  if (falp::is_fp8(*p))
+    return falp::launch_fp8_attention(*p, ws, out, ost, osh, lse, lse_stride_head, stream);
+  if (p->tbl_slots == 2)
+    return nvfp4_ring_forward(p, ws, out, ost, osh, lse, lse_stride_head, stream);
+  return falp::launch_nvfp4_attention(*p, ws, 0, out, ost, osh, lse, lse_stride_head, stream);
 }
 
 int fa_lp_forward_varlen(fa_lp_plan* p, const int32_t* cu_seqlens_dev, void* out, int64_t ost,
@@ -947,6 +1098,7 @@ int fa_lp_get_quantized(const fa_lp_plan* p, int which, fa_lp_array_desc* d) {
     case FA_LP_K_MEANS: return set(p->ws.k_mean, p->nseg, H, 128, 4);
     case FA_LP_Q_KM: return set(p->ws.q_km, 1, H, Tp, 4);
     case FA_LP_QMK_TABLE: {
+      if (p->tbl_slots != 1) return FA_LP_ERR_UNSUPPORTED;  // built per head group in the forward
       int64_t n = 0;
       for (const auto& sg : p->segs) n += int64_t(H) * sg.nblk * sg.nblk * 128;
       return set(p->ws.qmk, 1, 1, n, 4);

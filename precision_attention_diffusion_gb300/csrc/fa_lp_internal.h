@@ -109,6 +109,20 @@ struct fa_lp_plan {
   std::vector<falp::WorkItem> work;
   std::vector<falp::QmkItem> qmk_items;          // NVFP4 qm K^T table tiles
   std::vector<int64_t> c_off;                    // NVFP4: float offset of each segment's table
+                                                 // inside a table slot
+  // NVFP4 qm K^T table held per group of tbl_hg heads. tbl_slots == 1: one slot holds every
+  // head's table (tbl_hg = heads), written by the quantize. tbl_slots == 2: a ring of two slots;
+  // the forward builds group g's table into slot g % 2 right before group g's attention launch.
+  // The work list is ordered by group; group g's items are [tbl_work_off[g], tbl_work_off[g+1]).
+  int tbl_hg = 0;
+  int tbl_slots = 1;
+  size_t tbl_slot_floats = 0;
+  size_t tbl_limit = 0;                          // bytes; 0 = the library default
+  std::vector<int32_t> tbl_work_off;
+  int qmk_run = 0;                               // N tiles per table CTA
+  cudaStream_t tbl_stream[2] = {nullptr, nullptr};  // ring forward: one stream per slot
+  cudaEvent_t tbl_fork = nullptr;
+  cudaEvent_t tbl_join[2] = {nullptr, nullptr};
   falp::WsLayout ws;
   // block-sparse forward (FP8 plans): 64-row query blocks
   int64_t sp_G = 0;                   // query blocks over the packed batch
@@ -156,12 +170,14 @@ int launch_fp8_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t os
 int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64_t qst,
                           int64_t qsh, const void* k, int64_t kst, int64_t ksh, const void* v,
                           int64_t vst, int64_t vsh, cudaStream_t stream);
-int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, void* out, int64_t ost, int64_t osh,
-                           float* lse, int64_t lse_sh, cudaStream_t stream);
+// NVFP4 attention over table group g's work items, reading the table from slot g % tbl_slots.
+int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, int g, void* out, int64_t ost,
+                           int64_t osh, float* lse, int64_t lse_sh, cudaStream_t stream);
 int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* block_offsets,
                       const int32_t* block_indices, int64_t num_indices, void* out, int64_t ost,
                       int64_t osh, float* lse, int64_t lse_sh, cudaStream_t stream);
-int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, cudaStream_t stream);
+// The qm K^T table of table group g's heads into slot g % tbl_slots.
+int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, int g, cudaStream_t stream);
 int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
 
 // Distinct positive id per kernel launch (device-side abort words compare against it).

@@ -8,8 +8,9 @@
 //     Tq[s][h][b][j] = qm_b . deq(Kc_j)                                  (raw units of S)
 //
 // for the segment's query blocks b and its padded keys j (zero codes past the segment). The
-// attention kernel adds Tq to its scores. Layout: segment s at float offset c_off[s], then
-// [H][nb_s][128 nb_s].
+// attention kernel adds Tq to its scores. One launch writes the tables of a group of heads
+// [h0, h0 + gridDim.y) into one table slot: segment s at float offset c_off[s] of the slot, then
+// [head - h0][nb_s][128 nb_s].
 //
 // One CTA = one (segment, 128-block M tile, head) and a run of up to 16 256-key N tiles (the plan
 // picks the run per segment so that the CTAs fill whole waves; A is built once per CTA; B, the
@@ -19,6 +20,8 @@
 // 3 x 128 channels) accumulates in FP32 in tensor memory. B tiles and accumulators are double
 // buffered: the MMAs of tile n run while the 256 threads store tile n - 1 (the table's HBM writes
 // bound the kernel) and then build the B tile of n + 1.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -101,13 +104,13 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
     const QmkItem* __restrict__ items, const SegInfo* __restrict__ segs,
     const int64_t* __restrict__ c_off, const float* __restrict__ qmean,
     const uint8_t* __restrict__ kcodes, const uint8_t* __restrict__ ksf, int64_t Tp,
-    int64_t nblk, int H, float* __restrict__ table, int* err) {
+    int64_t nblk, int h0, float* __restrict__ table, int* err) {
   extern __shared__ uint8_t smem_raw[];
   QmkSmem& S = *reinterpret_cast<QmkSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
   const QmkItem it = items[blockIdx.x];
-  const int h = blockIdx.y;
+  const int hs = blockIdx.y, h = h0 + hs;  // head inside the slot, head
   const SegInfo sg = segs[it.seg];
   const int nb = sg.nblk, lp = sg.nblk * kTile;
   const int64_t krow0 = int64_t(h) * Tp + sg.row0;
@@ -199,7 +202,8 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
     const int row0 = it.mt * 128 + (warp & 3) * 32;
     float* stg = reinterpret_cast<float*>(&S.b[n & 1][0][0]) + warp * (32 * 33);
     const uint32_t taddr = tmem + 256u * uint32_t(n & 1) + uint32_t(k0) + (uint32_t((warp & 3) * 32) << 16);
-    const float* base = table + c_off[it.seg] + (int64_t(h) * nb + row0) * lp + int64_t(nt) * kNKeys + k0;
+    const float* base =
+        table + c_off[it.seg] + (int64_t(hs) * nb + row0) * lp + int64_t(nt) * kNKeys + k0;
 #pragma unroll 1
     for (int c32 = 0; c32 < 128; c32 += 32) {
       uint32_t r[32];
@@ -260,17 +264,18 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
 
 }  // namespace
 
-int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, cudaStream_t stream) {
-  if (p.qmk_items.empty()) return FA_LP_OK;
+int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, int g, cudaStream_t stream) {
+  const int h0 = g * p.tbl_hg, nh = std::min(p.tbl_hg, p.heads - h0);
+  if (p.qmk_items.empty() || nh <= 0) return FA_LP_OK;
   static std::atomic<uint64_t> smem_set{0};
   if (set_smem_limit_once(reinterpret_cast<const void*>(nvfp4_qmk_kernel), int(kQmkSmemBytes), p.device,
                           smem_set) != FA_LP_OK)
     return FA_LP_ERR_CUDA;
-  nvfp4_qmk_kernel<<<dim3(unsigned(p.qmk_items.size()), unsigned(p.heads)), kQmkThreads,
-                     kQmkSmemBytes, stream>>>(
-      p.d_qmk, p.d_segs, p.d_coff, reinterpret_cast<const float*>(ws + p.ws.q_mean),
-      ws + p.ws.k_codes, ws + p.ws.k_sf, p.tpad, int64_t(p.blocks.size()), p.heads,
-      reinterpret_cast<float*>(ws + p.ws.qmk), p.d_err);
+  float* slot = reinterpret_cast<float*>(ws + p.ws.qmk) + size_t(g % p.tbl_slots) * p.tbl_slot_floats;
+  nvfp4_qmk_kernel<<<dim3(unsigned(p.qmk_items.size()), unsigned(nh)), kQmkThreads, kQmkSmemBytes,
+                     stream>>>(p.d_qmk, p.d_segs, p.d_coff,
+                               reinterpret_cast<const float*>(ws + p.ws.q_mean), ws + p.ws.k_codes,
+                               ws + p.ws.k_sf, p.tpad, int64_t(p.blocks.size()), h0, slot, p.d_err);
   return cuda_status(cudaGetLastError());
 }
 

@@ -298,7 +298,9 @@ int launch_nvfp4_quantize(const fa_lp_plan& p, uint8_t* ws, const void* q, int64
       vb, vst, vsh, p.d_blocks, H, p.tpad, ws + p.ws.v_codes, ws + p.ws.v_sf);
   const int st = cuda_status(cudaGetLastError());
   if (st != FA_LP_OK) return st;
-  return launch_nvfp4_qmk(p, ws, stream);  // the qm K^T table from the means and K codes
+  // the qm K^T table from the means and K codes, when the plan holds all of it (a ring of
+  // head-group slots is filled by the forward instead)
+  return p.tbl_slots == 1 ? launch_nvfp4_qmk(p, ws, 0, stream) : FA_LP_OK;
 }
 
 }  // namespace falp

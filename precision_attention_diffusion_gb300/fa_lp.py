@@ -38,7 +38,7 @@ EXPORTS = (
     "fa_lp_get_last_error", "fa_lp_plan_set_wait_limit", "fa_lp_release_workspace",
     "fa_lp_encode", "fa_lp_fp8_descale_noalloc", "fa_lp_forward_varlen_lse",
     "fa_lp_attention_host", "fa_lp_forward_sparse", "fa_lp_sparse_query_blocks",
-    "fa_lp_attention_sparse_host",
+    "fa_lp_attention_sparse_host", "fa_lp_plan_set_table_limit", "fa_lp_plan_table_layout",
 )
 
 _lib = None
@@ -98,6 +98,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.fa_lp_copy_quantized.argtypes = [P, i32, P, sz, P]
         L.fa_lp_get_last_error.argtypes = [P, ctypes.POINTER(i32)]
         L.fa_lp_plan_set_wait_limit.argtypes = [P, i64]
+        L.fa_lp_plan_set_table_limit.argtypes = [P, sz]
+        L.fa_lp_plan_table_layout.argtypes = [P, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                              ctypes.POINTER(sz)]
         L.fa_lp_release_workspace.argtypes = [i32, P]
         L.fa_lp_encode.argtypes = [i32, P, i64, P, P]
         L.fa_lp_fp8_descale_noalloc.argtypes = [P, i64, i64, P, i64, i64, P, i64, i64, i64, i32, P,
@@ -186,6 +189,17 @@ class Plan:
 
     def set_wait_limit(self, spins: int):
         _check(load().fa_lp_plan_set_wait_limit(self._h, int(spins)), "fa_lp_plan_set_wait_limit")
+
+    def set_table_limit(self, nbytes: int):
+        """NVFP4: the largest qm K^T table held at once (0: the library default)."""
+        _check(load().fa_lp_plan_set_table_limit(self._h, int(nbytes)),
+               "fa_lp_plan_set_table_limit")
+
+    def table_layout(self):
+        hg, ns, sb = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+        _check(load().fa_lp_plan_table_layout(self._h, ctypes.byref(hg), ctypes.byref(ns),
+                                              ctypes.byref(sb)), "fa_lp_plan_table_layout")
+        return dict(heads_per_slot=hg.value, slots=ns.value, slot_bytes=sb.value)
 
     def last_error(self) -> int:
         v = ctypes.c_int()

@@ -8,7 +8,7 @@
 #include "../../precision_attention_diffusion_gb300/csrc/quant_nvfp4.cu"
 
 // the included file's quantize launcher refers to the table pass; this program never calls it
-int falp::launch_nvfp4_qmk(const fa_lp_plan&, uint8_t*, cudaStream_t) { return FA_LP_OK; }
+int falp::launch_nvfp4_qmk(const fa_lp_plan&, uint8_t*, int, cudaStream_t) { return FA_LP_OK; }
 
 namespace falp {
 namespace {

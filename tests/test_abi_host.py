@@ -151,6 +151,54 @@ def test_nvfp4_workspace_holds_the_qmk_table(lib):
     assert ws_of([0, 0, 30272], 56) <= one + 56 * 128 * 4 + 2048
 
 
+def test_nvfp4_table_ring_bounds_the_workspace(lib):
+    """A table limit below the whole qm K^T table makes the plan hold two slots of whole head
+    groups (equal groups, one head's table at the least); the work list keeps every item; the
+    limit 0 restores the whole table. At S = 30272, H = 56 a 64 MB limit puts the workspace under
+    0.5 GB (one head's table is 237^2 x 128 floats = 29 MB)."""
+    def layout(h):
+        hg, ns, sb = ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+        assert lib.fa_lp_plan_table_layout(h, ctypes.byref(hg), ctypes.byref(ns),
+                                           ctypes.byref(sb)) == 0
+        tp, wi, ws = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+        assert lib.fa_lp_plan_info(h, ctypes.byref(tp), ctypes.byref(wi), ctypes.byref(ws)) == 0
+        return hg.value, ns.value, sb.value, wi.value, ws.value
+
+    head = 237 * 237 * 128 * 4
+    st, h = _create(lib, [0, 30272], heads=56, mode=1)
+    assert st == 0
+    try:
+        hg, ns, sb, wi, ws_full = layout(h)
+        assert (hg, ns, sb) == (56, 1, 56 * head)
+        assert lib.fa_lp_plan_set_table_limit(h, 64 << 20) == 0
+        hg, ns, sb, wi2, ws = layout(h)
+        assert (hg, ns, sb) == (1, 2, head) and wi2 == wi
+        assert ws < 500_000_000 and ws_full - ws == 56 * head - 2 * head
+        # 200 MB: three heads per 100 MB slot, 19 groups -> equal groups of 3 (the last of 2)
+        assert lib.fa_lp_plan_set_table_limit(h, 200 << 20) == 0
+        assert layout(h)[:3] == (3, 2, 3 * head)
+        assert lib.fa_lp_plan_set_table_limit(h, 0) == 0
+        assert layout(h) == (56, 1, 56 * head, wi, ws_full)
+    finally:
+        assert lib.fa_lp_plan_destroy(h) == 0
+    # the default limit (4 GB) holds a 49456-token segment's table whole and rings a 50000-token
+    # one: 391^2 x 512 B = 78 MB per head, 27 heads per 2 GB slot -> 3 equal groups of 19
+    for L, want in ((49456, (56, 1)), (50000, (19, 2))):
+        st, h = _create(lib, [0, L], heads=56, mode=1)
+        assert st == 0
+        try:
+            assert layout(h)[:2] == want
+        finally:
+            assert lib.fa_lp_plan_destroy(h) == 0
+    # FP8 plans hold no table: the limit has no effect
+    st, h = _create(lib, [0, 4096], heads=4, mode=0)
+    try:
+        assert lib.fa_lp_plan_set_table_limit(h, 1) == 0
+        assert layout(h)[:3] == (0, 0, 0)
+    finally:
+        assert lib.fa_lp_plan_destroy(h) == 0
+
+
 def test_batched_front_end_packs_without_copies():
     """[batch, seq, heads, 128] views become the packed token axis only when no copy is needed."""
     import torch

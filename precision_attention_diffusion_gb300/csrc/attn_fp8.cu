@@ -71,8 +71,7 @@ struct Smem {
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
   uint64_t bar_q;
-  uint64_t bar_k[kStages];
-  uint64_t bar_v[kStages];
+  uint64_t bar_ld[kStages];  // K and V^T tiles of the stage landed
   uint64_t bar_free[kStages];
   uint64_t bar_s[2][2];  // [t][u & 1]: S_t(u) written (MMA commit)
   uint64_t bar_p[2][2];  // [t][u & 1]: P_t(u) written, O rescaled (128 arrivals)
@@ -176,18 +175,16 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
         !wait_hinted(smem_u32(&S.bar_free[st]), ((j / kStages) - 1) & 1, S, a, kRoleProducer))
       break;
     const int row = sg.row0 + j * kTile;
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[st]), kTileBytes);
-    tma_load_3d_elect(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_k[st]), 0, row, wi.head);
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[st]), kTileBytes);
-    tma_load_3d_elect(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_v[st]), row, 0, wi.head);
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_ld[st]), 2 * kTileBytes);
+    tma_load_3d_elect(smem_u32(S.k[st]), tm_k, smem_u32(&S.bar_ld[st]), 0, row, wi.head);
+    tma_load_3d_elect(smem_u32(S.v[st]), tm_v, smem_u32(&S.bar_ld[st]), row, 0, wi.head);
     issued = j + 1;
   }
   // No copy may still be landing in shared memory when the CTA exits.
   drain_phase(smem_u32(&S.bar_q), 0);
   for (int j = max(0, issued - kStages); j < issued; ++j) {
     const int st = j % kStages;
-    drain_phase(smem_u32(&S.bar_k[st]), (j / kStages) & 1);
-    drain_phase(smem_u32(&S.bar_v[st]), (j / kStages) & 1);
+    drain_phase(smem_u32(&S.bar_ld[st]), (j / kStages) & 1);
   }
 }
 
@@ -214,39 +211,39 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const Wor
   };
   // O_t += P_t(u) V(u): keys [64h, 64h + 64) are bytes [64h, 64h + 64) of each V^T row; P from
   // the first 16 columns of S buffer h
+  // the group also releases the stage after the tile's last use of it (h = 1, or the segment's
+  // last sub-tile)
   auto issue_pv = [&](int u) {
     const uint32_t j = uint32_t(u) >> 1, h = uint32_t(u) & 1;
     const uint64_t vb = dvv + (((j % kStages) * kTileBytes + h * kSub) >> 4);
     const uint32_t pa = tmem + col_s(t, h);
-    mma_f8f6f4_ts_k64_commit_elect(d_o, pa, vb, kIdescPV, u > 0 ? 1u : 0u,
-                                   smem_u32(&S.bar_o[t][h]));
+    const uint32_t release = (h == 1 || u + 1 == n_sub) ? 1u : 0u;
+    mma_f8f6f4_ts_k64_commit2_elect(d_o, pa, vb, kIdescPV, u > 0 ? 1u : 0u,
+                                    smem_u32(&S.bar_o[t][h]), release,
+                                    smem_u32(&S.bar_free[j % kStages]));
   };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return wait_hinted(smem_u32(bar), parity, S, a, kRoleMma);
   };
   do {
     if (!wait(&S.bar_q, 0)) break;
-    if (!wait(&S.bar_k[0], 0)) break;
+    if (!wait(&S.bar_ld[0], 0)) break;
     tc_fence_after();
     issue_s(0);
     if (n_sub > 1) issue_s(1);  // sub-tile 1 lies in key tile 0 as well
     bool ok = true;
     for (int u = 0; u < n_sub && ok; ++u) {
-      const int j = u >> 1, h = u & 1;
-      if (h == 0) {
-        ok = wait(&S.bar_v[j % kStages], (j / kStages) & 1);
-        if (!ok) break;
-      }
+      const int h = u & 1;
+      // the stage's V^T landed with its K, waited for before S of its first sub-tile
       ok = wait(&S.bar_p[t][h], (u >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
       issue_pv(u);
-      if (h == 1 || u + 1 == n_sub) mma_commit_elect(smem_u32(&S.bar_free[j % kStages]));
       const int u2 = u + 2;
       if (u2 < n_sub) {
         if ((u2 & 1) == 0) {  // sub-tile u+2 opens key tile j+1
           const int j2 = u2 >> 1;
-          ok = wait(&S.bar_k[j2 % kStages], (j2 / kStages) & 1);
+          ok = wait(&S.bar_ld[j2 % kStages], (j2 / kStages) & 1);
           if (!ok) break;
           tc_fence_after();
         }
@@ -395,8 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&S.bar_q), 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&S.bar_k[i]), 1);
-      mbar_init(smem_u32(&S.bar_v[i]), 1);
+      mbar_init(smem_u32(&S.bar_ld[i]), 1);
       mbar_init(smem_u32(&S.bar_free[i]), wi.nq);  // one commit per query tile
     }
     for (int t = 0; t < 2; ++t) {

@@ -66,8 +66,7 @@ struct Smem {
   uint8_t k[2][kSt][kKBytes];
   uint8_t v[2][kSt][kVBytes];
   uint64_t bar_q[2];
-  uint64_t bar_k[2][kSt];
-  uint64_t bar_v[2][kSt];
+  uint64_t bar_ld[2][kSt];  // K block and V^T block of the stage landed
   uint64_t bar_free[2][kSt];
   uint64_t bar_s[2][2];  // [t][u & 1]: S_t(u) written
   uint64_t bar_p[2][2];  // [t][u & 1]: P_t(u) written, O rescaled (256 arrivals)
@@ -264,17 +263,15 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
         !wait_hinted(smem_u32(&S.bar_free[t][st]), ((j / kSt) - 1) & 1, S, a, kRoleProducer))
       break;
     const int row = sg.row0 + kBlk * int(__ldg(ent + j) & kKbMask);
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_k[t][st]), kKBytes);
-    tma_load_3d_elect(smem_u32(S.k[t][st]), tm_k, smem_u32(&S.bar_k[t][st]), 0, row, tr.head);
-    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_v[t][st]), kVBytes);
-    tma_load_3d_elect(smem_u32(S.v[t][st]), tm_v, smem_u32(&S.bar_v[t][st]), row, 0, tr.head);
+    mbar_arrive_expect_tx_elect(smem_u32(&S.bar_ld[t][st]), kKBytes + kVBytes);
+    tma_load_3d_elect(smem_u32(S.k[t][st]), tm_k, smem_u32(&S.bar_ld[t][st]), 0, row, tr.head);
+    tma_load_3d_elect(smem_u32(S.v[t][st]), tm_v, smem_u32(&S.bar_ld[t][st]), row, 0, tr.head);
     issued = j + 1;
   }
   drain_phase(smem_u32(&S.bar_q[t]), 0);
   for (int j = max(0, issued - kSt); j < issued; ++j) {
     const int st = j % kSt;
-    drain_phase(smem_u32(&S.bar_k[t][st]), (j / kSt) & 1);
-    drain_phase(smem_u32(&S.bar_v[t][st]), (j / kSt) & 1);
+    drain_phase(smem_u32(&S.bar_ld[t][st]), (j / kSt) & 1);
   }
 }
 
@@ -289,37 +286,36 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const SpArgs& a, uint32_t tm
     mma_f8f6f4_ss_k128_commit_elect(tmem + col_s(t, u & 1), dq, kb, kIdescS,
                                     smem_u32(&S.bar_s[t][u & 1]));
   };
+  // the group also releases the block's stage (its K was read by S(u), issued earlier)
   auto issue_pv = [&](int u) {
     const uint64_t vb = dv + ((uint32_t(u % kSt) * kVBytes) >> 4);
-    mma_f8f6f4_ts_k64_commit_elect(d_o, tmem + col_s(t, u & 1), vb, kIdescPV, u > 0 ? 1u : 0u,
-                                   smem_u32(&S.bar_o[t][u & 1]));
+    mma_f8f6f4_ts_k64_commit2_elect(d_o, tmem + col_s(t, u & 1), vb, kIdescPV, u > 0 ? 1u : 0u,
+                                    smem_u32(&S.bar_o[t][u & 1]), 1u,
+                                    smem_u32(&S.bar_free[t][u % kSt]));
   };
   auto wait = [&](uint64_t* bar, uint32_t parity) {
     return wait_hinted(smem_u32(bar), parity, S, a, kRoleMma);
   };
   do {
     if (!wait(&S.bar_q[t], 0)) break;
-    if (!wait(&S.bar_k[t][0], 0)) break;
+    if (!wait(&S.bar_ld[t][0], 0)) break;
     tc_fence_after();
     issue_s(0);
     if (n > 1) {
-      if (!wait(&S.bar_k[t][1 % kSt], 0)) break;
+      if (!wait(&S.bar_ld[t][1 % kSt], 0)) break;
       tc_fence_after();
       issue_s(1);
     }
     bool ok = true;
     for (int u = 0; u < n && ok; ++u) {
-      const int st = u % kSt;
-      ok = wait(&S.bar_v[t][st], (u / kSt) & 1);
-      if (!ok) break;
+      // V(u) landed with K(u), waited for before S(u)
       ok = wait(&S.bar_p[t][u & 1], (u >> 1) & 1);
       if (!ok) break;
       tc_fence_after();
       issue_pv(u);
-      mma_commit_elect(smem_u32(&S.bar_free[t][st]));
       const int u2 = u + 2;
       if (u2 < n) {
-        ok = wait(&S.bar_k[t][u2 % kSt], (u2 / kSt) & 1);
+        ok = wait(&S.bar_ld[t][u2 % kSt], (u2 / kSt) & 1);
         if (!ok) break;
         tc_fence_after();
         issue_s(u2);
@@ -500,8 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&S.bar_q[t]), 1);
       for (int i = 0; i < kSt; ++i) {
-        mbar_init(smem_u32(&S.bar_k[t][i]), 1);
-        mbar_init(smem_u32(&S.bar_v[t][i]), 1);
+        mbar_init(smem_u32(&S.bar_ld[t][i]), 1);
         mbar_init(smem_u32(&S.bar_free[t][i]), 1);
       }
       for (int x = 0; x < 2; ++x) {

@@ -502,6 +502,26 @@ __device__ __forceinline__ void mma_f8f6f4_ts_k64_commit_elect(uint32_t d_tmem, 
       : "memory");
 }
 
+// The same, with a second commit to `bar2` when `second` is non-zero (one elect for the group).
+__device__ __forceinline__ void mma_f8f6f4_ts_k64_commit2_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                                uint64_t bdesc, uint32_t idesc,
+                                                                uint32_t accumulate, uint32_t bar,
+                                                                uint32_t second, uint32_t bar2) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1, r;\n\t.reg .b64 b1;\n\t.reg .b32 a1;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\tsetp.ne.b32 r, %6, 0;\n\t"
+      "add.s32 a1, %1, 8;\n\tadd.s64 b1, %2, 2;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %3, p1;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+      "and.pred r, r, e;\n\t"
+      "@r tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(bar), "r"(second),
+        "r"(bar2)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"

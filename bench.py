@@ -57,12 +57,12 @@ METRICS = {"fp8": METRIC, "nvfp4": METRIC_NVFP4, "sparse": METRIC_SPARSE}
 # an ncu capture of the full-size workload (profiles/attn_traffic_s30272_h56.md), keyed by the
 # workload and the SHA-256 of the kernel source at capture time (null once the kernel changed).
 NCU_TRAFFIC = {
-    ("fp8_s30272_h56", "c4d859e722b16da15611b2f7a0ceda46cc94bd070c1a0281cc76db9cdfa00ac7"):
-        1.9135e9 + 425.66e6,
+    ("fp8_s30272_h56", "5c4e3acaebf498a7c336d8f98dcaaaef96b865c581cd664f3f3468fe2e8fffc0"):
+        2.0026e9 + 425.68e6,
     ("nvfp4_s30272_h56", "e7f2ad5fa8c60b71cd10034706bba0bb74db700231839eafe8aa09d55506567b"):
         2.3446e9 + 424.98e6,
-    ("sparse_fp8_s30272_h56", "d2d6614eace3c46dbd23531dc472ff5480646146b4c97f8a33a0c740d2a874f7"):
-        1.5350e9 + 425.51e6,
+    ("sparse_fp8_s30272_h56", "42c9279ec4b825fa00ada438e6df1573acb500021fc931519873dd5697e6a54b"):
+        1.5510e9 + 425.50e6,
 }
 
 

@@ -279,7 +279,8 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
  *                     holds the result. Returns after enqueueing.
  * Device memory: two chunk slots of Q, K, V and output (8 x tokens x (largest chunk) x 256
  * bytes), allocated on the first call (or a call with another heads_per_chunk) and kept by the
- * plan, plus plans of the chunk sizes (cached like any plan). Device-side wait
+ * plan, plus plans of the chunk sizes (cached like any plan; each call gives them this plan's
+ * NVFP4 table limit, see fa_lp_plan_set_table_limit). Device-side wait
  * expiries are reported by fa_lp_get_last_error on this plan. A plan must not run this call
  * from two host threads at once.
  * Errors: INVALID_ARG (null or misaligned view, heads_per_chunk out of range, wrong device),

@@ -920,8 +920,12 @@ int host_pipeline(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const 
       return FA_LP_ERR_CUDA;
     }
   }
-  for (fa_lp_plan* sp : hp.sub)
-    if (sp) sp->spin_limit = p->spin_limit;
+  for (fa_lp_plan* sp : hp.sub) {
+    if (!sp) continue;
+    sp->spin_limit = p->spin_limit;
+    // the chunk plans hold the NVFP4 table under the caller's limit (a no-op when unchanged)
+    if ((st = fa_lp_plan_set_table_limit(sp, p->tbl_limit)) != FA_LP_OK) return st;
+  }
   const size_t tb = size_t(T) * size_t(hp.maxn) * FA_LP_HEAD_DIM * 2;  // one tensor of one slot
   uint8_t* base = static_cast<uint8_t*>(hp.buf);
   auto dev = [&](int slot, int which) { return base + (size_t(slot) * 4 + which) * tb; };

@@ -51,6 +51,32 @@ def test_host_entry_equals_device_call(fa, mode):
     assert plan.last_error() == 0
 
 
+def test_host_entry_nvfp4_under_a_table_limit(fa):
+    """NVFP4 through the host entry with the plan's qm K^T table limited to one head per slot: the
+    chunk plans take the limit (their tables become rings of one-head slots) and the result still
+    equals the whole-table device call bit for bit."""
+    T, H = 1500, 6
+    cu = [0, 17, 700, 1500]
+    buf = fused_host(T, H, seed=33)
+    plan = fa.Plan(cu, H, mode=1)
+    ref = device_reference(fa, plan, buf)
+    head_bytes = sum(((b - a + 127) // 128) ** 2 for a, b in zip(cu[:-1], cu[1:])) * 128 * 4
+    try:
+        plan.set_table_limit(2 * head_bytes)
+        for nh in (0, 3):
+            out = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+            plan.attention_host(buf[:, 0], buf[:, 1], buf[:, 2], out, heads_per_chunk=nh)
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"heads_per_chunk={nh}"
+            sub = fa.Plan(cu, 3, mode=1)  # the 3-head chunk plan (from the plan cache)
+            if nh == 3:
+                assert sub.table_layout() == dict(heads_per_slot=1, slots=2, slot_bytes=head_bytes)
+        assert plan.last_error() == 0
+    finally:
+        plan.set_table_limit(0)
+        fa.Plan(cu, 3, mode=1).set_table_limit(0)
+
+
 def test_host_entry_pageable_memory_and_strided_output(fa):
     T, H = 900, 5
     cu = [0, 300, 301, 900]

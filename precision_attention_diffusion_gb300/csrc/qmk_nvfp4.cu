@@ -64,20 +64,30 @@ __device__ __forceinline__ float e4m3f(uint32_t code) {
   return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
 }
 
-// B tile of N tile nt into buffer b: rows kr = keys nt * 256 + kr of the segment (one key per
-// thread), dequantized to BF16 (exact); keys past the segment are zero.
-__device__ __forceinline__ void build_b(QmkSmem& S, int b, int nt, int kr, int64_t row0,
-                                        int lp, const uint8_t* __restrict__ kcodes,
-                                        const uint8_t* __restrict__ ksf) {
+// The codes and scale record of key nt * 256 + kr of the segment (one key per thread); zero past
+// the segment. Loaded a tile ahead, so that their latency hides behind the current tile's store.
+struct KeyRec {
+  uint4 cw[4];
+  uint2 sw;
+};
+__device__ __forceinline__ KeyRec load_key(int nt, int kr, int64_t row0, int lp,
+                                           const uint8_t* __restrict__ kcodes,
+                                           const uint8_t* __restrict__ ksf) {
+  KeyRec r = {};
   const int key = nt * kNKeys + kr;
-  uint4 cw[4] = {};
-  uint2 sw = make_uint2(0u, 0u);
   if (key < lp) {
     const uint4* src = reinterpret_cast<const uint4*>(kcodes + (row0 + key) * 64);
 #pragma unroll
-    for (int x = 0; x < 4; ++x) cw[x] = src[x];
-    sw = *reinterpret_cast<const uint2*>(ksf + (row0 + key) * 8);
+    for (int x = 0; x < 4; ++x) r.cw[x] = src[x];
+    r.sw = *reinterpret_cast<const uint2*>(ksf + (row0 + key) * 8);
   }
+  return r;
+}
+
+// B tile row kr in buffer b from that key's record, dequantized to BF16 (exact).
+__device__ __forceinline__ void build_b(QmkSmem& S, int b, int kr, const KeyRec& k) {
+  const uint4 (&cw)[4] = k.cw;
+  const uint2 sw = k.sw;
   const uint32_t words[16] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y,
                               cw[1].z, cw[1].w, cw[2].x, cw[2].y, cw[2].z, cw[2].w,
                               cw[3].x, cw[3].y, cw[3].z, cw[3].w};
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
             make_uint4(w[p][0], w[p][1], w[p][2], w[p][3]);
     }
   }
-  if (it.ntiles > 0) build_b(S, 0, it.nt, i, krow0, lp, kcodes, ksf);
+  if (it.ntiles > 0) build_b(S, 0, i, load_key(it.nt, i, krow0, lp, kcodes, ksf));
   fence_proxy_async_smem();
   // the barrier after the A / first B build publishes the tensor-memory base
   tc_fence_before();
@@ -229,6 +239,9 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
   for (int n = 0; n < it.ntiles && ok; ++n) {
     issue(n & 1);  // B tile n is built and visible (barrier at the end of the previous step)
     issued = n + 1;
+    // the next tile's key record, in flight during the wait and the store below
+    const KeyRec next = n + 1 < it.ntiles ? load_key(it.nt + n + 1, i, krow0, lp, kcodes, ksf)
+                                          : KeyRec{};
     if (n > 0) {
       if (!(ok = wait_tile(n - 1))) break;
       tc_fence_after();
@@ -237,7 +250,7 @@ __global__ void __launch_bounds__(kQmkThreads, 1) nvfp4_qmk_kernel(
     }
     if (n + 1 < it.ntiles) {
       // buffer (n + 1) & 1 was last read by the MMAs of tile n - 1, finished above
-      build_b(S, (n + 1) & 1, it.nt + n + 1, i, krow0, lp, kcodes, ksf);
+      build_b(S, (n + 1) & 1, i, next);
       fence_proxy_async_smem();
     }
     // B tile n + 1 visible to the MMA issuer; accumulator (n + 1) & 1 (tile n - 1) fully read

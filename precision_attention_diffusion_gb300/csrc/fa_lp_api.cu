@@ -487,7 +487,6 @@ void layout_work_and_workspace(fa_lp_plan* p) {
         run = r;
       }
     }
-    p->qmk_run = run;
     for (int s = 0; s < ns; ++s) {
       const int64_t nb = p->segs[s].nblk;
       p->c_off[s] = int64_t(floats);

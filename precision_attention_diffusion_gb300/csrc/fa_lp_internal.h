@@ -119,7 +119,6 @@ struct fa_lp_plan {
   size_t tbl_slot_floats = 0;
   size_t tbl_limit = 0;                          // bytes; 0 = the library default
   std::vector<int32_t> tbl_work_off;
-  int qmk_run = 0;                               // N tiles per table CTA
   cudaStream_t tbl_stream[2] = {nullptr, nullptr};  // ring forward: one stream per slot
   cudaEvent_t tbl_fork = nullptr;
   cudaEvent_t tbl_join[2] = {nullptr, nullptr};

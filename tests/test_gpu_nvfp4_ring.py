@@ -116,3 +116,29 @@ def test_ring_equals_whole_table_h3_shape(fa):
         assert plan.last_error() == 0
     finally:
         plan.set_table_limit(0)
+
+
+def test_ring_device_wait_limit_returns_error_not_hang(fa):
+    """A wait limit of one probe in ring mode: the launches of the head groups on the two internal
+    streams report the expiry through the plan's error word (0x100 | role), nothing hangs, and a
+    correct ring run follows on the same plan."""
+    cu, H = [0, 640], 3
+    q, k, v = inputs.qkv_separate(640, H, seed=23)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    plan = fa.Plan(cu, H, mode=fa.MODE_NVFP4)
+    try:
+        ref_out, ref_lse = run(fa, plan, q, k, v, 640, H)
+        plan.set_table_limit(2 * head_table_bytes(cu))
+        assert plan.table_layout()["slots"] == 2
+        plan.last_error()  # clear
+        plan.set_wait_limit(1)
+        run(fa, plan, q, k, v, 640, H)
+        status = plan.last_error()
+        assert status != 0 and (status & 0xFF00) == 0x100
+        plan.set_wait_limit(20000)
+        out, lse = run(fa, plan, q, k, v, 640, H)
+        assert plan.last_error() == 0
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    finally:
+        plan.set_wait_limit(20000)
+        plan.set_table_limit(0)

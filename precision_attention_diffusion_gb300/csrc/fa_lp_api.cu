@@ -181,11 +181,36 @@ cudaError_t copy_heads(void* dst, int64_t dst_st, int64_t dst_sh, const void* sr
   return cudaSuccess;
 }
 
+// Device address of a page-locked host view the current device can read directly, or nullptr
+// (pageable memory, device memory, or a view not 16-byte aligned in its base and strides).
+const void* device_mapping(const void* host, int64_t st, int64_t sh) {
+  if ((reinterpret_cast<uintptr_t>(host) & 15) != 0 || (st * 2) % 16 != 0 || (sh * 2) % 16 != 0)
+    return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Copy-in of one tensor of a chunk: a 2D DMA copy, or, for the first chunk (whose copy-in no
+// compute overlaps) from page-locked memory, the gather kernel, which is not slowed by the DMA
+// engine's per-row cost.
+cudaError_t copy_in(void* dst, const void* src, int64_t st, int64_t sh, int64_t T, int n,
+                    bool gather, cudaStream_t s) {
+  const void* d = gather ? device_mapping(src, st, sh) : nullptr;
+  if (d) return falp::launch_gather_heads(dst, d, st, sh, T, n, s) == FA_LP_OK ? cudaSuccess
+                                                                              : cudaErrorUnknown;
+  return copy_heads(dst, int64_t(n) * FA_LP_HEAD_DIM, FA_LP_HEAD_DIM, src, st, sh, T, n,
+                    cudaMemcpyHostToDevice, s);
+}
+
 // Chunks of heads for the host-buffer pipeline: equal chunks (the last may be shorter) of
 // heads_per_chunk heads, or, when the caller leaves it open, of the size that gives 4 to 8 chunks
 // whose CTAs fill the GPU's waves best (ties: more chunks, so that the first copy-in and the last
 // copy-out, which nothing overlaps, are shorter).
-std::vector<int> host_schedule(const fa_lp_plan& p, int heads_per_chunk) {
+std::vector<int> host_schedule(const fa_lp_plan& p, int heads_per_chunk, bool sparse) {
   const int H = p.heads;
   int nh = heads_per_chunk;
   if (nh <= 0) {
@@ -218,10 +243,14 @@ std::vector<int> host_schedule(const fa_lp_plan& p, int heads_per_chunk) {
   }
   std::vector<int> out;
   if (heads_per_chunk <= 0 && nh >= 2 && H >= 3 * nh) {
-    // the library's choice: half-size first and last chunks, whose copy-in and copy-out nothing
-    // overlaps; a half chunk computes about as long as a full chunk's copy-in takes (the copies
-    // move a head in about half the time its compute takes), so the pipeline does not stall
-    const int first = (nh + 1) / 2;
+    // the library's choice: a short first chunk, whose copy-in nothing overlaps, then chunks of
+    // nh, the last one the remainder (its copy-out overlaps nothing either). The first chunk
+    // computes about as long as the next chunk's copy-in takes: half a chunk for NVFP4 and the
+    // block-sparse forward; for the dense FP8 forward, which computes a head in ~0.22 ms while a
+    // 14-head chunk's DMA copy-in moves one in ~0.15 ms, two thirds of a chunk (at S=30272,
+    // H=56: [9, 14, 14, 14, 5], median host-entry step 14.00 ms against 14.25 ms for
+    // [7, 14, 14, 14, 7])
+    const int first = (falp::is_fp8(p) && !sparse) ? (2 * nh + 1) / 3 : (nh + 1) / 2;
     int rest = H - first;
     out.push_back(first);
     while (rest > nh) {
@@ -878,13 +907,14 @@ int host_pipeline(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const 
   const int H = p->heads;
   const int64_t T = p->tokens;
   falp::HostPipe& hp = p->host;
-  if (hp.key != heads_per_chunk) {  // (re)build the pipeline for this chunking
+  const int key = 2 * heads_per_chunk + (lists ? 1 : 0);
+  if (hp.key != key) {  // (re)build the pipeline for this chunking
     fa_lp_plan* old[4] = {nullptr, nullptr, nullptr, nullptr};
     st = host_pipe_release(p, old);
     for (fa_lp_plan* sp : old)
       if (sp) fa_lp_plan_destroy(sp);
     if (st != FA_LP_OK) return st;
-    hp.sizes = host_schedule(*p, heads_per_chunk);
+    hp.sizes = host_schedule(*p, heads_per_chunk, lists != nullptr);
     hp.maxn = *std::max_element(hp.sizes.begin(), hp.sizes.end());
     const size_t bytes = size_t(8) * size_t(T) * size_t(hp.maxn) * FA_LP_HEAD_DIM * 2;
     if (cudaMalloc(&hp.buf, bytes) != cudaSuccess) {
@@ -910,7 +940,7 @@ int host_pipeline(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const 
       ok = ok && hp.sub[nsub] != p;
       hp.sub_n[nsub++] = n;
     }
-    hp.key = heads_per_chunk;
+    hp.key = key;
     if (!ok) {
       cudaGetLastError();
       host_pipe_release(p, old);
@@ -985,13 +1015,11 @@ int host_pipeline(fa_lp_plan* p, const void* q, int64_t qst, int64_t qsh, const 
     const uint8_t* hv = static_cast<const uint8_t*>(v) + size_t(h0) * vsh * 2;
     uint8_t* ho = static_cast<uint8_t*>(out) + size_t(h0) * osh * 2;
     // copy-in of chunk c once the quantize of chunk c - 2 has consumed the slot
+    const bool gather = c == 0;
     bool good = (c < 2 || ok_(cudaStreamWaitEvent(hp.s_in, hp.in_free[slot], 0))) &&
-                ok_(copy_heads(dev(slot, 0), dst, dsh, hq, qst, qsh, T, n,
-                               cudaMemcpyHostToDevice, hp.s_in)) &&
-                ok_(copy_heads(dev(slot, 1), dst, dsh, hk, kst, ksh, T, n,
-                               cudaMemcpyHostToDevice, hp.s_in)) &&
-                ok_(copy_heads(dev(slot, 2), dst, dsh, hv, vst, vsh, T, n,
-                               cudaMemcpyHostToDevice, hp.s_in)) &&
+                ok_(copy_in(dev(slot, 0), hq, qst, qsh, T, n, gather, hp.s_in)) &&
+                ok_(copy_in(dev(slot, 1), hk, kst, ksh, T, n, gather, hp.s_in)) &&
+                ok_(copy_in(dev(slot, 2), hv, vst, vsh, T, n, gather, hp.s_in)) &&
                 ok_(cudaEventRecord(hp.in_done[slot], hp.s_in)) &&
                 ok_(cudaStreamWaitEvent(stream, hp.in_done[slot], 0));
     if (!good) {

@@ -76,7 +76,8 @@ struct WsLayout {
 
 // State of the host-buffer entry point (fa_lp_attention_host): head-chunk pipeline.
 struct HostPipe {
-  int key = -1;                               // heads_per_chunk the pipeline was built for
+  int key = -1;                               // 2 heads_per_chunk + (block-sparse call) it was
+                                              // built for
   std::vector<int> sizes;                     // heads of each chunk, in order
   int maxn = 0;                               // largest chunk
   fa_lp_plan* sub[4] = {nullptr, nullptr, nullptr, nullptr};  // plans of the chunk sizes
@@ -175,6 +176,10 @@ int launch_nvfp4_attention(const fa_lp_plan& p, uint8_t* ws, int g, void* out, i
 int launch_fp8_sparse(const fa_lp_plan& p, uint8_t* ws, const int32_t* block_offsets,
                       const int32_t* block_indices, int64_t num_indices, void* out, int64_t ost,
                       int64_t osh, float* lse, int64_t lse_sh, cudaStream_t stream);
+// Dense [T][n][128] BF16 copy of n heads of a [T, H, 128] view (element strides st, sh) whose
+// memory the device can read (`src_dev`: page-locked host memory through its device mapping).
+int launch_gather_heads(void* dst, const void* src_dev, int64_t src_st, int64_t src_sh,
+                        int64_t T, int n, cudaStream_t stream);
 // The qm K^T table of table group g's heads into slot g % tbl_slots.
 int launch_nvfp4_qmk(const fa_lp_plan& p, uint8_t* ws, int g, cudaStream_t stream);
 int launch_encode(int format, const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);

@@ -270,13 +270,17 @@ FA_LP_API int fa_lp_attention(fa_lp_plan* plan, const void* q, int64_t q_stride_
  *                     (all tokens lie in a segment) is written. Caller-owned.
  *   heads_per_chunk : 1..heads for chunks of that many heads (the last may be shorter), or 0 for
  *                     the library's choice: the size n giving 4 to 8 chunks whose CTAs fill the
- *                     GPU's waves best (1-head chunks when heads < 4), with the first chunk of
- *                     ceil(n / 2) heads and the rest of n (the last takes what remains) when
- *                     heads >= 3 n.
+ *                     GPU's waves best (1-head chunks when heads < 4), with a shorter first
+ *                     chunk and the rest of n (the last takes what remains) when heads >= 3 n:
+ *                     the first chunk has round(2 n / 3) heads for the FP8 modes, ceil(n / 2)
+ *                     for NVFP4 (and in fa_lp_attention_sparse_host).
  *   stream          : the quantize and attention kernels run on it; the copies run on two
  *                     streams of the plan, ordered after the work already on `stream`, and
  *                     `stream` is ordered after the last copy-out: once `stream` completes, `out`
- *                     holds the result. Returns after enqueueing.
+ *                     holds the result. The first chunk's copy-in from page-locked views is a
+ *                     gather kernel reading them through their device mapping (a 2D DMA copy
+ *                     pays a fixed cost per token row); the other copies are DMA copies.
+ *                     Returns after enqueueing.
  * Device memory: two chunk slots of Q, K, V and output (8 x tokens x (largest chunk) x 256
  * bytes), allocated on the first call (or a call with another heads_per_chunk) and kept by the
  * plan, plus plans of the chunk sizes (cached like any plan; each call gives them this plan's

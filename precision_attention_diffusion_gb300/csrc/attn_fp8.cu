@@ -169,6 +169,8 @@ __device__ __forceinline__ void producer(const CUtensorMap* tm_q, const CUtensor
   if (wi.nq == 2)
     tma_load_3d_elect(smem_u32(S.q[1]), tm_q, smem_u32(&S.bar_q), 0, rq + kTile, wi.head);
   int issued = 0;
+  // two stages per iteration (see the sub-tile loops)
+#pragma unroll 2
   for (int j = 0; j < n_kv; ++j) {
     const int st = j % kStages;
     if (j >= kStages &&
@@ -232,6 +234,8 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const AttnArgs& a, const Wor
     issue_s(0);
     if (n_sub > 1) issue_s(1);  // sub-tile 1 lies in key tile 0 as well
     bool ok = true;
+    // two sub-tiles per iteration: the buffer and barrier parities become constants of each copy
+#pragma unroll 2
     for (int u = 0; u < n_sub && ok; ++u) {
       const int h = u & 1;
       // the stage's V^T landed with its K, waited for before S of its first sub-tile
@@ -274,6 +278,8 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const AttnArgs& a,
   const int last_valid = sg.len - (n_sub - 1) * kSub;  // keys of the last sub-tile, 1..64
   float m = -INFINITY, l = 0.f;                         // reference maximum, this half's sum
   bool ok = true;
+  // two sub-tiles per iteration: the buffer and barrier parities become constants of each copy
+#pragma unroll 2
   for (int u = 0; u < n_sub; ++u) {
     const int b = u & 1;
     const uint32_t s_addr = tmem + col_s(t, b) + lane_off;

@@ -307,6 +307,8 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const SpArgs& a, uint32_t tm
       issue_s(1);
     }
     bool ok = true;
+    // two sub-tiles per iteration: the buffer and barrier parities become constants of each copy
+#pragma unroll 2
     for (int u = 0; u < n && ok; ++u) {
       // V(u) landed with K(u), waited for before S(u)
       ok = wait(&S.bar_p[t][u & 1], (u >> 1) & 1);
@@ -345,6 +347,8 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const SpArgs& a, c
   float m = -INFINITY, l = 0.f;
   bool started = false, ok = true;
   uint32_t e_next = n > 0 ? __ldg(ent) : 0u;
+  // two sub-tiles per iteration: the buffer and barrier parities become constants of each copy
+#pragma unroll 2
   for (int u = 0; u < n; ++u) {
     const uint32_t e = e_next;
     if (u + 1 < n) e_next = __ldg(ent + u + 1);

@@ -57,12 +57,12 @@ METRICS = {"fp8": METRIC, "nvfp4": METRIC_NVFP4, "sparse": METRIC_SPARSE}
 # an ncu capture of the full-size workload (profiles/attn_traffic_s30272_h56.md), keyed by the
 # workload and the SHA-256 of the kernel source at capture time (null once the kernel changed).
 NCU_TRAFFIC = {
-    ("fp8_s30272_h56", "5c4e3acaebf498a7c336d8f98dcaaaef96b865c581cd664f3f3468fe2e8fffc0"):
-        2.0026e9 + 425.68e6,
-    ("nvfp4_s30272_h56", "e7f2ad5fa8c60b71cd10034706bba0bb74db700231839eafe8aa09d55506567b"):
-        2.3446e9 + 424.98e6,
-    ("sparse_fp8_s30272_h56", "42c9279ec4b825fa00ada438e6df1573acb500021fc931519873dd5697e6a54b"):
-        1.5510e9 + 425.50e6,
+    ("fp8_s30272_h56", "b3ad149c12b4ac4340efe7ccee09fa7e91263d2f081840ce7168a8d83d44c52b"):
+        2.0465e9 + 425.72e6,
+    ("nvfp4_s30272_h56", "fe743e38f6d1c9f9a8e91591a2c17999b205748f0371e8ce44ed30d67b9d1c99"):
+        2.3485e9 + 425.04e6,
+    ("sparse_fp8_s30272_h56", "eb658a222e5667e01266b4c38d660a59a787924fe699ae2e50be04b6dc2433b8"):
+        1.5226e9 + 425.39e6,
 }
 
 

@@ -312,8 +312,8 @@ __device__ __forceinline__ void mma_issuer(Smem& S, const Nvfp4Args& a, const Wo
     if (!wait(&S.bar_q, 0)) break;
     if (!wait(&S.bar_qsf[t], 0)) break;
     bool ok = true;
-    // two sub-tiles per iteration: the buffer and barrier parities become constants of each copy
-#pragma unroll 2
+    // four sub-tiles per iteration: the slot and barrier parities become constants of each copy
+#pragma unroll 4
     for (int u = 0; u <= n_sub && ok; ++u) {
       if (u < n_sub) {
         // the auxiliary warp's blocks of u (written after the stage of u landed; the auxiliary
@@ -437,8 +437,8 @@ __device__ __forceinline__ void softmax_and_epilogue(Smem& S, const Nvfp4Args& a
   const uint32_t s_addr = tmem + col_s(t) + lane_off;
   float m = -INFINITY;  // running maximum (log2 units)
   bool ok = true;
-  // two sub-tiles per iteration: the buffer and barrier parities become constants of each copy
-#pragma unroll 2
+  // four sub-tiles per iteration: the slot and barrier parities become constants of each copy
+#pragma unroll 4
   for (int u = 0; u < n_sub; ++u) {
     if (!(ok = wait_hinted(&S.bar_s[t], uint32_t(u) & 1, S, a, kRoleSoftmax))) break;
     tc_fence_after();

@@ -59,8 +59,8 @@ METRICS = {"fp8": METRIC, "nvfp4": METRIC_NVFP4, "sparse": METRIC_SPARSE}
 NCU_TRAFFIC = {
     ("fp8_s30272_h56", "b3ad149c12b4ac4340efe7ccee09fa7e91263d2f081840ce7168a8d83d44c52b"):
         2.0465e9 + 425.72e6,
-    ("nvfp4_s30272_h56", "fe743e38f6d1c9f9a8e91591a2c17999b205748f0371e8ce44ed30d67b9d1c99"):
-        2.3485e9 + 425.04e6,
+    ("nvfp4_s30272_h56", "c3f77846df62152f8a18889af84af063ae7a19782cc4cdcdcdd69a12ccbcfcb0"):
+        2.2708e9 + 425.24e6,
     ("sparse_fp8_s30272_h56", "eb658a222e5667e01266b4c38d660a59a787924fe699ae2e50be04b6dc2433b8"):
         1.5226e9 + 425.39e6,
 }

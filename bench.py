@@ -618,7 +618,7 @@ def run_arm(args, name, ws, rank, with_e2e, with_cpu):
 EXTRA_ARMS = (("nvfp4", "nvfp4_s30272_h56"), ("sparse", "sparse_fp8_s30272_h56"))
 ARM_KEYS = ("metric", "value", "unit", "ms_per_step", "forward_ms", "forward_tflops",
             "quantize_ms", "quantize_gbs", "roofline", "clocks", "gpu_launches", "config", "dtype",
-            "table_ring")
+            "table_ring", "e2e")
 
 
 def run_ours(args):
@@ -639,7 +639,7 @@ def run_ours(args):
                    with_cpu=rank == 0 and ws == 1 and not args.no_cpu_baseline)
     if args.workload == "fp8_s30272_h56" and not args.no_extra_arms:
         for key, name in EXTRA_ARMS:
-            sub = run_arm(args, name, ws, rank, with_e2e=False, with_cpu=False)
+            sub = run_arm(args, name, ws, rank, with_e2e=not args.no_e2e, with_cpu=False)
             line[key] = {k: sub[k] for k in ARM_KEYS if k in sub}
     if rank == 0:
         print(json.dumps(line))
